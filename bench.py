@@ -1,0 +1,503 @@
+#!/usr/bin/env python3
+"""Benchmark of the ds4 layer step on one GB300 (or N independent replicas).
+
+Headline: batch-1 decode tok/s of one full-width layer (hidden 4096, 64 x 128 MQA over a
+128-token window, 256 experts top-6 + shared expert, BF16 weights and KV, KV pre-filled
+with 4096 seeded positions): each step is one token through the whole layer step.  The
+same JSON line carries layer-major prefill tok/s (8 layers, 4096 tokens), stack decode
+tok/s with lm_head + top-p sampling (8 layers), and the common-prefix resync latency
+(16994 live -> 16846 common -> 91-token suffix), each with its roofline.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+
+
+# --------------------------------------------------------------------------- workload facts
+
+def layer_bytes(m: synth.ModelShape) -> dict:
+    """Algorithmic bytes per decode-step launch of each kernel (weights streamed once,
+    the K/V window and activations counted)."""
+    H, QD, RQ, RKV, HD = m.hidden, m.n_heads * m.head_dim, m.q_rank, m.kv_rank, m.head_dim
+    E, K, I, W = m.n_experts, m.top_k, m.expert_inter, m.window
+    w = 2  # bf16
+    return {
+        "qkv_a": (RQ + RKV) * H * w + H * 4 + (RQ + RKV) * 4,
+        "qkv_b": (QD * RQ + 2 * HD * RKV) * w + (RQ + RKV) * 4 + QD * 4 + 2 * HD * w,
+        "attn": 2 * W * HD * w + 2 * QD * 4,
+        "wo": H * QD * w + QD * 4 + 2 * H * 4,
+        "router": E * H * w + 2 * H * 4 + E * 4,
+        "expert_gu": (K + 1) * 2 * I * H * w + H * 4 + (K + 1) * I * 4,
+        "expert_down": (K + 1) * H * I * w + (K + 1) * I * 4 + 2 * H * 4,
+    }
+
+
+def lm_head_bytes(m):
+    return m.vocab * m.hidden * 2 + m.hidden * 4 + m.vocab * 4
+
+
+def prefill_flops_per_token_layer(m) -> float:
+    H, QD, RQ, RKV, HD = m.hidden, m.n_heads * m.head_dim, m.q_rank, m.kv_rank, m.head_dim
+    E, K, I, W = m.n_experts, m.top_k, m.expert_inter, m.window
+    mac = (H * (RQ + RKV) + RQ * QD + RKV * 2 * HD + QD * H + H * E
+           + (K + 1) * (2 * H * I + I * H)) + 2 * m.n_heads * W * HD
+    return 2.0 * mac
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), \
+            "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, 1700.0, "fallback"
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "prefill_decode_layer_gb300", "csrc", "decode.cu")
+    try:
+        digest = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+        for line in open(path):
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel and parts[1] == digest:
+                return int(float(parts[2]))
+    except OSError:
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- helpers
+
+def nproc():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_decode_rate(m: synth.ModelShape, n_pre: int, seconds: float, seed: int = 0):
+    """Oracle decode steps/s on the single-layer workload (one thread), bounded by time."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from helpers import LazyOracleModel, OracleKV, oracle_embed, oracle_layer
+    om = LazyOracleModel(m.with_(n_layers=1), seed)
+    om.layer(0)                                   # generate weights outside the timing
+    kv = OracleKV(m.with_(n_layers=1), n_pre + 256)
+    hk, hv = synth.host_kv(m, 0, n_pre, seed)
+    kv.k[0][:n_pre] = hk
+    kv.v[0][:n_pre] = hv
+    toks = synth.host_tokens(256, m.vocab, seed, stream=5)
+    t0 = time.perf_counter()
+    n = 0
+    while n < 256:
+        x = oracle_embed(om, toks[n])
+        oracle_layer(om, kv, 0, n_pre + n, x)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    del oracle
+    return n / dt, n, dt
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args) -> dict:
+    secs = float(os.environ.get("DS4G_REF_SECONDS", "40"))
+    m = synth.LAYER
+    # every step is one oracle decode step of the same workload; the run is bounded in time
+    budget_steps = args.warmup + args.steps
+    rate, n, dt = oracle_decode_rate(m, 4096, secs)
+    value = rate
+    return {
+        "metric": "decode tok/s (batch 1)", "value": value, "unit": "tok/s", "n_gpus": 0,
+        "steps": n, "warmup": 0, "ms_per_step": 1000.0 / value, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": workload_config(m),
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} of the requested {budget_steps} oracle decode steps "
+                                   f"(positions 4096.., {dt:.1f} s, single thread, "
+                                   f"{cpu_model()}, {nproc()} cores present)"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def workload_config(m):
+    return {"workload": "decode_layer: 1 layer, hidden 4096, 64x128 MQA (1 KV head), q/kv "
+                        "rank 1024/512, window 128, 256 experts top-6 + shared (inter 1024), "
+                        "BF16 weights ~N(0,0.02), BF16 KV pre-filled with 4096 seeded N(0,1) "
+                        "positions, batch 1, random token ids",
+            "global_batch": 1, "kv_prefill": 4096, "l2": "flushed (512 MB write) between steps",
+            "parallelism": "replicas"}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the prefill / stack / resync measurements")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    import prefill_decode_layer_gb300 as pdl
+    from synth import torch_weights as tw
+
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
+    stack = synth.STACK
+    layer = synth.LAYER
+    extra = not args.no_extra and rank == 0
+    n_layers_alloc = stack.n_layers if extra else 1
+    emb = tw.dev_embedding(stack)
+    lm = tw.dev_lm_head(stack)
+    layers = [tw.dev_layer(stack, l) for l in range(n_layers_alloc)]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # ---------------- headline: single full-width decode layer at batch 1
+    m1 = pdl.Model(layer, emb, lm, layers[:1])
+    n_pre = 4096
+    n_ctx = n_pre + args.warmup + args.steps + 64
+    sess = pdl.Session(m1, n_ctx)
+    k, v = sess.kv(0)
+    tw.fill_kv(layer, 0, k, v, n_pre)
+    assert sess.restore(synth.host_tokens(n_pre, layer.vocab, stream=11)) == 0
+    toks = synth.host_tokens(args.warmup + args.steps + 64, layer.vocab, stream=5)
+    for i in range(args.warmup):
+        flush.zero_()
+        assert sess.decode(int(toks[i])) == 0
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = sess.launches
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        rc = sess.decode(int(toks[args.warmup + i]))
+        ev[i][1].record(stream)
+        if rc != 0:
+            raise RuntimeError(f"decode failed: {rc}")
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    gpu_launches = sess.launches - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * args.steps / (total_ms / 1000.0)
+    ms_per_step = total_ms / args.steps
+
+    # per-kernel timing pass (events between kernels) for the dominant kernel's roofline
+    sess.set_timing(True)
+    sess.timing()
+    base = args.warmup + args.steps
+    for i in range(48):
+        flush.zero_()
+        assert sess.decode(int(toks[(base + i) % len(toks)])) == 0
+    kt = sess.timing()
+    sess.set_timing(False)
+    lb = layer_bytes(layer)
+    per_kernel = {}
+    for kname, (ms, cnt) in kt.items():
+        if cnt and kname in lb:
+            avg = ms / cnt
+            per_kernel[kname] = {"avg_us": round(avg * 1000, 2),
+                                 "gbs": round(lb[kname] / (avg / 1000) / 1e9, 1)}
+    dom = max((k for k in per_kernel if k in lb), key=lambda k: kt[k][0])
+    dom_avg_s = kt[dom][0] / kt[dom][1] / 1000.0
+    achieved = lb[dom] / dom_avg_s / 1e9
+    traffic = ncu_traffic(dom)
+    roofline = {"kernel": f"decode {dom}", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "peak_source": f"{peak_src} hbm_gbs (copy, read+write)",
+                "traffic": traffic, "algorithmic_bytes": lb[dom],
+                "timing": "per-kernel CUDA events (timing mode), L2 flushed between steps"}
+    step_bytes = sum(lb.values())
+    step_roof = {"bound": "hbm", "bytes_per_step": step_bytes,
+                 "achieved": round(step_bytes / (ms_per_step / 1000) / 1e9, 1),
+                 "peak": hbm_peak, "unit": "GB/s",
+                 "frac": round(step_bytes / (ms_per_step / 1000) / 1e9 / hbm_peak, 4),
+                 "per_kernel": per_kernel}
+
+    # ---------------- end to end through the C ABI with host buffers
+    hidden_host = torch.empty(layer.hidden, dtype=torch.float32, pin_memory=True)
+    tok_host = torch.tensor(toks[:64].astype(np.int32), dtype=torch.int32).pin_memory()
+    x_dev = sess.debug("x", layer.hidden)
+    e2e_ms = []
+    for i in range(32):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        rc = sess.decode(int(tok_host[i].item()))
+        hidden_host.copy_(x_dev, non_blocking=True)
+        stream.synchronize()
+        e2e_ms.append((time.perf_counter() - t0) * 1000)
+        assert rc == 0
+    e2e = {"value": round(1000.0 / statistics.mean(e2e_ms) * world, 1), "unit": "tok/s",
+           "h2d_bytes_per_step": 4, "d2h_bytes_per_step": layer.hidden * 4,
+           "how": "host wall clock per step: decode call with the token from pinned host "
+                  "memory, hidden state copied back to pinned host memory, stream synchronised"}
+    del sess, m1
+
+    line = {
+        "metric": "decode tok/s (batch 1)", "value": round(value, 1), "unit": "tok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator)",
+        "config": workload_config(layer), "roofline": roofline, "step_roofline": step_roof,
+        "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clk,
+    }
+
+    if extra:
+        line.update(extra_measurements(pdl, tw, torch, stack, emb, lm, layers, flush, hbm_peak,
+                                       bf16_peak, bf16_sus))
+
+    if rank == 0:
+        rate, n, dt = oracle_decode_rate(layer, n_pre, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(rate, 4), "unit": "tok/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{n} oracle decode steps of the same layer at positions "
+                                          f"4096.. ({dt:.1f} s, single thread, {cpu_model()}, "
+                                          f"{nproc()} cores present)"}
+        print(json.dumps(line), flush=True)
+    barrier()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def extra_measurements(pdl, tw, torch, stack, emb, lm, layers, flush, hbm_peak, bf16_peak,
+                       bf16_sus):
+    out = {}
+    model = pdl.Model(stack, emb, lm, layers)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+
+    # layer-major prefill: 8 layers x 4096 tokens
+    toks = synth.host_tokens(4096, stack.vocab, stream=31)
+    sess = pdl.Session(model, 4200)
+    times = []
+    for rep in range(3):
+        assert sess.truncate(0) == 0
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        assert sess.prefill(toks) == 0
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if rep > 0:
+            times.append(ev0.elapsed_time(ev1) / 1000.0)
+    t = min(times)
+    flops = prefill_flops_per_token_layer(stack) * 4096 * stack.n_layers
+    wbytes = sum(np.prod(s) for _, k, s, sg in synth.layer_tensors(stack) if sg) * 2 * stack.n_layers
+    out["prefill"] = {
+        "metric": "prefill tok/s", "value": round(4096 / t, 1), "unit": "tok/s",
+        "workload": "8 layers of the full-width shapes, 4096 prompt tokens, layer-major",
+        "ms": round(t * 1000, 2),
+        "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 2),
+                     "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": round(flops / t / 1e12 / bf16_peak, 4),
+                     "algorithmic_flops": flops,
+                     "memory_floor_ms": round(wbytes / (hbm_peak * 1e9) * 1000, 2),
+                     "compute_floor_ms": round(flops / (bf16_peak * 1e12) * 1000, 2)},
+    }
+    del sess
+
+    # decode stack + lm_head + top-p sampler: prompt 512, 256 generated tokens
+    sess = pdl.Session(model, 512 + 256 + 16)
+    prompt = synth.host_tokens(512, stack.vocab, stream=41)
+    assert sess.prefill(prompt) == 0
+    ws = torch.empty(pdl.sample_workspace_bytes(stack.vocab), dtype=torch.uint8, device="cuda")
+    state = 0x9E3779B97F4A7C15
+    tok, state = pdl.sample(sess.logits(), 0.7, 0.95, state, ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(256):
+        assert sess.decode(tok) == 0
+        tok, state = pdl.sample(sess.logits(), 0.7, 0.95, state, ws)
+        assert tok >= 0
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t = ev0.elapsed_time(ev1) / 1000.0
+    tok_bytes = stack.n_layers * sum(layer_bytes(stack).values()) + lm_head_bytes(stack)
+    out["stack"] = {
+        "metric": "decode tok/s (8 layers + lm_head + top-p 0.95, T 0.7)",
+        "value": round(256 / t, 1), "unit": "tok/s",
+        "roofline": {"bound": "hbm", "bytes_per_token": int(tok_bytes),
+                     "achieved": round(tok_bytes * 256 / t / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(tok_bytes * 256 / t / 1e9 / hbm_peak, 4)},
+        "note": "each token synchronises to return the sampled id to the host",
+    }
+    del sess
+
+    # common-prefix resync: live 16994 -> common 16846 -> canonical 16937
+    P = synth.host_tokens(16846, stack.vocab, stream=51)
+    live_tail = synth.host_tokens(148, stack.vocab, stream=52)
+    new_tail = synth.host_tokens(91, stack.vocab, stream=53)
+    new_tail[0] = (live_tail[0] + 1) % stack.vocab
+    prompt = np.concatenate([P, new_tail])
+    live = pdl.Session(model, 17100)
+    assert live.prefill(np.concatenate([P, live_tail])) == 0
+    torch.cuda.synchronize()
+    cp = live.common_prefix(prompt)
+    ev0.record(stream)
+    assert live.truncate(cp) == 0
+    assert live.prefill(prompt[cp:]) == 0
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    resync_ms = ev0.elapsed_time(ev1)
+    ws2 = torch.empty(pdl.sample_workspace_bytes(stack.vocab), dtype=torch.uint8, device="cuda")
+    ids_live = []
+    t0 = time.perf_counter()
+    for i in range(64):
+        tk, _ = pdl.sample(live.logits(), 0.0, 1.0, None, ws2)
+        ids_live.append(tk)
+        assert live.decode(tk) == 0
+    torch.cuda.synchronize()
+    dec_s = time.perf_counter() - t0
+    logits_live = live.logits().clone()
+    del live
+    scratch = pdl.Session(model, 17100)
+    assert scratch.prefill(prompt) == 0
+    ids_scratch = []
+    for i in range(64):
+        tk, _ = pdl.sample(scratch.logits(), 0.0, 1.0, None, ws2)
+        ids_scratch.append(tk)
+        assert scratch.decode(tk) == 0
+    torch.cuda.synchronize()
+    same = ids_live == ids_scratch and torch.equal(logits_live, scratch.logits())
+    del scratch
+    sfl = prefill_flops_per_token_layer(stack) * 91 * stack.n_layers
+    out["resync"] = {
+        "metric": "resync latency (truncate + 91-token prefill, 8 layers)",
+        "value": round(resync_ms, 3), "unit": "ms", "common_prefix": cp,
+        "greedy_decode_tok_s": round(64 / dec_s, 1),
+        "matches_scratch_prefill": bool(same),
+        "algorithmic_flops": sfl,
+    }
+    return out
+
+
+if __name__ == "__main__":
+    main()

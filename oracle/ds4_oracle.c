@@ -348,6 +348,7 @@ int32_t orc_sample(const float *logits, int n, double temperature, double top_p,
     qsort(order, (size_t)n, sizeof(int), cmp_desc);
     double target = top_p * sum_all;
     int n_kept = n;
+    info->cut_index = -1;
     if (top_p >= 1.0) {
         for (int i = 0; i < n; i++) kept[i] = 1;
         info->cut_sum_margin = info->cut_gap_margin = 1.0;
@@ -361,15 +362,32 @@ int32_t orc_sample(const float *logits, int n, double temperature, double top_p,
                 double before = cum - p[order[r]];
                 double a = fabs(cum - target), b = fabs(target - before);
                 info->cut_sum_margin = (a < b ? a : b) / sum_all;
-                info->cut_gap_margin =
-                    (r + 1 < n) ? (p[order[r]] - p[order[r + 1]]) / p[order[r]] : 1.0;
+                /* nearest different probability on either side of the crossing
+                   token: exact ties are ordered by index everywhere, near-ties
+                   are where a lower-precision computation may order differently */
+                double pc = p[order[r]], gap = 1.0;
+                for (int j = r + 1; j < n; j++)
+                    if (p[order[j]] != pc) { gap = (pc - p[order[j]]) / pc; break; }
+                for (int j = r - 1; j >= 0; j--)
+                    if (p[order[j]] != pc) {
+                        double g2 = (p[order[j]] - pc) / pc;
+                        if (g2 < gap) gap = g2;
+                        break;
+                    }
+                info->cut_gap_margin = gap;
+                info->cut_index = order[r];
                 break;
             }
         }
     }
-    double sum = 0.0;
+    double sum = 0.0, sq = 0.0;
     for (int i = 0; i < n; i++)
-        if (kept[i]) sum += p[i];
+        if (kept[i]) {
+            sum += p[i];
+            sq += p[i] * p[i];
+        }
+    info->p_rms = sqrt(sq) / sum;
+    info->cut_p = info->cut_index >= 0 ? p[info->cut_index] / sum : 0.0;
 
     /* 3. inverse CDF in vocabulary order over the kept tokens */
     double rnd = u * sum;

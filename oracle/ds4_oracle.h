@@ -113,9 +113,15 @@ typedef struct {
     double sum_kept;        /* sum of p over kept tokens */
     double cut_sum_margin;  /* distance of the top-p target from the cumulative sums
                                on both sides of the crossing token, / sum_all */
-    double cut_gap_margin;  /* relative p gap between the crossing token and the next */
+    double cut_gap_margin;  /* relative p gap between the crossing token and the nearest
+                               token of different probability on either side */
     double cdf_margin;      /* distance of u*sum_kept from the selected token's CDF
                                interval ends, / sum_kept */
+    int cut_index;          /* vocabulary id of the crossing token (-1: all kept) */
+    double cut_p;           /* its probability, / sum_kept */
+    double p_rms;           /* sqrt(sum of kept p^2) / sum_kept: scale of how far a
+                               cumulative sum moves when every p carries a small
+                               independent relative error */
 } orc_sample_info;
 
 /* ---- scalar formats ---- */

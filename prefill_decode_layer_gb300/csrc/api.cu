@@ -1,0 +1,525 @@
+// C ABI of the ds4g library (include/ds4g.h): model and session bookkeeping,
+// validation, and the order in which the kernels of a call are issued.
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace ds4g;
+
+struct ds4g_model {
+    ds4g_config cfg;
+    Dims d;
+    std::vector<LayerPtrs> layers;
+    const uint16_t *tok_embd;
+    const void *lm_head;
+    int nsm;
+};
+
+struct ds4g_session {
+    ds4g_model *m;
+    int n_ctx;
+    int len;
+    std::vector<int32_t> hist;
+    cudaStream_t st;
+    std::vector<void *> kc, vc;
+    float2 *rope;
+    DecodeBufs b;
+    PrefillBufs pb;
+    uint64_t launches = 0;
+    bool timing = false;
+    cudaEvent_t ev[DS4G_K_COUNT][2];
+    double t_ms[DS4G_K_COUNT] = {};
+    uint64_t t_n[DS4G_K_COUNT] = {};
+};
+
+namespace {
+// Adds the kernels launched on this thread during a call to the session's count.
+struct LaunchScope {
+    ds4g_session *s;
+    uint64_t start;
+    explicit LaunchScope(ds4g_session *s_) : s(s_), start(ds4g::launch_count()) {}
+    ~LaunchScope() { s->launches += ds4g::launch_count() - start; }
+};
+}  // namespace
+
+namespace {
+
+size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int prefill_P(const ds4g_config &c) { return c.prefill_chunk > 0 ? c.prefill_chunk : 4096; }
+
+Dims dims_of(const ds4g_config &c)
+{
+    Dims d;
+    d.L = c.n_layers; d.H = c.hidden; d.NH = c.n_heads; d.HD = c.head_dim; d.RQ = c.q_rank;
+    d.RKV = c.kv_rank; d.W = c.window; d.E = c.n_experts; d.K = c.top_k; d.I = c.expert_inter;
+    d.V = c.vocab; d.QD = c.n_heads * c.head_dim; d.eps = c.rms_eps; d.wdt = c.weight_dtype;
+    d.kvdt = c.kv_dtype;
+    return d;
+}
+
+bool cfg_ok(const ds4g_config *c)
+{
+    if (!c) return false;
+    if (c->n_layers < 1 || c->hidden < 8 || c->n_heads < 1 || c->head_dim < 8) return false;
+    if (c->hidden % 8 || c->q_rank % 8 || c->kv_rank % 8 || c->expert_inter % 8) return false;
+    if (c->head_dim % 8 || c->head_dim > 256 || c->q_rank < 8 || c->kv_rank < 8) return false;
+    if (c->window < 1 || c->window > 1024) return false;
+    if (c->n_experts < 1 || c->n_experts > 1024 || c->top_k < 1 || c->top_k > 8 ||
+        c->top_k > c->n_experts)
+        return false;
+    if (c->vocab < 1 || c->expert_inter < 8) return false;
+    if (c->weight_dtype != DS4G_F32 && c->weight_dtype != DS4G_BF16) return false;
+    if (c->kv_dtype != DS4G_F32 && c->kv_dtype != DS4G_BF16) return false;
+    if (c->prefill_chunk < 0 || c->prefill_chunk > 65536) return false;
+    if (!(c->rope_base > 0.f) || !(c->rms_eps >= 0.f)) return false;
+    if (c->n_experts % 4) return false;  // 4-wide epilogues of the batched kernels
+    // shared-memory footprints of the kernels (floats unless stated)
+    const size_t smem_max = 227 * 1024;
+    const size_t kvs = c->kv_dtype == DS4G_BF16 ? 2 : 4;
+    const size_t win = 2 * (size_t)c->window * c->head_dim * kvs;
+    if (win + (size_t)(c->head_dim + c->window + 32) * 4 > smem_max) return false;
+    if (win + 8 * (size_t)(c->head_dim + c->window) * 4 > smem_max) return false;
+    const size_t qd = (size_t)c->n_heads * c->head_dim;
+    const size_t vecs[] = {(size_t)(c->hidden > c->n_experts ? c->hidden : c->n_experts) + 32,
+                           (size_t)c->q_rank + c->kv_rank, qd,
+                           (size_t)(c->top_k + 1) * c->expert_inter};
+    for (size_t v : vecs)
+        if (v * 4 > smem_max) return false;
+    return true;
+}
+
+bool aligned16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+struct Layout {
+    size_t kv, rope, dec, pre, total;
+};
+
+Layout layout(const ds4g_config &c, int n_ctx)
+{
+    const Dims d = dims_of(c);
+    const size_t kvs = c.kv_dtype == DS4G_BF16 ? 2 : 4;
+    Layout L;
+    size_t o = 0;
+    L.kv = o;
+    o += (size_t)d.L * 2 * al((size_t)n_ctx * d.HD * kvs);
+    L.rope = o;
+    o += al((size_t)n_ctx * (d.HD / 2) * sizeof(float2));
+    L.dec = o;
+    o += 4 * al((size_t)d.H * 4);                      // x, xm, xn2, hidden
+    o += al((size_t)(d.RQ + d.RKV) * 4);               // c
+    o += 2 * al((size_t)d.QD * 4);                     // q, o
+    o += al((size_t)d.E * 4);                          // scores
+    o += 2 * al((size_t)d.L * d.K * 4);                // ids, wts
+    o += al((size_t)(d.K + 1) * d.I * 4);              // h
+    o += al((size_t)d.V * 4);                          // logits
+    o += al(64);                                       // counters
+    L.pre = o;
+    o += prefill_bytes(d, prefill_P(c));
+    L.total = o;
+    return L;
+}
+
+__global__ void k_rope_table(float2 *t, int n_ctx, int half, double base)
+{
+    const size_t total = (size_t)n_ctx * half;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int p = (int)(i / half), j = (int)(i % half);
+        const double theta = pow(base, -2.0 * (double)j / (double)(2 * half));
+        double s, c;
+        sincos((double)p * theta, &s, &c);
+        t[i] = make_float2((float)c, (float)s);
+    }
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DS4G_OK : DS4G_ECUDA; }
+
+// xorshift64* (Vigna 2016): shifts 12, 25, 27; output multiplied by the published constant.
+uint64_t xorshift64s(uint64_t *s)
+{
+    uint64_t x = *s;
+    x ^= x >> 12;
+    x ^= x << 25;
+    x ^= x >> 27;
+    *s = x;
+    return x * 0x2545F4914F6CDD1DULL;
+}
+
+StepArgs step_base(ds4g_session *s)
+{
+    StepArgs a;
+    memset(&a, 0, sizeof(a));
+    a.d = s->m->d;
+    a.rope = s->rope;
+    a.b = s->b;
+    a.tok_embd = s->m->tok_embd;
+    a.lm_head = s->m->lm_head;
+    a.token = -1;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ds4g_model_create(const ds4g_config *cfg, const ds4g_weights *w, ds4g_model **out)
+{
+    if (!out) return DS4G_EINVAL;
+    *out = nullptr;
+    if (!cfg_ok(cfg) || !w || !w->layers) return DS4G_EINVAL;
+    if (!aligned16(w->tok_embd) || !aligned16(w->lm_head)) return DS4G_EINVAL;
+    ds4g_model *m = new (std::nothrow) ds4g_model;
+    if (!m) return DS4G_EINVAL;
+    m->cfg = *cfg;
+    m->d = dims_of(*cfg);
+    m->tok_embd = static_cast<const uint16_t *>(w->tok_embd);
+    m->lm_head = w->lm_head;
+    for (int l = 0; l < cfg->n_layers; ++l) {
+        const ds4g_layer_weights &s = w->layers[l];
+        const void *all[] = {s.attn_norm, s.wq_a, s.wq_b, s.wkv_a, s.wk_b, s.wv_b, s.wo,
+                             s.ffn_norm, s.w_router, s.w_gate, s.w_up, s.w_down, s.ws_gate,
+                             s.ws_up, s.ws_down};
+        for (const void *p : all)
+            if (!aligned16(p)) { delete m; return DS4G_EINVAL; }
+        LayerPtrs L;
+        L.attn_norm = static_cast<const float *>(s.attn_norm);
+        L.wq_a = s.wq_a; L.wq_b = s.wq_b; L.wkv_a = s.wkv_a; L.wk_b = s.wk_b; L.wv_b = s.wv_b;
+        L.wo = s.wo;
+        L.ffn_norm = static_cast<const float *>(s.ffn_norm);
+        L.w_router = s.w_router; L.w_gate = s.w_gate; L.w_up = s.w_up; L.w_down = s.w_down;
+        L.ws_gate = s.ws_gate; L.ws_up = s.ws_up; L.ws_down = s.ws_down;
+        m->layers.push_back(L);
+    }
+    int dev = 0, max_smem = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (!e) e = cudaDeviceGetAttribute(&m->nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (!e) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (!e) e = decode_setup(m->d, max_smem);
+    if (!e) e = prefill_setup(m->d, max_smem);
+    if (e) {
+        if (getenv("DS4G_VERBOSE")) fprintf(stderr, "ds4g_model_create: %s\n", cudaGetErrorString(e));
+        delete m;
+        return DS4G_ECUDA;
+    }
+    *out = m;
+    return DS4G_OK;
+}
+
+void ds4g_model_destroy(ds4g_model *m) { delete m; }
+
+size_t ds4g_session_bytes(const ds4g_config *cfg, int n_ctx)
+{
+    if (!cfg_ok(cfg) || n_ctx < 1) return 0;
+    return layout(*cfg, n_ctx).total;
+}
+
+int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, void *stream,
+                        ds4g_session **out)
+{
+    if (!out) return DS4G_EINVAL;
+    *out = nullptr;
+    if (!m || n_ctx < 1 || !dev_mem || ((uintptr_t)dev_mem & 255u)) return DS4G_EINVAL;
+    const Layout L = layout(m->cfg, n_ctx);
+    if (bytes < L.total) return DS4G_ESIZE;
+    ds4g_session *s = new (std::nothrow) ds4g_session;
+    if (!s) return DS4G_EINVAL;
+    const Dims &d = m->d;
+    char *base = static_cast<char *>(dev_mem);
+    s->m = m;
+    s->n_ctx = n_ctx;
+    s->len = 0;
+    s->hist.assign((size_t)n_ctx, 0);
+    s->st = static_cast<cudaStream_t>(stream);
+    const size_t kvs = m->cfg.kv_dtype == DS4G_BF16 ? 2 : 4;
+    const size_t per = al((size_t)n_ctx * d.HD * kvs);
+    for (int l = 0; l < d.L; ++l) {
+        s->kc.push_back(base + L.kv + (2 * (size_t)l) * per);
+        s->vc.push_back(base + L.kv + (2 * (size_t)l + 1) * per);
+    }
+    s->rope = reinterpret_cast<float2 *>(base + L.rope);
+    char *p = base + L.dec;
+    auto take = [&](size_t n) { char *r = p; p += al(n); return r; };
+    DecodeBufs &b = s->b;
+    b.x = (float *)take((size_t)d.H * 4);
+    b.xm = (float *)take((size_t)d.H * 4);
+    b.xn2 = (float *)take((size_t)d.H * 4);
+    b.hidden = (float *)take((size_t)d.H * 4);
+    b.c = (float *)take((size_t)(d.RQ + d.RKV) * 4);
+    b.q = (float *)take((size_t)d.QD * 4);
+    b.o = (float *)take((size_t)d.QD * 4);
+    b.scores = (float *)take((size_t)d.E * 4);
+    b.ids = (int *)take((size_t)d.L * d.K * 4);
+    b.wts = (float *)take((size_t)d.L * d.K * 4);
+    b.h = (float *)take((size_t)(d.K + 1) * d.I * 4);
+    b.logits = (float *)take((size_t)d.V * 4);
+    b.counters = (unsigned *)take(64);
+    prefill_carve(d, prefill_P(m->cfg), base + L.pre, s->pb);
+    cudaError_t e = cudaMemsetAsync(base + L.dec, 0, L.pre - L.dec, s->st);
+    if (!e) {
+        k_rope_table<<<256, 256, 0, s->st>>>(s->rope, n_ctx, d.HD / 2, (double)m->cfg.rope_base);
+        ++launch_count();
+        e = cudaGetLastError();
+    }
+    if (e) { delete s; return DS4G_ECUDA; }
+    *out = s;
+    return DS4G_OK;
+}
+
+void ds4g_session_destroy(ds4g_session *s)
+{
+    if (!s) return;
+    if (s->timing)
+        for (int k = 0; k < DS4G_K_COUNT; ++k) {
+            cudaEventDestroy(s->ev[k][0]);
+            cudaEventDestroy(s->ev[k][1]);
+        }
+    delete s;
+}
+
+int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
+{
+    if (!s || n < 0 || (n > 0 && !tokens)) return DS4G_EINVAL;
+    if (n == 0) return DS4G_OK;
+    const Dims &d = s->m->d;
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= d.V) return DS4G_ETOKEN;
+    if ((long long)s->len + n >= s->n_ctx) return DS4G_ECONTEXT;
+    LaunchScope scope(s);
+    const int P = s->pb.P;
+    for (int c = 0; c < n; c += P) {
+        const int nc = n - c < P ? n - c : P;
+        cudaError_t e = cudaMemcpyAsync(s->pb.tok, tokens + c, (size_t)nc * 4,
+                                        cudaMemcpyHostToDevice, s->st);
+        if (!e) e = prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,
+                                  s->m->tok_embd, s->pb, s->len + c, nc, s->st, s->m->nsm);
+        if (!e && c + nc == n) {
+            StepArgs a = step_base(s);
+            a.b.x = s->pb.X + (size_t)(nc - 1) * d.H;
+            e = decode_lm_head(a, s->st, s->m->nsm);
+        }
+        if (e) return DS4G_ECUDA;
+    }
+    memcpy(s->hist.data() + s->len, tokens, (size_t)n * 4);
+    s->len += n;
+    return DS4G_OK;
+}
+
+int ds4g_decode_step(ds4g_session *s, int32_t token)
+{
+    if (!s) return DS4G_EINVAL;
+    const Dims &d = s->m->d;
+    if (token < 0 || token >= d.V) return DS4G_ETOKEN;
+    if (s->len + 1 >= s->n_ctx) return DS4G_ECONTEXT;
+    LaunchScope scope(s);
+    StepArgs a = step_base(s);
+    a.pos = s->len;
+    cudaEvent_t(*ev)[2] = s->timing ? s->ev : nullptr;
+    for (int l = 0; l < d.L; ++l) {
+        a.w = s->m->layers[l];
+        a.kc = s->kc[l];
+        a.vc = s->vc[l];
+        a.layer = l;
+        a.token = l == 0 ? token : -1;
+        if (decode_layer(a, s->st, s->m->nsm, ev)) return DS4G_ECUDA;
+        if (ev) {  // read this layer's kernel times before the events are reused
+            if (cudaStreamSynchronize(s->st)) return DS4G_ECUDA;
+            for (int k = 0; k <= DS4G_K_EXPERT_DOWN; ++k) {
+                float ms = 0.f;
+                if (cudaEventElapsedTime(&ms, ev[k][0], ev[k][1])) return DS4G_ECUDA;
+                s->t_ms[k] += ms;
+                s->t_n[k] += 1;
+            }
+        }
+    }
+    a.token = -1;
+    if (ev) cudaEventRecord(ev[DS4G_K_LM_HEAD][0], s->st);
+    if (decode_lm_head(a, s->st, s->m->nsm)) return DS4G_ECUDA;
+    if (ev) {
+        float ms = 0.f;
+        cudaEventRecord(ev[DS4G_K_LM_HEAD][1], s->st);
+        if (cudaEventSynchronize(ev[DS4G_K_LM_HEAD][1]) ||
+            cudaEventElapsedTime(&ms, ev[DS4G_K_LM_HEAD][0], ev[DS4G_K_LM_HEAD][1]))
+            return DS4G_ECUDA;
+        s->t_ms[DS4G_K_LM_HEAD] += ms;
+        s->t_n[DS4G_K_LM_HEAD] += 1;
+    }
+    s->hist[s->len] = token;
+    s->len += 1;
+    return DS4G_OK;
+}
+
+int ds4g_session_common_prefix(const ds4g_session *s, const int32_t *tokens, int n)
+{
+    if (!s || n < 0 || (n > 0 && !tokens)) return DS4G_EINVAL;
+    int i = 0;
+    while (i < n && i < s->len && s->hist[i] == tokens[i]) ++i;
+    return i;
+}
+
+int ds4g_session_truncate(ds4g_session *s, int common_prefix)
+{
+    if (!s || common_prefix < 0 || common_prefix > s->len) return DS4G_EINVAL;
+    s->len = common_prefix;
+    return DS4G_OK;
+}
+
+int ds4g_session_len(const ds4g_session *s) { return s ? s->len : DS4G_EINVAL; }
+
+const float *ds4g_session_logits(const ds4g_session *s) { return s ? s->b.logits : nullptr; }
+
+int ds4g_session_kv(ds4g_session *s, int layer, void **k, void **v)
+{
+    if (!s || layer < 0 || layer >= s->m->d.L || !k || !v) return DS4G_EINVAL;
+    *k = s->kc[layer];
+    *v = s->vc[layer];
+    return DS4G_OK;
+}
+
+int ds4g_session_restore(ds4g_session *s, const int32_t *tokens, int n)
+{
+    if (!s || n < 0 || (n > 0 && !tokens)) return DS4G_EINVAL;
+    if (n >= s->n_ctx) return DS4G_ECONTEXT;
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= s->m->d.V) return DS4G_ETOKEN;
+    if (n) memcpy(s->hist.data(), tokens, (size_t)n * 4);
+    s->len = n;
+    return DS4G_OK;
+}
+
+int ds4g_session_router(ds4g_session *s, int layer, int32_t *ids, float *weights)
+{
+    if (!s || layer < 0 || layer >= s->m->d.L || !ids || !weights) return DS4G_EINVAL;
+    const int K = s->m->d.K;
+    cudaError_t e = cudaMemcpyAsync(ids, s->b.ids + (size_t)layer * K, (size_t)K * 4,
+                                    cudaMemcpyDeviceToHost, s->st);
+    if (!e) e = cudaMemcpyAsync(weights, s->b.wts + (size_t)layer * K, (size_t)K * 4,
+                                cudaMemcpyDeviceToHost, s->st);
+    if (!e) e = cudaStreamSynchronize(s->st);
+    return cuda_status(e);
+}
+
+const void *ds4g_session_debug(const ds4g_session *s, int which)
+{
+    if (!s) return nullptr;
+    switch (which) {
+    case DS4G_DBG_X: return s->b.x;
+    case DS4G_DBG_CQKV: return s->b.c;
+    case DS4G_DBG_Q: return s->b.q;
+    case DS4G_DBG_ATTN: return s->b.o;
+    case DS4G_DBG_XMID: return s->b.xm;
+    case DS4G_DBG_XN2: return s->b.xn2;
+    case DS4G_DBG_SCORES: return s->b.scores;
+    case DS4G_DBG_H: return s->b.h;
+    case DS4G_DBG_HIDDEN: return s->b.hidden;
+    case DS4G_DBG_PREFILL_X: return s->pb.X;
+    default: return nullptr;
+    }
+}
+
+uint64_t ds4g_session_launches(const ds4g_session *s) { return s ? s->launches : 0; }
+
+int ds4g_session_set_timing(ds4g_session *s, int on)
+{
+    if (!s) return DS4G_EINVAL;
+    if (on && !s->timing) {
+        for (int k = 0; k < DS4G_K_COUNT; ++k)
+            if (cudaEventCreate(&s->ev[k][0]) || cudaEventCreate(&s->ev[k][1])) return DS4G_ECUDA;
+        s->timing = true;
+    } else if (!on && s->timing) {
+        if (cudaStreamSynchronize(s->st)) return DS4G_ECUDA;
+        for (int k = 0; k < DS4G_K_COUNT; ++k) {
+            cudaEventDestroy(s->ev[k][0]);
+            cudaEventDestroy(s->ev[k][1]);
+        }
+        s->timing = false;
+    }
+    return DS4G_OK;
+}
+
+int ds4g_session_timing(ds4g_session *s, double *ms, uint64_t *counts, int n)
+{
+    if (!s || n < 0 || (n > 0 && (!ms || !counts))) return DS4G_EINVAL;
+    for (int k = 0; k < n && k < DS4G_K_COUNT; ++k) {
+        ms[k] = s->t_ms[k];
+        counts[k] = s->t_n[k];
+    }
+    for (int k = 0; k < DS4G_K_COUNT; ++k) {
+        s->t_ms[k] = 0.0;
+        s->t_n[k] = 0;
+    }
+    return DS4G_OK;
+}
+
+size_t ds4g_sample_workspace_bytes(int n_vocab)
+{
+    return n_vocab > 0 ? sample_workspace_bytes(n_vocab) : 0;
+}
+
+static int32_t sample_common(const float *logits, int n_vocab, float temperature, float top_p,
+                             unsigned u24, void *workspace, size_t workspace_bytes, void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int *res = nullptr;
+    int32_t tok = -1;
+    cudaError_t e = sample_launch(logits, n_vocab, temperature, top_p, u24, workspace, st, &res);
+    if (!e) e = cudaMemcpyAsync(&tok, res, 4, cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return DS4G_ECUDA;
+    return tok;
+}
+
+static int sample_args_ok(const float *logits, int n_vocab, float temperature, float top_p,
+                          void *workspace, size_t workspace_bytes)
+{
+    if (!logits || n_vocab < 1 || !workspace || ((uintptr_t)workspace & 255u)) return DS4G_EINVAL;
+    if (workspace_bytes < sample_workspace_bytes(n_vocab)) return DS4G_ESIZE;
+    if (temperature != temperature || top_p != top_p) return DS4G_EINVAL;
+    return DS4G_OK;
+}
+
+int32_t ds4g_sample(const float *logits, int n_vocab, float temperature, float top_p,
+                    uint64_t *rng_state, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const int rc = sample_args_ok(logits, n_vocab, temperature, top_p, workspace, workspace_bytes);
+    if (rc) return rc;
+    unsigned u24 = 0;
+    if (temperature > 0.f) {
+        if (!rng_state || *rng_state == 0) return DS4G_EINVAL;
+        u24 = (unsigned)(xorshift64s(rng_state) >> 40);
+    }
+    return sample_common(logits, n_vocab, temperature, top_p, u24, workspace, workspace_bytes,
+                         stream);
+}
+
+int32_t ds4g_sample_u(const float *logits, int n_vocab, float temperature, float top_p,
+                      uint32_t u24, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const int rc = sample_args_ok(logits, n_vocab, temperature, top_p, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (u24 >= (1u << 24)) return DS4G_EINVAL;
+    return sample_common(logits, n_vocab, temperature, top_p, u24, workspace, workspace_bytes,
+                         stream);
+}
+
+const char *ds4g_strerror(int code)
+{
+    switch (code) {
+    case DS4G_OK: return "ok";
+    case DS4G_EINVAL: return "invalid argument, shape or handle";
+    case DS4G_ECONTEXT: return "tokens do not fit in the session context";
+    case DS4G_ETOKEN: return "token id outside the vocabulary";
+    case DS4G_ECUDA: return "CUDA call or kernel launch failed";
+    case DS4G_ETIMEOUT: return "a bounded device-side wait gave up";
+    case DS4G_ESIZE: return "buffer too small";
+    default: return "unknown error";
+    }
+}
+
+}  // extern "C"

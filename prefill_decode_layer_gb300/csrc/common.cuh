@@ -1,0 +1,244 @@
+// Shared device helpers and host-side structures of the ds4g library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ds4g.h"
+
+namespace ds4g {
+
+using bf16 = __nv_bfloat16;
+
+// Model dimensions, copied into every kernel's arguments.
+struct Dims {
+    int L, H, NH, HD, RQ, RKV, W, E, K, I, V, QD;  // QD = NH * HD
+    float eps;
+    int wdt, kvdt;
+};
+
+// One layer's weight pointers (device).
+struct LayerPtrs {
+    const float *attn_norm;
+    const void *wq_a, *wq_b, *wkv_a, *wk_b, *wv_b, *wo;
+    const float *ffn_norm;
+    const void *w_router, *w_gate, *w_up, *w_down, *ws_gate, *ws_up, *ws_down;
+};
+
+// Decode-step activations (device, inside the session buffer).
+struct DecodeBufs {
+    float *x;        // [H]   residual: layer input, then layer output
+    float *xm;       // [H]   residual after the attention half
+    float *xn2;      // [H]   normalised residual entering the MoE
+    float *c;        // [RQ+RKV] Q and KV latents
+    float *q;        // [QD]  queries after RoPE
+    float *o;        // [QD]  attention output
+    float *scores;   // [E]   router scores
+    int *ids;        // [L*K] selected experts per layer
+    float *wts;      // [L*K] their weights
+    float *h;        // [(K+1)*I] SwiGLU hidden
+    float *logits;   // [V]
+    float *hidden;   // [H]   final hidden state
+    unsigned *counters;  // [8] grid-completion tickets (reset by their last user)
+};
+
+// Arguments of every decode kernel: one layer at one position.
+struct StepArgs {
+    Dims d;
+    LayerPtrs w;
+    void *kc, *vc;          // this layer's K and V caches [n_ctx][HD]
+    const float2 *rope;     // [n_ctx][HD/2] (cos, sin)
+    DecodeBufs b;
+    const uint16_t *tok_embd;
+    const void *lm_head;
+    int layer, pos, token;  // token >= 0 only for the first layer's first kernel
+};
+
+// ------------------------------------------------------------------ device helpers
+
+// Programmatic dependent launch: wait for the preceding grid's results, and
+// allow the next grid to be scheduled.  Both are no-ops without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 16-byte read-only streaming load that does not allocate in L1 and marks the
+// line first-to-evict in L2 (weights are read once per step).
+__device__ __forceinline__ uint4 ld_stream(const void *ptr, uint64_t pol)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(ptr), "l"(pol));
+    return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <typename T> struct VecOf;
+template <> struct VecOf<bf16> { static constexpr int n = 8; };
+template <> struct VecOf<float> { static constexpr int n = 4; };
+
+// acc += dot(16 bytes of weights, x[0..n)) with x 16-byte aligned in shared memory.
+template <typename TW> __device__ __forceinline__ float dotv(const uint4 &w, const float *x,
+                                                            float acc);
+template <> __device__ __forceinline__ float dotv<bf16>(const uint4 &w, const float *x, float acc)
+{
+    const float4 a = *reinterpret_cast<const float4 *>(x);
+    const float4 b = *reinterpret_cast<const float4 *>(x + 4);
+    acc = fmaf(__uint_as_float(w.x << 16), a.x, acc);
+    acc = fmaf(__uint_as_float(w.x & 0xffff0000u), a.y, acc);
+    acc = fmaf(__uint_as_float(w.y << 16), a.z, acc);
+    acc = fmaf(__uint_as_float(w.y & 0xffff0000u), a.w, acc);
+    acc = fmaf(__uint_as_float(w.z << 16), b.x, acc);
+    acc = fmaf(__uint_as_float(w.z & 0xffff0000u), b.y, acc);
+    acc = fmaf(__uint_as_float(w.w << 16), b.z, acc);
+    acc = fmaf(__uint_as_float(w.w & 0xffff0000u), b.w, acc);
+    return acc;
+}
+template <> __device__ __forceinline__ float dotv<float>(const uint4 &w, const float *x, float acc)
+{
+    const float4 a = *reinterpret_cast<const float4 *>(x);
+    acc = fmaf(__uint_as_float(w.x), a.x, acc);
+    acc = fmaf(__uint_as_float(w.y), a.y, acc);
+    acc = fmaf(__uint_as_float(w.z), a.z, acc);
+    acc = fmaf(__uint_as_float(w.w), a.w, acc);
+    return acc;
+}
+
+// Per-lane partial dot products of R weight rows (global) with one vector xs
+// (shared memory), over nvec 16-byte vectors.  Lane l takes vectors l, l+32, ...;
+// U vectors per row are in flight at once.  Reduce with warp_sum afterwards.
+template <typename TW, int R, int U>
+__device__ __forceinline__ void gemv_rows(const TW *const (&rows)[R], const float *xs, int nvec,
+                                          float (&acc)[R], int lane, uint64_t pol)
+{
+    constexpr int VEC = VecOf<TW>::n;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+        uint4 w[R][U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 32 * u;
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                w[r][u] = (v < nvec) ? ld_stream(rows[r] + (size_t)v * VEC, pol)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 32 * u;
+            if (v < nvec) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) acc[r] = dotv<TW>(w[r][u], xs + v * VEC, acc[r]);
+            }
+        }
+    }
+}
+
+// Block-wide sum (fixed order: per-warp shuffle tree, then warp 0 over warps).
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (warp == 0) {
+        t = lane < nw ? red[lane] : 0.f;
+        t = warp_sum(t);
+        if (lane == 0) red[0] = t;
+    }
+    __syncthreads();
+    t = red[0];
+    return t;
+}
+
+__device__ __forceinline__ float block_max(float v, float *red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < nw ? red[lane] : -INFINITY;
+        t = warp_max(t);
+        if (lane == 0) red[0] = t;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// ------------------------------------------------------------------ host helpers
+
+// Kernels launched by the calling thread (a session has one owner thread).
+inline uint64_t &launch_count()
+{
+    static thread_local uint64_t n = 0;
+    return n;
+}
+
+// Allow a kernel the largest dynamic shared memory the device offers beside its
+// static shared memory.
+static inline cudaError_t allow_max_dyn_smem(const void *f, int optin)
+{
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, f);
+    if (e) return e;
+    return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - (int)fa.sharedSizeBytes);
+}
+
+// Launch with programmatic stream serialisation so the kernel may be scheduled
+// while its predecessor drains (the kernel itself waits with pdl_wait()).
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                     size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ++launch_count();
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace ds4g

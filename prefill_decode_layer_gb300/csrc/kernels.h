@@ -1,0 +1,49 @@
+// Host-side entry points of the kernel files (internal to the library).
+#pragma once
+
+#include "common.cuh"
+
+namespace ds4g {
+
+// decode.cu
+cudaError_t decode_setup(const Dims &d, int max_smem);
+cudaError_t decode_layer(const StepArgs &a, cudaStream_t st, int nsm,
+                         cudaEvent_t (*ev)[2] = nullptr);
+cudaError_t decode_lm_head(const StepArgs &a, cudaStream_t st, int nsm);
+
+// sampler.cu
+size_t sample_workspace_bytes(int n);
+cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p,
+                          unsigned u24, void *ws, cudaStream_t st, int **result_dev);
+
+// prefill.cu
+struct PrefillBufs {
+    int P;            // chunk capacity (tokens)
+    int *tok;         // [P]
+    float *X;         // [P][H] residual
+    void *XN;         // [P][H] normalised activations (activation type)
+    float *XN32;      // [P][H] f32 copy of the MoE-side normalised activations (router)
+    void *C;          // [P][RQ+RKV] latents
+    void *Q;          // [P][QD] queries after RoPE
+    void *O;          // [P][QD] attention output
+    float *S;         // [P][E] router scores
+    int *ids;         // [P][K]
+    float *wts;       // [P][K]
+    int *cnt;         // [E] tokens per expert
+    int *off;         // [E+1] start of each expert's rows in the grouped order
+    int *rows;        // [P*K] grouped order: token * K + slot
+    int *tiles;       // [P*K/16 + E + 1] (expert, first row) work items; tiles[0] = count
+    void *HG;         // [P*K][I] routed SwiGLU hidden, grouped order
+    void *HS;         // [P][I] shared SwiGLU hidden
+    float *YS;        // [P*K][H] routed expert outputs, token-slot order
+};
+size_t prefill_bytes(const Dims &d, int P);
+void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb);
+cudaError_t prefill_setup(const Dims &d, int max_smem);
+// Layer-major pass of tokens [0, n) of the chunk (already in pb.tok) at positions
+// [p0, p0 + n): embed, every layer, and leaves the final hidden states in pb.X.
+cudaError_t prefill_chunk(const Dims &d, const LayerPtrs *layers, void *const *kc,
+                          void *const *vc, const float2 *rope, const uint16_t *tok_embd,
+                          const PrefillBufs &pb, int p0, int n, cudaStream_t st, int nsm);
+
+}  // namespace ds4g

@@ -1,0 +1,492 @@
+// Layer-major prefill (page "ds4.c 学习笔记 -- 端到端推理流程", 阶段三
+// prefill_layer_major_cpu): layer l runs over every token of the chunk before
+// layer l+1, so each layer's weights are streamed once per chunk.
+//
+// Per layer: RMSNorm -> [W_qa; W_kva] GEMM -> W_qb GEMM with RoPE -> [W_kb; W_vb]
+// GEMM with RoPE and the KV-cache append -> windowed causal MQA -> W_o GEMM with
+// the residual -> RMSNorm -> router GEMM -> per-token top-k -> tokens grouped per
+// expert (stable counting sort) -> grouped gate/up GEMMs with SwiGLU -> shared
+// expert -> grouped down GEMMs scattered per (token, slot) -> shared down GEMM
+// whose epilogue adds the weighted routed outputs in slot order and the residual.
+//
+// Every output element is accumulated in a fixed order that does not depend on
+// how many tokens share the chunk, so a token's results are the same whether it
+// is prefilled alone, in a suffix after a truncation, or inside a long prompt.
+//
+// The GEMMs here are SIMT tiles with f32 activations and f32 accumulation.
+#include "common.cuh"
+#include "gemm.cuh"
+#include "kernels.h"
+
+namespace ds4g {
+
+// ------------------------------------------------------------------ small kernels
+
+__global__ void k_embed_rows(const uint16_t *table, const int *tok, float *X, int H)
+{
+    const int t = blockIdx.x;
+    const __half *row = reinterpret_cast<const __half *>(table) + (size_t)tok[t] * H;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) X[(size_t)t * H + i] = __half2float(row[i]);
+}
+
+// out = RMSNorm(X) in the activation type; out32 (optional) keeps an f32 copy for
+// the router, whose top-k decisions need more than bf16 input precision.
+template <typename TA>
+__global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *X, const float *g, TA *out,
+                                                      float *out32, int H, float eps)
+{
+    __shared__ float red[32];
+    const int t = blockIdx.x;
+    const float *x = X + (size_t)t * H;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+    ss = block_sum(ss, red);
+    const float inv = rsqrtf(ss / (float)H + eps);
+    for (int i = threadIdx.x; i < H; i += blockDim.x) {
+        const float y = x[i] * inv * g[i];
+        out[(size_t)t * H + i] = from_f32<TA>(y);
+        if (out32) out32[(size_t)t * H + i] = y;
+    }
+}
+
+// Router decision per token: top-k of the scores (ties to the lower id), softmax
+// over the selected scores.  One warp per token.
+__global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E, int K)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= n) return;
+    const float *s = S + (size_t)warp * E;
+    unsigned taken = 0u;  // bit j: this lane's j-th expert (e = lane + 32 j) is chosen
+    float sel[8];
+    int sid[8];
+    for (int k = 0; k < K; ++k) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int e = lane, j = 0; e < E; e += 32, ++j) {
+            if ((taken >> j) & 1u) continue;
+            const float v = s[e];
+            if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        sel[k] = bv;
+        sid[k] = bi;
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    }
+    if (lane == 0) {
+        float sum = 0.f, w[8];
+        for (int k = 0; k < K; ++k) { w[k] = expf(sel[k] - sel[0]); sum += w[k]; }
+        for (int k = 0; k < K; ++k) {
+            ids[(size_t)warp * K + k] = sid[k];
+            wts[(size_t)warp * K + k] = w[k] / sum;
+        }
+    }
+}
+
+// Stable grouping of the (token, slot) entries by expert.  Pass 1: one CTA per
+// expert counts its entries.
+__global__ void __launch_bounds__(256) k_group_count(const int *ids, int nent, int *cnt)
+{
+    __shared__ int red[8];
+    const int e = blockIdx.x;
+    int c = 0;
+    for (int i = threadIdx.x; i < nent; i += blockDim.x) c += (ids[i] == e);
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+        cnt[e] = t;
+    }
+}
+
+// Pass 2 (one thread): expert offsets and the (expert, first row) tile list.
+__global__ void k_group_scan(const int *cnt, int E, int bm, int *off, int *tiles)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int o = 0, nt = 0;
+    for (int e = 0; e < E; ++e) {
+        off[e] = o;
+        for (int r = 0; r < cnt[e]; r += bm) {
+            tiles[1 + 2 * nt] = e;
+            tiles[2 + 2 * nt] = o + r;
+            ++nt;
+        }
+        o += cnt[e];
+    }
+    off[E] = o;
+    tiles[0] = nt;
+}
+
+// Pass 3: one CTA per expert writes its entries in index (token, slot) order.
+__global__ void __launch_bounds__(256) k_group_fill(const int *ids, int nent, const int *off,
+                                                    int *rows)
+{
+    __shared__ int wcount[8];
+    __shared__ int base;
+    const int e = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) base = off[e];
+    __syncthreads();
+    for (int i0 = 0; i0 < nent; i0 += blockDim.x) {
+        const int i = i0 + threadIdx.x;
+        const bool m = i < nent && ids[i] == e;
+        const unsigned bal = __ballot_sync(0xffffffffu, m);
+        if (lane == 0) wcount[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += wcount[w];
+        if (m) rows[base + before + __popc(bal & ((1u << lane) - 1u))] = i;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int t = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += wcount[w];
+            base += t;
+        }
+        __syncthreads();
+    }
+}
+
+// Windowed causal multi-query attention for a chunk: CTA (token t, group of heads).
+// The window's K/V rows are staged once in shared memory for all heads of the group.
+template <typename TA, typename TKV>
+__global__ void __launch_bounds__(256) k_attn_prefill(const TA *Q, TA *O, const TKV *kc,
+                                                      const TKV *vc, int p0, Dims d, int hg)
+{
+    extern __shared__ __align__(16) unsigned char sm[];
+    const int HD = d.HD, W = d.W;
+    TKV *Ks = reinterpret_cast<TKV *>(sm);
+    TKV *Vs = Ks + (size_t)W * HD;
+    float *qs = reinterpret_cast<float *>(Vs + (size_t)W * HD);  // [8 warps][HD]
+    float *ps = qs + 8 * HD;                                     // [8 warps][W]
+    const int t = blockIdx.x, pos = p0 + t;
+    const int lo = max(0, pos - W + 1), n = pos - lo + 1;
+    const int nv = n * HD * (int)sizeof(TKV) / 16;
+    const uint4 *ks = reinterpret_cast<const uint4 *>(kc + (size_t)lo * HD);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(vc + (size_t)lo * HD);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        reinterpret_cast<uint4 *>(Ks)[i] = ks[i];
+        reinterpret_cast<uint4 *>(Vs)[i] = vs[i];
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float scale = rsqrtf((float)HD);
+    float *q = qs + warp * HD, *p = ps + warp * W;
+    for (int hh = warp; hh < hg; hh += 8) {
+        const int h = blockIdx.y * hg + hh;
+        if (h >= d.NH) break;
+        const TA *qrow = Q + (size_t)t * d.QD + (size_t)h * HD;
+        for (int i = lane; i < HD; i += 32) q[i] = to_f32<TA>(qrow[i]) * scale;
+        __syncwarp();
+        // scores: lanes split the head dimension (conflict-free rows), 4 keys at a time
+        float m = -INFINITY;
+        for (int j0 = 0; j0 < n; j0 += 4) {
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = lane; i < HD; i += 32) {
+                const float qi = q[i];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (j0 + u < n) s[u] = fmaf(qi, to_f32<TKV>(Ks[(size_t)(j0 + u) * HD + i]), s[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                s[u] = warp_sum(s[u]);
+                if (j0 + u < n) {
+                    m = fmaxf(m, s[u]);
+                    if (lane == 0) p[j0 + u] = s[u];
+                }
+            }
+        }
+        __syncwarp();
+        float sum = 0.f;
+        for (int j = lane; j < n; j += 32) {
+            const float e = __expf(p[j] - m);
+            p[j] = e;
+            sum += e;
+        }
+        sum = warp_sum(sum);
+        __syncwarp();
+        const float inv = 1.f / sum;
+        for (int i = lane; i < HD; i += 32) {
+            float acc = 0.f;
+            for (int j = 0; j < n; ++j) acc = fmaf(p[j], to_f32<TKV>(Vs[(size_t)j * HD + i]), acc);
+            O[(size_t)t * d.QD + (size_t)h * HD + i] = from_f32<TA>(acc * inv);
+        }
+        __syncwarp();
+    }
+}
+
+// ------------------------------------------------------------------ GEMM problems
+// Each problem maps rows of A, rows of W (an [N][K] row-major operand) and a 4-wide
+// column group of outputs; see gemm.cuh for the kernels that drive them.
+
+template <typename TA, typename TW>
+struct ProbQKVA {  // C = XN [W_qa; W_kva]^T
+    const TA *XN; const TW *wqa, *wkva; TA *C; int H, RQ, ldc;
+    __device__ const TA *a_row(int m, int) const { return XN + (size_t)m * H; }
+    __device__ const TW *w_row(int n, int) const {
+        return n < RQ ? wqa + (size_t)n * H : wkva + (size_t)(n - RQ) * H;
+    }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) C[(size_t)m * ldc + n + j] = from_f32<TA>(v[j]);
+    }
+};
+
+template <typename TA, typename TW>
+struct ProbQB {  // Q = RoPE(C[:, :RQ] W_qb^T)
+    const TA *C; const TW *wqb; TA *Q; const float2 *rope; int ldc, RQ, QD, HD, p0;
+    __device__ const TA *a_row(int m, int) const { return C + (size_t)m * ldc; }
+    __device__ const TW *w_row(int n, int) const { return wqb + (size_t)n * RQ; }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+        const float2 *rp = rope + (size_t)(p0 + m) * (HD / 2);
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            const float2 cs = rp[((n + j) % HD) / 2];
+            Q[(size_t)m * QD + n + j] = from_f32<TA>(v[j] * cs.x - v[j + 1] * cs.y);
+            Q[(size_t)m * QD + n + j + 1] = from_f32<TA>(v[j] * cs.y + v[j + 1] * cs.x);
+        }
+    }
+};
+
+template <typename TA, typename TW, typename TKV>
+struct ProbKVB {  // K = RoPE(C[:, RQ:] W_kb^T), V = C[:, RQ:] W_vb^T, appended to the cache
+    const TA *C; const TW *wkb, *wvb; TKV *kc, *vc; const float2 *rope; int ldc, RQ, RKV, HD, p0;
+    __device__ const TA *a_row(int m, int) const { return C + (size_t)m * ldc + RQ; }
+    __device__ const TW *w_row(int n, int) const {
+        return n < HD ? wkb + (size_t)n * RKV : wvb + (size_t)(n - HD) * RKV;
+    }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+        const size_t row = (size_t)(p0 + m) * HD;
+        if (n < HD) {
+            const float2 *rp = rope + (size_t)(p0 + m) * (HD / 2);
+#pragma unroll
+            for (int j = 0; j < 4; j += 2) {
+                const float2 cs = rp[(n + j) / 2];
+                kc[row + n + j] = from_f32<TKV>(v[j] * cs.x - v[j + 1] * cs.y);
+                kc[row + n + j + 1] = from_f32<TKV>(v[j] * cs.y + v[j + 1] * cs.x);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) vc[row + n - HD + j] = from_f32<TKV>(v[j]);
+        }
+    }
+};
+
+template <typename TA, typename TW>
+struct ProbWO {  // X += O W_o^T
+    const TA *O; const TW *wo; float *X; int QD, H;
+    __device__ const TA *a_row(int m, int) const { return O + (size_t)m * QD; }
+    __device__ const TW *w_row(int n, int) const { return wo + (size_t)n * QD; }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) X[(size_t)m * H + n + j] += v[j];
+    }
+};
+
+template <typename TW>
+struct ProbRouter {  // S = XN W_r^T from f32 activations (f32 scores)
+    const float *XN; const TW *wr; float *S; int H, E;
+    __device__ const float *a_row(int m, int) const { return XN + (size_t)m * H; }
+    __device__ const TW *w_row(int n, int) const { return wr + (size_t)n * H; }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) S[(size_t)m * E + n + j] = v[j];
+    }
+};
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// Gate/up with SwiGLU; W rows interleaved (gate_i, up_i) so an output pair is local.
+template <typename TA, typename TW, bool GROUPED>
+struct ProbGU {
+    const TA *XN; const int *rows; const TW *wg, *wu; TA *Hout; int H, I, K;
+    size_t estride;  // elements between experts' matrices (I * H)
+    __device__ const TA *a_row(int m, int) const {
+        return XN + (size_t)(GROUPED ? rows[m] / K : m) * H;
+    }
+    __device__ const TW *w_row(int n, int e) const {
+        const TW *b = (n & 1) ? wu : wg;
+        return b + (GROUPED ? (size_t)e * estride : 0) + (size_t)(n >> 1) * H;
+    }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+        Hout[(size_t)m * I + (n >> 1)] = from_f32<TA>(silu_mul(v[0], v[1]));
+        Hout[(size_t)m * I + (n >> 1) + 1] = from_f32<TA>(silu_mul(v[2], v[3]));
+    }
+};
+
+template <typename TA, typename TW>
+struct ProbDown {  // YS[token*K + slot] = HG W_d(e)^T, grouped rows
+    const TA *HG; const int *rows; const TW *wd; float *YS; int H, I;
+    __device__ const TA *a_row(int m, int) const { return HG + (size_t)m * I; }
+    __device__ const TW *w_row(int n, int e) const {
+        return wd + (size_t)e * H * I + (size_t)n * I;
+    }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+        float *y = YS + (size_t)rows[m] * H + n;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) y[j] = v[j];
+    }
+};
+
+template <typename TA, typename TW>
+struct ProbSharedDown {  // X += HS W_sd^T + sum_s w[s] YS[token, s]  (slot order, then shared)
+    const TA *HS; const TW *wsd; const float *YS; const float *wts; float *X; int H, I, K;
+    __device__ const TA *a_row(int m, int) const { return HS + (size_t)m * I; }
+    __device__ const TW *w_row(int n, int) const { return wsd + (size_t)n * I; }
+    __device__ void store4(int m, int n, const float (&v)[4], int) const {
+        float r[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s = 0; s < K; ++s) {
+            const float w = wts[(size_t)m * K + s];
+            const float *y = YS + ((size_t)m * K + s) * H + n;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r[j] = fmaf(w, y[j], r[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) X[(size_t)m * H + n + j] += r[j] + v[j];
+    }
+};
+
+// ------------------------------------------------------------------ host side
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t prefill_bytes(const Dims &d, int P)
+{
+    const size_t ta = 4;  // activation element size
+    const size_t PK = (size_t)P * d.K;
+    size_t b = 0;
+    b += align256((size_t)P * 4);                        // tok
+    b += align256((size_t)P * d.H * 4);                  // X
+    b += align256((size_t)P * d.H * ta);                 // XN
+    b += align256((size_t)P * d.H * 4);                  // XN32
+    b += align256((size_t)P * (d.RQ + d.RKV) * ta);      // C
+    b += 2 * align256((size_t)P * d.QD * ta);            // Q, O
+    b += align256((size_t)P * d.E * 4);                  // S
+    b += 2 * align256(PK * 4);                           // ids, wts
+    b += align256((size_t)d.E * 4) + align256((size_t)(d.E + 1) * 4);
+    b += align256(PK * 4);                               // rows
+    b += align256((PK / 16 + d.E + 2) * 2 * 4);          // tiles
+    b += align256(PK * d.I * ta);                        // HG
+    b += align256((size_t)P * d.I * ta);                 // HS
+    b += align256(PK * d.H * 4);                         // YS
+    return b;
+}
+
+void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb)
+{
+    const size_t ta = 4;
+    const size_t PK = (size_t)P * d.K;
+    char *p = base;
+    auto take = [&](size_t n) { char *r = p; p += align256(n); return (void *)r; };
+    pb.P = P;
+    pb.tok = (int *)take((size_t)P * 4);
+    pb.X = (float *)take((size_t)P * d.H * 4);
+    pb.XN = take((size_t)P * d.H * ta);
+    pb.XN32 = (float *)take((size_t)P * d.H * 4);
+    pb.C = take((size_t)P * (d.RQ + d.RKV) * ta);
+    pb.Q = take((size_t)P * d.QD * ta);
+    pb.O = take((size_t)P * d.QD * ta);
+    pb.S = (float *)take((size_t)P * d.E * 4);
+    pb.ids = (int *)take(PK * 4);
+    pb.wts = (float *)take(PK * 4);
+    pb.cnt = (int *)take((size_t)d.E * 4);
+    pb.off = (int *)take((size_t)(d.E + 1) * 4);
+    pb.rows = (int *)take(PK * 4);
+    pb.tiles = (int *)take((PK / 16 + d.E + 2) * 2 * 4);
+    pb.HG = take(PK * d.I * ta);
+    pb.HS = take((size_t)P * d.I * ta);
+    pb.YS = (float *)take(PK * d.H * 4);
+}
+
+static size_t attn_prefill_smem(const Dims &d)
+{
+    const size_t kvs = d.kvdt == DS4G_BF16 ? 2 : 4;
+    return 2 * (size_t)d.W * d.HD * kvs + 8 * (size_t)(d.HD + d.W) * 4;
+}
+
+cudaError_t prefill_setup(const Dims &d, int max_smem)
+{
+    return d.kvdt == DS4G_BF16
+               ? allow_max_dyn_smem((const void *)k_attn_prefill<float, bf16>, max_smem)
+               : allow_max_dyn_smem((const void *)k_attn_prefill<float, float>, max_smem);
+}
+
+template <typename TA, typename TW, typename TKV>
+static cudaError_t chunk_t(const Dims &d, const LayerPtrs *layers, void *const *kcs,
+                           void *const *vcs, const float2 *rope, const uint16_t *tok_embd,
+                           const PrefillBufs &pb, int p0, int n, cudaStream_t st, int nsm)
+{
+    cudaError_t e;
+    const int H = d.H, K = d.K, nent = n * K;
+    TA *XN = (TA *)pb.XN, *C = (TA *)pb.C, *Q = (TA *)pb.Q, *O = (TA *)pb.O;
+    TA *HG = (TA *)pb.HG, *HS = (TA *)pb.HS;
+    k_embed_rows<<<n, 256, 0, st>>>(tok_embd, pb.tok, pb.X, H);
+    ++launch_count();
+    if ((e = cudaGetLastError())) return e;
+    for (int l = 0; l < d.L; ++l) {
+        const LayerPtrs &w = layers[l];
+        TKV *kc = (TKV *)kcs[l], *vc = (TKV *)vcs[l];
+        k_rmsnorm_rows<TA><<<n, 256, 0, st>>>(pb.X, w.attn_norm, XN, nullptr, H, d.eps);
+        ++launch_count();
+        ProbQKVA<TA, TW> pa{XN, (const TW *)w.wq_a, (const TW *)w.wkv_a, C, H, d.RQ, d.RQ + d.RKV};
+        if ((e = gemm_dense<TA, TW>(pa, n, d.RQ + d.RKV, H, st, nsm))) return e;
+        ProbQB<TA, TW> pq{C, (const TW *)w.wq_b, Q, rope, d.RQ + d.RKV, d.RQ, d.QD, d.HD, p0};
+        if ((e = gemm_dense<TA, TW>(pq, n, d.QD, d.RQ, st, nsm))) return e;
+        ProbKVB<TA, TW, TKV> pk{C, (const TW *)w.wk_b, (const TW *)w.wv_b, kc, vc, rope,
+                                d.RQ + d.RKV, d.RQ, d.RKV, d.HD, p0};
+        if ((e = gemm_dense<TA, TW>(pk, n, 2 * d.HD, d.RKV, st, nsm))) return e;
+        const int hg = d.NH < 16 ? d.NH : 16;
+        k_attn_prefill<TA, TKV><<<dim3(n, (d.NH + hg - 1) / hg), 256, attn_prefill_smem(d), st>>>(
+            Q, O, kc, vc, p0, d, hg);
+        ++launch_count();
+        if ((e = cudaGetLastError())) return e;
+        ProbWO<TA, TW> po{O, (const TW *)w.wo, pb.X, d.QD, H};
+        if ((e = gemm_dense<TA, TW>(po, n, H, d.QD, st, nsm))) return e;
+        k_rmsnorm_rows<TA><<<n, 256, 0, st>>>(pb.X, w.ffn_norm, XN, pb.XN32, H, d.eps);
+        ++launch_count();
+        ProbRouter<TW> pr{pb.XN32, (const TW *)w.w_router, pb.S, H, d.E};
+        if ((e = gemm_dense<float, TW>(pr, n, d.E, H, st, nsm))) return e;
+        k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K);
+        ++launch_count();
+        k_group_count<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.cnt);
+        ++launch_count();
+        k_group_scan<<<1, 32, 0, st>>>(pb.cnt, d.E, kGroupBM, pb.off, pb.tiles);
+        ++launch_count();
+        k_group_fill<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.off, pb.rows);
+        ++launch_count();
+        if ((e = cudaGetLastError())) return e;
+        const int max_tiles = nent / kGroupBM + d.E + 1;
+        ProbGU<TA, TW, true> pg{XN, pb.rows, (const TW *)w.w_gate, (const TW *)w.w_up, HG, H,
+                                d.I, K, (size_t)d.I * H};
+        if ((e = gemm_grouped<TA, TW>(pg, pb.tiles, pb.off, max_tiles, 2 * d.I, H, st))) return e;
+        ProbGU<TA, TW, false> ps{XN, nullptr, (const TW *)w.ws_gate, (const TW *)w.ws_up, HS, H,
+                                 d.I, K, 0};
+        if ((e = gemm_dense<TA, TW>(ps, n, 2 * d.I, H, st, nsm))) return e;
+        ProbDown<TA, TW> pd{HG, pb.rows, (const TW *)w.w_down, pb.YS, H, d.I};
+        if ((e = gemm_grouped<TA, TW>(pd, pb.tiles, pb.off, max_tiles, H, d.I, st))) return e;
+        ProbSharedDown<TA, TW> psd{HS, (const TW *)w.ws_down, pb.YS, pb.wts, pb.X, H, d.I, K};
+        if ((e = gemm_dense<TA, TW>(psd, n, H, d.I, st, nsm))) return e;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t prefill_chunk(const Dims &d, const LayerPtrs *layers, void *const *kc,
+                          void *const *vc, const float2 *rope, const uint16_t *tok_embd,
+                          const PrefillBufs &pb, int p0, int n, cudaStream_t st, int nsm)
+{
+    // SIMT path: f32 activations for every weight format
+    if (d.wdt == DS4G_BF16)
+        return d.kvdt == DS4G_BF16
+                   ? chunk_t<float, bf16, bf16>(d, layers, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
+                   : chunk_t<float, bf16, float>(d, layers, kc, vc, rope, tok_embd, pb, p0, n, st, nsm);
+    return d.kvdt == DS4G_BF16
+               ? chunk_t<float, float, bf16>(d, layers, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
+               : chunk_t<float, float, float>(d, layers, kc, vc, rope, tok_embd, pb, p0, n, st, nsm);
+}
+
+}  // namespace ds4g

@@ -1,0 +1,345 @@
+// Sampler kernels: page "ds4.c 学习笔记 -- 端到端推理流程", 阶段四 4.3
+// (sample_full_vocab / sample_top_p_min_p / sample_argmax).
+//
+// T > 0.  z_i = l_i / T and p_i = exp(z_i - max z) in f32 (the page's float
+// arithmetic), then q_i = round(p_i * 2^40) as a
+// 64-bit fixed-point integer.  All sums are integer sums, so every reduction
+// order gives the same bits and the drawn token does not depend on timing.
+//   pass 0   max of the logits (ordered-integer atomicMax)
+//   pass 1-4 radix select, 8 bits at a time from the top, of the top-p
+//            threshold tau on the f32 bit pattern of p (p >= 0, so the bit
+//            pattern orders like the value): per digit, the sum of q over the
+//            candidates; the last CTA of each pass picks the digit at which
+//            the running sum from the top reaches ceil(top_p * total).
+//            Ties at tau are kept in index order, as many as the target needs.
+//   pass 5   per-chunk sums of kept q; the last CTA finds the chunk and then the
+//            first token, in vocabulary order, whose running kept sum reaches
+//            R = max(1, ceil(u * kept_total)) (u = k / 2^24 exactly).
+// T <= 0.   argmax: max of (ordered logit bits, inverted index) as one u64.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ds4g {
+
+static constexpr int kChunk = 1024;   // tokens per CTA
+static constexpr int kSThreads = 256;
+
+struct SampleWS {
+    unsigned long long hist[4][256];   // per-pass digit sums of q
+    unsigned long long total;          // sum of q over the vocabulary
+    unsigned long long above;          // sum of q with p bits above the selected prefix
+    unsigned long long target;         // ceil(top_p * total)
+    unsigned long long keep_ties;      // tie tokens (p == tau) kept, in index order
+    unsigned long long argmax_key;
+    unsigned int max_key;              // ordered bits of max logit
+    unsigned int prefix;               // selected high bits of tau so far
+    unsigned int tickets[8];
+    int result;
+    int pad[3];
+    // followed by: u64 chunk_above[nchunks], u32 chunk_ties[nchunks]
+};
+
+__device__ __forceinline__ unsigned ordered_bits(float f)
+{
+    const unsigned u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered(unsigned k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ float prob(float l, float t, float zm)
+{
+    return expf(__fdiv_rn(l, t) - zm);
+}
+
+__device__ __forceinline__ unsigned long long fixed_q(float p)
+{
+    return (unsigned long long)__float2ll_rn(p * 1099511627776.0f);  // 2^40, exact scaling
+}
+
+// Ticket: returns true in the last CTA to arrive (all of its threads).
+__device__ __forceinline__ bool last_cta(unsigned *ticket)
+{
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned t = atomicAdd(ticket, 1u);
+        s_last = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last) __threadfence();
+    return s_last != 0;
+}
+
+__global__ void __launch_bounds__(kSThreads) k_s_max(const float *logits, int n, SampleWS *ws,
+                                                     int greedy)
+{
+    const int base = blockIdx.x * kChunk;
+    unsigned mk = 0u;
+    unsigned long long ak = 0ull;
+    for (int i = base + threadIdx.x; i < min(base + kChunk, n); i += blockDim.x) {
+        const unsigned k = ordered_bits(logits[i]);
+        mk = max(mk, k);
+        if (greedy) ak = max(ak, ((unsigned long long)k << 32) | (0xffffffffu - (unsigned)i));
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+        ak = max(ak, __shfl_xor_sync(0xffffffffu, ak, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicMax(&ws->max_key, mk);
+        if (greedy) atomicMax(&ws->argmax_key, ak);
+    }
+    if (greedy && last_cta(&ws->tickets[0]) && threadIdx.x == 0) {
+        ws->result = (int)(0xffffffffu - (unsigned)(ws->argmax_key & 0xffffffffull));
+        ws->tickets[0] = 0u;
+    }
+}
+
+// Digit-histogram pass d (0..3) over the candidates matching the prefix chosen so far.
+__global__ void __launch_bounds__(kSThreads) k_s_hist(const float *logits, int n, float temp,
+                                                      float top_p, SampleWS *ws, int d)
+{
+    __shared__ unsigned long long h[256];
+    __shared__ unsigned long long s_tot;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0ull;
+    if (threadIdx.x == 0) s_tot = 0ull;
+    __syncthreads();
+    const float zm = __fdiv_rn(from_ordered(ws->max_key), temp);
+    const unsigned prefix = ws->prefix;
+    const int shift = 24 - 8 * d;
+    const unsigned hi_mask = d == 0 ? 0u : (0xffffffffu << (32 - 8 * d));
+    const int base = blockIdx.x * kChunk;
+    unsigned long long tot = 0ull;
+    for (int i = base + threadIdx.x; i < min(base + kChunk, n); i += blockDim.x) {
+        const float p = prob(logits[i], temp, zm);
+        const unsigned long long q = fixed_q(p);
+        const unsigned bits = __float_as_uint(p);
+        tot += q;
+        if ((bits & hi_mask) == prefix && q) atomicAdd(&h[(bits >> shift) & 0xffu], q);
+    }
+    if (d == 0) {
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if ((threadIdx.x & 31) == 0) atomicAdd(&s_tot, tot);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+        if (h[i]) atomicAdd(&ws->hist[d][i], h[i]);
+    if (d == 0 && threadIdx.x == 0) atomicAdd(&ws->total, s_tot);
+    if (!last_cta(&ws->tickets[1 + d])) return;
+    if (threadIdx.x == 0) {
+        if (d == 0) {
+            const double t = ceil((double)top_p * (double)ws->total);
+            ws->target = t < 1.0 ? 1ull : (unsigned long long)t;  // keep at least one token
+        }
+        const unsigned long long target = ws->target;
+        unsigned long long above = ws->above;
+        int b = 255;
+        for (; b > 0; --b) {
+            const unsigned long long hb = ws->hist[d][b];
+            if (above + hb >= target) break;
+            above += hb;
+        }
+        ws->above = above;
+        ws->prefix = prefix | ((unsigned)b << shift);
+        ws->tickets[1 + d] = 0u;
+    }
+}
+
+// Final pass: per-chunk kept sums, then the inverse-CDF search by the last CTA.
+__global__ void __launch_bounds__(kSThreads) k_s_draw(const float *logits, int n, float temp,
+                                                      int keep_all, unsigned u24, SampleWS *ws,
+                                                      unsigned long long *chunk_above,
+                                                      unsigned *chunk_ties)
+{
+    __shared__ unsigned long long s_sum;
+    __shared__ unsigned s_ties;
+    const float zm = __fdiv_rn(from_ordered(ws->max_key), temp);
+    const unsigned tau = ws->prefix;
+    const int base = blockIdx.x * kChunk;
+    if (threadIdx.x == 0) { s_sum = 0ull; s_ties = 0u; }
+    __syncthreads();
+    unsigned long long sum = 0ull;
+    unsigned ties = 0u;
+    for (int i = base + threadIdx.x; i < min(base + kChunk, n); i += blockDim.x) {
+        const float p = prob(logits[i], temp, zm);
+        const unsigned bits = __float_as_uint(p);
+        if (keep_all || bits > tau) sum += fixed_q(p);
+        else if (bits == tau) ties += 1u;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        ties += __shfl_xor_sync(0xffffffffu, ties, o);
+    }
+    if ((threadIdx.x & 31) == 0) { atomicAdd(&s_sum, sum); atomicAdd(&s_ties, ties); }
+    __syncthreads();
+    if (threadIdx.x == 0) { chunk_above[blockIdx.x] = s_sum; chunk_ties[blockIdx.x] = s_ties; }
+    if (!last_cta(&ws->tickets[5])) return;
+
+    // ---- last CTA: ties to keep, kept total, target R, chunk search, token search
+    __shared__ unsigned long long s_qtau, s_keep, s_R, s_before;
+    __shared__ unsigned s_ties_before;
+    __shared__ int s_chunk;
+    const int nch = gridDim.x;
+    if (threadIdx.x == 0) {
+        const unsigned long long qtau = keep_all ? 0ull : fixed_q(__uint_as_float(tau));
+        unsigned long long keep = 0ull;
+        if (!keep_all) {
+            const unsigned long long need = ws->target > ws->above ? ws->target - ws->above : 0ull;
+            keep = qtau ? (need + qtau - 1) / qtau : ~0ull;
+        }
+        unsigned long long kept_total = 0ull, tb = 0ull;
+        for (int c = 0; c < nch; ++c) {
+            const unsigned long long t = __ldcg(&chunk_ties[c]);
+            const unsigned long long kt = keep_all ? 0ull : (tb >= keep ? 0ull : min(t, keep - tb));
+            kept_total += __ldcg(&chunk_above[c]) + kt * qtau;
+            tb += t;
+        }
+        // R = max(1, ceil(u24 * kept_total / 2^24)), exact in 128-bit arithmetic
+        const unsigned long long lo = (unsigned long long)u24 * (kept_total & 0xffffffull);
+        const unsigned long long hi = (unsigned long long)u24 * (kept_total >> 24);
+        unsigned long long R = hi + (lo >> 24) + ((lo & 0xffffffull) ? 1ull : 0ull);
+        if (R == 0ull) R = 1ull;
+        // the chunk in which the running kept sum reaches R
+        unsigned long long run = 0ull;
+        tb = 0ull;
+        int chunk = nch - 1;
+        unsigned long long before = 0ull, tbefore = 0ull;
+        for (int c = 0; c < nch; ++c) {
+            const unsigned long long t = __ldcg(&chunk_ties[c]);
+            const unsigned long long kt = keep_all ? 0ull : (tb >= keep ? 0ull : min(t, keep - tb));
+            const unsigned long long cs = __ldcg(&chunk_above[c]) + kt * qtau;
+            if (run + cs >= R) { chunk = c; before = run; tbefore = tb; break; }
+            run += cs;
+            tb += t;
+            before = run;
+            tbefore = tb;
+        }
+        s_qtau = qtau; s_keep = keep; s_R = R; s_before = before;
+        s_ties_before = (unsigned)tbefore; s_chunk = chunk;
+        ws->keep_ties = keep;
+    }
+    __syncthreads();
+    // scan the chunk: threads take consecutive runs of tokens; block-wide ordered scan
+    const int c0 = s_chunk * kChunk, c1 = min(c0 + kChunk, n);
+    constexpr int per = kChunk / kSThreads;
+    __shared__ unsigned long long s_part[kSThreads];
+    __shared__ unsigned s_tpart[kSThreads];
+    unsigned long long qv[per];
+    unsigned char tie[per];
+    unsigned long long psum = 0ull;
+    unsigned tcount = 0u;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+        const int i = c0 + threadIdx.x * per + j;
+        qv[j] = 0ull;
+        tie[j] = 0;
+        if (i < c1) {
+            const float p = prob(logits[i], temp, zm);
+            const unsigned bits = __float_as_uint(p);
+            if (keep_all || bits > tau) qv[j] = fixed_q(p);
+            else if (bits == tau) { tie[j] = 1; tcount++; }
+        }
+        psum += qv[j];
+    }
+    s_part[threadIdx.x] = psum;
+    s_tpart[threadIdx.x] = tcount;
+    __syncthreads();
+    if (threadIdx.x == 0) {  // exclusive prefix over threads (fixed order)
+        unsigned long long r = 0ull;
+        unsigned t = 0u;
+        for (int k = 0; k < kSThreads; ++k) {
+            const unsigned long long a = s_part[k];
+            const unsigned b = s_tpart[k];
+            s_part[k] = r;
+            s_tpart[k] = t;
+            r += a;
+            t += b;
+        }
+    }
+    __syncthreads();
+    // each thread walks its own tokens; ties count toward the kept set in index order
+    unsigned long long run = s_before + s_part[threadIdx.x];
+    unsigned long long tidx = (unsigned long long)s_ties_before + s_tpart[threadIdx.x];
+    int found = 0x7fffffff;
+    // running sum including ties requires the number of kept ties before this thread
+    // (ties before it that were kept add q_tau each)
+    {
+        // recompute the kept-tie contribution preceding this thread's first token
+        const unsigned long long keep = s_keep;
+        const unsigned long long tb = (unsigned long long)s_ties_before;
+        const unsigned long long ties_prior = tidx;  // global tie index of our first tie
+        const unsigned long long kept_prior_in_chunk =
+            keep_all ? 0ull
+                     : (ties_prior >= keep ? (tb >= keep ? 0ull : keep - tb)
+                                           : ties_prior - tb);
+        run += kept_prior_in_chunk * s_qtau;
+    }
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+        unsigned long long q = qv[j];
+        if (tie[j]) {
+            q = tidx < s_keep ? s_qtau : 0ull;
+            tidx++;
+        }
+        run += q;
+        if (q && run >= s_R && found == 0x7fffffff) found = c0 + threadIdx.x * per + j;
+    }
+    __shared__ int s_found;
+    if (threadIdx.x == 0) s_found = 0x7fffffff;
+    __syncthreads();
+    if (found != 0x7fffffff) atomicMin(&s_found, found);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int r = s_found;
+        if (r == 0x7fffffff) {  // rounding guard: the last kept token of the chunk
+            for (int i = c1 - 1; i >= c0; --i) {
+                const float p = prob(logits[i], temp, zm);
+                if (fixed_q(p) && (keep_all || __float_as_uint(p) >= tau)) { r = i; break; }
+            }
+        }
+        ws->result = r;
+        ws->tickets[5] = 0u;
+    }
+}
+
+size_t sample_workspace_bytes(int n)
+{
+    const int nch = (n + kChunk - 1) / kChunk;
+    return sizeof(SampleWS) + (size_t)nch * 12 + 256;
+}
+
+// Issues the sampler kernels; the token id is left at *result_dev.
+cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p,
+                          unsigned u24, void *ws_mem, cudaStream_t st, int **result_dev)
+{
+    SampleWS *ws = static_cast<SampleWS *>(ws_mem);
+    const int nch = (n + kChunk - 1) / kChunk;
+    unsigned long long *chunk_above = reinterpret_cast<unsigned long long *>(ws + 1);
+    unsigned *chunk_ties = reinterpret_cast<unsigned *>(chunk_above + nch);
+    *result_dev = &ws->result;
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(SampleWS), st);
+    if (e) return e;
+    const int greedy = temperature <= 0.f;
+    k_s_max<<<nch, kSThreads, 0, st>>>(logits, n, ws, greedy);
+    ++launch_count();
+    if ((e = cudaGetLastError())) return e;
+    if (greedy) return cudaSuccess;
+    const int keep_all = top_p >= 1.0f;
+    if (!keep_all) {
+        for (int d = 0; d < 4; ++d) {
+            k_s_hist<<<nch, kSThreads, 0, st>>>(logits, n, temperature, top_p, ws, d);
+            ++launch_count();
+            if ((e = cudaGetLastError())) return e;
+        }
+    }
+    k_s_draw<<<nch, kSThreads, 0, st>>>(logits, n, temperature, keep_all, u24, ws, chunk_above,
+                                         chunk_ties);
+    ++launch_count();
+    return cudaGetLastError();
+}
+
+}  // namespace ds4g

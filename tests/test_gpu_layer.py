@@ -1,0 +1,75 @@
+"""Full-width decode layer (hidden 4096, 64 x 128 MQA, window 128, 256 experts top-6,
+BF16 weights and KV) at batch 1 against the oracle, in the launch configuration
+the benchmark times: KV pre-filled with 4096 seeded positions, then decode steps."""
+import numpy as np
+import pytest
+
+import synth
+from helpers import (TOL_BF16, LazyOracleModel, OracleKV, gpu_model, kv_to_f64, oracle_embed,
+                     oracle_layer, rel_err, to_np)
+
+pytestmark = pytest.mark.gpu
+
+N_PRE = 4096
+
+
+@pytest.fixture(scope="module")
+def layer_setup():
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    from synth import torch_weights as tw
+    shape = synth.LAYER
+    gm = gpu_model(shape)
+    n_ctx = N_PRE + 200
+    sess = pdl.Session(gm, n_ctx)
+    k, v = sess.kv(0)
+    tw.fill_kv(shape, 0, k, v, N_PRE)
+    hist = synth.host_tokens(N_PRE, shape.vocab, stream=11)
+    assert sess.restore(hist) == 0
+    torch.cuda.synchronize()
+    om = LazyOracleModel(shape)
+    kv = OracleKV(shape, n_ctx)
+    hk, hv = synth.host_kv(shape, 0, N_PRE)
+    kv.k[0][:N_PRE] = hk
+    kv.v[0][:N_PRE] = hv
+    return shape, gm, sess, om, kv
+
+
+def test_seeded_kv_matches_host_generator(layer_setup):
+    shape, gm, sess, om, kv = layer_setup
+    k, v = sess.kv(0)
+    gk = k[:N_PRE].view(dtype=__import__("torch").int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(gk, kv.k[0][:N_PRE])
+
+
+def test_decode_steps_match_oracle(layer_setup):
+    import torch
+    shape, gm, sess, om, kv = layer_setup
+    toks = synth.host_tokens(3, shape.vocab, stream=5)
+    H, QD, K, I = shape.hidden, shape.n_heads * shape.head_dim, shape.top_k, shape.expert_inter
+    ties = 0
+    for s, t in enumerate(toks):
+        pos = N_PRE + s
+        assert sess.decode(int(t)) == 0
+        x = oracle_embed(om, t)
+        tr = oracle_layer(om, kv, 0, pos, x, trace=True)
+        torch.cuda.synchronize()
+        assert rel_err(to_np(sess.debug("q", QD)), tr["q"]) <= TOL_BF16
+        gk, gv = sess.kv(0)
+        assert rel_err(to_np(gk[pos]), kv_to_f64(shape, kv.k[0][pos])) <= TOL_BF16
+        assert rel_err(to_np(gv[pos]), kv_to_f64(shape, kv.v[0][pos])) <= TOL_BF16
+        assert rel_err(to_np(sess.debug("attn", QD)), tr["attn"]) <= TOL_BF16
+        assert rel_err(to_np(sess.debug("xmid", H)), tr["x_mid"]) <= TOL_BF16
+        sc = to_np(sess.debug("scores", shape.n_experts))
+        assert rel_err(sc, tr["scores"]) <= TOL_BF16
+        ids, w = sess.router(0)
+        srt = np.sort(tr["scores"].astype(np.float64))[::-1]
+        gap = srt[K - 1] - srt[K]
+        if gap > 1e-3 * np.max(np.abs(srt)):
+            assert ids == list(tr["ids"]), f"step {s}: {ids} vs {list(tr['ids'])}"
+            assert rel_err(w, tr["weights"]) <= TOL_BF16
+            assert rel_err(to_np(sess.debug("h", (K + 1) * I)), tr["h"]) <= TOL_BF16
+            assert rel_err(to_np(sess.debug("x", H)), x) <= TOL_BF16
+        else:
+            ties += 1
+    assert ties <= 1
