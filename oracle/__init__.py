@@ -60,7 +60,8 @@ class Trace(C.Structure):
 class SampleInfo(C.Structure):
     _fields_ = [("n_kept", C.c_int), ("sum_all", C.c_double), ("sum_kept", C.c_double),
                 ("cut_sum_margin", C.c_double), ("cut_gap_margin", C.c_double),
-                ("cdf_margin", C.c_double), ("cut_index", C.c_int), ("cut_p", C.c_double),
+                ("cdf_margin", C.c_double), ("cut_index", C.c_int), ("cut_next_index", C.c_int),
+                ("cut_p", C.c_double),
                 ("p_rms", C.c_double)]
 
 

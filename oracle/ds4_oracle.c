@@ -349,6 +349,7 @@ int32_t orc_sample(const float *logits, int n, double temperature, double top_p,
     double target = top_p * sum_all;
     int n_kept = n;
     info->cut_index = -1;
+    info->cut_next_index = -1;
     if (top_p >= 1.0) {
         for (int i = 0; i < n; i++) kept[i] = 1;
         info->cut_sum_margin = info->cut_gap_margin = 1.0;
@@ -376,6 +377,7 @@ int32_t orc_sample(const float *logits, int n, double temperature, double top_p,
                     }
                 info->cut_gap_margin = gap;
                 info->cut_index = order[r];
+                info->cut_next_index = r + 1 < n ? order[r + 1] : -1;
                 break;
             }
         }

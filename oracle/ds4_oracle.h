@@ -118,6 +118,7 @@ typedef struct {
     double cdf_margin;      /* distance of u*sum_kept from the selected token's CDF
                                interval ends, / sum_kept */
     int cut_index;          /* vocabulary id of the crossing token (-1: all kept) */
+    int cut_next_index;     /* vocabulary id of the token after it in top-p order */
     double cut_p;           /* its probability, / sum_kept */
     double p_rms;           /* sqrt(sum of kept p^2) / sum_kept: scale of how far a
                                cumulative sum moves when every p carries a small
