@@ -55,7 +55,9 @@ enum {
     DS4G_ETOKEN = -3,    /* a token id outside [0, vocab) */
     DS4G_ECUDA = -4,     /* a CUDA call or kernel launch failed */
     DS4G_ETIMEOUT = -5,  /* a bounded device-side wait gave up */
-    DS4G_ESIZE = -6      /* a caller buffer is too small */
+    DS4G_ESIZE = -6,     /* a caller buffer is too small */
+    DS4G_ENONFINITE = -7 /* a router score was NaN or infinite (the hidden state is not
+                            finite); the step's results are invalid */
 };
 
 /* Model shape and formats.  The five synthetic workloads use hidden 4096,
@@ -78,7 +80,12 @@ typedef struct {
     int weight_dtype;  /* DS4G_BF16 or DS4G_F32, all matrices including lm_head */
     int kv_dtype;      /* DS4G_BF16 or DS4G_F32, KV-cache storage */
     int prefill_chunk; /* tokens per layer-major pass (0: 4096); sets workspace size */
+    int decode_kernel; /* DS4G_DECODE_AUTO: one persistent launch per decode step when
+                          the device supports cooperative launch, else one kernel per
+                          stage; DS4G_DECODE_STAGED forces one kernel per stage */
 } ds4g_config;
+
+enum { DS4G_DECODE_AUTO = 0, DS4G_DECODE_STAGED = 1 };
 
 /* One layer's weights (device pointers).  Gains are f32; matrices weight_dtype. */
 typedef struct {
@@ -137,6 +144,12 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n);
  * lm_head (4.3).  Same errors as ds4g_prefill with n = 1. */
 int ds4g_decode_step(ds4g_session *s, int32_t token);
 
+/* [P3] 阶段四 4.2 without 4.3: one token through every layer, no lm_head (for
+ * callers that need the KV cache and the final hidden state but not the logits).
+ * The final hidden state is at ds4g_session_hidden; the logits are not updated.
+ * Same errors as ds4g_decode_step. */
+int ds4g_decode_layers(ds4g_session *s, int32_t token);
+
 /* [P1] section 3 ds4_session_common_prefix: number of leading tokens shared by
  * the session's history and tokens[0..n). */
 int ds4g_session_common_prefix(const ds4g_session *s, const int32_t *tokens, int n);
@@ -151,6 +164,10 @@ int ds4g_session_len(const ds4g_session *s);
 
 /* Device pointer to the f32 [V] logits of the last processed token. */
 const float *ds4g_session_logits(const ds4g_session *s);
+
+/* Device pointer to the f32 [H] final hidden state (last layer's output) of the
+ * last processed token. */
+const float *ds4g_session_hidden(const ds4g_session *s);
 
 /* Device pointers of layer `layer`'s K and V caches: [n_ctx][HD] of kv_dtype,
  * K stored after RoPE.  For tests and for restoring a saved cache. */
@@ -176,19 +193,27 @@ enum {
     DS4G_DBG_XN2 = 5,     /* f32 [H] normalised residual entering the MoE */
     DS4G_DBG_SCORES = 6,  /* f32 [E] router scores */
     DS4G_DBG_H = 7,       /* f32 [(K+1)*I] SwiGLU hidden, routed slots then shared */
-    DS4G_DBG_HIDDEN = 8,  /* f32 [H] final hidden state entering the lm_head */
-    DS4G_DBG_PREFILL_X = 9  /* f32 [prefill_chunk][H] final hidden states of the last
+    DS4G_DBG_HIDDEN = 8,  /* f32 [H] final hidden state (same as DS4G_DBG_X) */
+    DS4G_DBG_PREFILL_X = 9, /* f32 [prefill_chunk][H] final hidden states of the last
                                prefill chunk (row t = t-th token of that chunk) */
+    DS4G_DBG_STATUS = 10    /* int32 raw device status word (0: no device-side error) */
 };
 const void *ds4g_session_debug(const ds4g_session *s, int which);
+
+/* Synchronise the session stream and report the first device-side error since the
+ * last call: DS4G_ETIMEOUT (a bounded wait gave up) or DS4G_ENONFINITE (a router
+ * score was not finite; the expert choice then falls back to the lowest unused
+ * ids, so every access stays in bounds).  The step's results are then invalid.
+ * The flag is cleared.  DS4G_ECUDA if the stream reports an error. */
+int ds4g_session_status(ds4g_session *s);
 
 /* Kernels this session has launched so far (all calls on it). */
 uint64_t ds4g_session_launches(const ds4g_session *s);
 
-/* Tracing: per-kernel timing of decode steps.  While on, every kernel of a
- * decode step is bracketed by CUDA events on the session stream and the step
- * synchronises the stream at its end (timing removes the overlap that
- * programmatic dependent launch gives consecutive kernels).  ds4g_session_timing
+/* Tracing: per-kernel timing of decode steps.  While on, decode steps run one
+ * kernel per stage, every kernel is bracketed by CUDA events on the session
+ * stream and the step synchronises the stream at its end (timing removes the
+ * overlap that programmatic dependent launch gives consecutive kernels).  ds4g_session_timing
  * copies the accumulated milliseconds and launch counts of each kernel kind
  * (DS4G_K_*) into ms[0..n) and counts[0..n), then resets them. */
 enum {
@@ -203,6 +228,15 @@ enum {
     DS4G_K_COUNT = 8
 };
 int ds4g_session_set_timing(ds4g_session *s, int on);
+
+/* Tracing of the single-launch decode step: when buf (device, caller-owned) is
+ * not NULL, each later decode step writes the GPU global time (ns) at which every
+ * CTA starts each stage: entry [e * n_cta + c] for event e = 7 * layer + stage
+ * (stages: Q/KV down, up + RoPE + append, attention, output projection, router,
+ * gate/up, down + combine), e = 7 * n_layers for the lm_head and 7 * n_layers + 1
+ * for the end; n_cta is the number of SMs.  Events beyond bytes / (8 n_cta) are
+ * dropped.  NULL turns tracing off. */
+int ds4g_session_set_trace(ds4g_session *s, void *buf, size_t bytes);
 int ds4g_session_timing(ds4g_session *s, double *ms, uint64_t *counts, int n);
 
 /* Sampler workspace bytes for a vocabulary of n_vocab (device memory). */

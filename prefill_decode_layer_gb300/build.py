@@ -30,16 +30,20 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          out: str | None = None) -> str:
+    """Compile csrc/*.cu into `out` (default: libds4g.so next to this file)."""
     deps = _deps()
-    if not force and not _stale(OUT, deps):
-        return OUT
-    os.makedirs(OBJ, exist_ok=True)
+    target = out or OUT
+    if not force and not _stale(target, deps):
+        return target
+    objdir = OBJ if out is None else target + ".objs"
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     flags = FLAGS + (extra or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = ["nvcc"] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -50,10 +54,10 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = OUT + ".tmp"
+    tmp = target + ".tmp"
     subprocess.check_call(["nvcc"] + ARCH + ["-shared", "-o", tmp] + objs)
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, target)
+    return target
 
 
 if __name__ == "__main__":

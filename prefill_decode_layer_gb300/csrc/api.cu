@@ -19,6 +19,7 @@ struct ds4g_model {
     const uint16_t *tok_embd;
     const void *lm_head;
     int nsm;
+    bool persistent;   // decode steps use the single cooperative launch
 };
 
 struct ds4g_session {
@@ -31,7 +32,15 @@ struct ds4g_session {
     float2 *rope;
     DecodeBufs b;
     PrefillBufs pb;
+    LayerPtrs *layers_dev;      // [L] device copy of the layer table
+    void **kv_dev;              // [2L] device K then V cache pointers
+    unsigned *bar;              // grid-barrier arrival counter of the persistent kernel
+    unsigned bar_count = 0;     // its value after every launch so far (host copy)
+    int *status;                // device status word
+    std::vector<void *> kv_host;
     uint64_t launches = 0;
+    unsigned long long *trace = nullptr;
+    int trace_events = 0;
     bool timing = false;
     cudaEvent_t ev[DS4G_K_COUNT][2];
     double t_ms[DS4G_K_COUNT] = {};
@@ -78,6 +87,7 @@ bool cfg_ok(const ds4g_config *c)
     if (c->weight_dtype != DS4G_F32 && c->weight_dtype != DS4G_BF16) return false;
     if (c->kv_dtype != DS4G_F32 && c->kv_dtype != DS4G_BF16) return false;
     if (c->prefill_chunk < 0 || c->prefill_chunk > 65536) return false;
+    if (c->decode_kernel != DS4G_DECODE_AUTO && c->decode_kernel != DS4G_DECODE_STAGED) return false;
     if (!(c->rope_base > 0.f) || !(c->rms_eps >= 0.f)) return false;
     if (c->n_experts % 4) return false;  // 4-wide epilogues of the batched kernels
     // shared-memory footprints of the kernels (floats unless stated)
@@ -120,6 +130,9 @@ Layout layout(const ds4g_config &c, int n_ctx)
     o += al((size_t)(d.K + 1) * d.I * 4);              // h
     o += al((size_t)d.V * 4);                          // logits
     o += al(64);                                       // counters
+    o += al(64);                                       // barrier + status
+    o += al((size_t)d.L * sizeof(LayerPtrs));          // layer table
+    o += al((size_t)2 * d.L * sizeof(void *));         // K/V pointer table
     L.pre = o;
     o += prefill_bytes(d, prefill_P(c));
     L.total = o;
@@ -203,6 +216,9 @@ int ds4g_model_create(const ds4g_config *cfg, const ds4g_weights *w, ds4g_model 
     if (!e) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (!e) e = decode_setup(m->d, max_smem);
     if (!e) e = prefill_setup(m->d, max_smem);
+    m->persistent = false;
+    if (!e && cfg->decode_kernel == DS4G_DECODE_AUTO)
+        e = persistent_setup(m->d, max_smem, m->nsm, &m->persistent);
     if (e) {
         if (getenv("DS4G_VERBOSE")) fprintf(stderr, "ds4g_model_create: %s\n", cudaGetErrorString(e));
         delete m;
@@ -260,8 +276,21 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     b.h = (float *)take((size_t)(d.K + 1) * d.I * 4);
     b.logits = (float *)take((size_t)d.V * 4);
     b.counters = (unsigned *)take(64);
+    s->bar = (unsigned *)take(64);
+    s->status = (int *)(s->bar + 4);
+    b.status = s->status;
+    s->layers_dev = (LayerPtrs *)take((size_t)d.L * sizeof(LayerPtrs));
+    s->kv_dev = (void **)take((size_t)2 * d.L * sizeof(void *));
+    s->kv_host.assign(s->kc.begin(), s->kc.end());
+    s->kv_host.insert(s->kv_host.end(), s->vc.begin(), s->vc.end());
     prefill_carve(d, prefill_P(m->cfg), base + L.pre, s->pb);
+    s->pb.status = s->status;
     cudaError_t e = cudaMemsetAsync(base + L.dec, 0, L.pre - L.dec, s->st);
+    if (!e) e = cudaMemcpyAsync(s->layers_dev, m->layers.data(), (size_t)d.L * sizeof(LayerPtrs),
+                                cudaMemcpyHostToDevice, s->st);
+    if (!e) e = cudaMemcpyAsync(s->kv_dev, s->kv_host.data(), (size_t)2 * d.L * sizeof(void *),
+                                cudaMemcpyHostToDevice, s->st);
+    if (!e) e = cudaStreamSynchronize(s->st);  // the host tables above are read by the copies
     if (!e) {
         k_rope_table<<<256, 256, 0, s->st>>>(s->rope, n_ctx, d.HD / 2, (double)m->cfg.rope_base);
         ++launch_count();
@@ -299,10 +328,10 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
                                         cudaMemcpyHostToDevice, s->st);
         if (!e) e = prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,
                                   s->m->tok_embd, s->pb, s->len + c, nc, s->st, s->m->nsm);
-        if (!e && c + nc == n) {
-            StepArgs a = step_base(s);
-            a.b.x = s->pb.X + (size_t)(nc - 1) * d.H;
-            e = decode_lm_head(a, s->st, s->m->nsm);
+        if (!e && c + nc == n) {  // last token's hidden state, then its logits
+            e = cudaMemcpyAsync(s->b.x, s->pb.X + (size_t)(nc - 1) * d.H, (size_t)d.H * 4,
+                                cudaMemcpyDeviceToDevice, s->st);
+            if (!e) e = decode_lm_head(step_base(s), s->st, s->m->nsm);
         }
         if (e) return DS4G_ECUDA;
     }
@@ -311,13 +340,40 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
     return DS4G_OK;
 }
 
-int ds4g_decode_step(ds4g_session *s, int32_t token)
+static int decode_common(ds4g_session *s, int32_t token, bool logits)
 {
     if (!s) return DS4G_EINVAL;
     const Dims &d = s->m->d;
     if (token < 0 || token >= d.V) return DS4G_ETOKEN;
     if (s->len + 1 >= s->n_ctx) return DS4G_ECONTEXT;
     LaunchScope scope(s);
+    if (s->m->persistent && !s->timing) {
+        PersistArgs pa;
+        memset(&pa, 0, sizeof(pa));
+        pa.d = d;
+        pa.layers = s->layers_dev;
+        pa.kc = s->kv_dev;
+        pa.vc = s->kv_dev + d.L;
+        pa.rope = s->rope;
+        pa.b = s->b;
+        pa.tok_embd = s->m->tok_embd;
+        pa.lm_head = s->m->lm_head;
+        pa.pos = s->len;
+        pa.token = token;
+        pa.logits = logits ? 1 : 0;
+        pa.bar = s->bar;
+        pa.bar_base = s->bar_count;
+        pa.status = s->status;
+        pa.trace = s->trace;
+        pa.trace_events = s->trace_events;
+        if (decode_persistent(pa, s->st, s->m->nsm)) return DS4G_ECUDA;
+        // grid barriers per launch: six inside every layer, one between layers and
+        // one before the lm_head
+        s->bar_count += (unsigned)(7 * d.L - 1 + pa.logits) * (unsigned)s->m->nsm;
+        s->hist[s->len] = token;
+        s->len += 1;
+        return DS4G_OK;
+    }
     StepArgs a = step_base(s);
     a.pos = s->len;
     cudaEvent_t(*ev)[2] = s->timing ? s->ev : nullptr;
@@ -339,6 +395,11 @@ int ds4g_decode_step(ds4g_session *s, int32_t token)
         }
     }
     a.token = -1;
+    if (!logits) {
+        s->hist[s->len] = token;
+        s->len += 1;
+        return DS4G_OK;
+    }
     if (ev) cudaEventRecord(ev[DS4G_K_LM_HEAD][0], s->st);
     if (decode_lm_head(a, s->st, s->m->nsm)) return DS4G_ECUDA;
     if (ev) {
@@ -354,6 +415,10 @@ int ds4g_decode_step(ds4g_session *s, int32_t token)
     s->len += 1;
     return DS4G_OK;
 }
+
+int ds4g_decode_step(ds4g_session *s, int32_t token) { return decode_common(s, token, true); }
+
+int ds4g_decode_layers(ds4g_session *s, int32_t token) { return decode_common(s, token, false); }
 
 int ds4g_session_common_prefix(const ds4g_session *s, const int32_t *tokens, int n)
 {
@@ -373,6 +438,8 @@ int ds4g_session_truncate(ds4g_session *s, int common_prefix)
 int ds4g_session_len(const ds4g_session *s) { return s ? s->len : DS4G_EINVAL; }
 
 const float *ds4g_session_logits(const ds4g_session *s) { return s ? s->b.logits : nullptr; }
+
+const float *ds4g_session_hidden(const ds4g_session *s) { return s ? s->b.x : nullptr; }
 
 int ds4g_session_kv(ds4g_session *s, int layer, void **k, void **v)
 {
@@ -417,13 +484,31 @@ const void *ds4g_session_debug(const ds4g_session *s, int which)
     case DS4G_DBG_XN2: return s->b.xn2;
     case DS4G_DBG_SCORES: return s->b.scores;
     case DS4G_DBG_H: return s->b.h;
-    case DS4G_DBG_HIDDEN: return s->b.hidden;
+    case DS4G_DBG_HIDDEN: return s->b.x;
     case DS4G_DBG_PREFILL_X: return s->pb.X;
+    case DS4G_DBG_STATUS: return s->status;
     default: return nullptr;
     }
 }
 
 uint64_t ds4g_session_launches(const ds4g_session *s) { return s ? s->launches : 0; }
+
+int ds4g_session_status(ds4g_session *s)
+{
+    if (!s) return DS4G_EINVAL;
+    int st = 0;
+    cudaError_t e = cudaMemcpyAsync(&st, s->status, 4, cudaMemcpyDeviceToHost, s->st);
+    if (!e) e = cudaStreamSynchronize(s->st);
+    if (e) return DS4G_ECUDA;
+    if (st != 0) {  // clear the flag and the barrier counter a failed wait left behind
+        e = cudaMemsetAsync(s->bar, 0, 64, s->st);
+        if (!e) e = cudaStreamSynchronize(s->st);
+        s->bar_count = 0;
+        if (e) return DS4G_ECUDA;
+        return st == DS4G_ENONFINITE ? DS4G_ENONFINITE : DS4G_ETIMEOUT;
+    }
+    return DS4G_OK;
+}
 
 int ds4g_session_set_timing(ds4g_session *s, int on)
 {
@@ -440,6 +525,14 @@ int ds4g_session_set_timing(ds4g_session *s, int on)
         }
         s->timing = false;
     }
+    return DS4G_OK;
+}
+
+int ds4g_session_set_trace(ds4g_session *s, void *buf, size_t bytes)
+{
+    if (!s) return DS4G_EINVAL;
+    s->trace = static_cast<unsigned long long *>(buf);
+    s->trace_events = buf ? (int)(bytes / (8 * (size_t)s->m->nsm)) : 0;
     return DS4G_OK;
 }
 
@@ -518,6 +611,7 @@ const char *ds4g_strerror(int code)
     case DS4G_ECUDA: return "CUDA call or kernel launch failed";
     case DS4G_ETIMEOUT: return "a bounded device-side wait gave up";
     case DS4G_ESIZE: return "buffer too small";
+    case DS4G_ENONFINITE: return "a router score was not finite";
     default: return "unknown error";
     }
 }

@@ -42,6 +42,7 @@ struct DecodeBufs {
     float *logits;   // [V]
     float *hidden;   // [H]   final hidden state
     unsigned *counters;  // [8] grid-completion tickets (reset by their last user)
+    int *status;         // session status word (DS4G_* error raised on the device)
 };
 
 // Arguments of every decode kernel: one layer at one position.
@@ -54,6 +55,24 @@ struct StepArgs {
     const uint16_t *tok_embd;
     const void *lm_head;
     int layer, pos, token;  // token >= 0 only for the first layer's first kernel
+};
+
+// Arguments of the persistent decode kernel: every layer of one token.
+struct PersistArgs {
+    Dims d;
+    const LayerPtrs *layers;   // device [L]
+    void *const *kc;           // device [L]
+    void *const *vc;           // device [L]
+    const float2 *rope;
+    DecodeBufs b;
+    const uint16_t *tok_embd;
+    const void *lm_head;
+    int pos, token, logits;
+    unsigned *bar;             // grid-barrier arrival counter (only grows)
+    unsigned bar_base;         // its value when this launch starts
+    int *status;               // DS4G_ETIMEOUT if a barrier wait gave up
+    unsigned long long *trace; // optional [events][gridDim] stage start times (ns)
+    int trace_events;
 };
 
 // ------------------------------------------------------------------ device helpers
@@ -84,6 +103,20 @@ __device__ __forceinline__ uint4 ld_stream(const void *ptr, uint64_t pol)
     return r;
 }
 
+// Asynchronous bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 16-byte asynchronous global -> shared copy (no register staging) and its wait.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -96,6 +129,91 @@ __device__ __forceinline__ float warp_max(float v)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
+}
+
+// Top-k of the scores s[0..E) (E <= 1024) by one warp: values sel[k] and ids[k],
+// largest first, equal scores to the lower id.  A NaN ranks as -inf, so the K ids
+// are always distinct valid experts; returns false if a selected score was not
+// finite (the caller raises DS4G_ENONFINITE).
+//  - E <= 256: lane l holds experts l, l+32, ... (at most eight), sorted once by a
+//    19-comparator network; each of the K rounds is then one warp arg-max over the
+//    lanes' heads, and the winning lane shifts its list.
+//  - larger E: each round rescans the lane's untaken experts.
+__device__ __forceinline__ bool topk_better(float va, int ia, float vb, int ib)
+{
+    return va > vb || (va == vb && ia < ib);
+}
+__device__ __forceinline__ bool warp_topk(const float *s, int E, int K, float *sel, int *ids, int lane)
+{
+    bool finite = true;
+    if (E <= 256) {
+        float v[8];
+        int id[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = lane + 32 * u;
+            const float x = e < E ? s[e] : -INFINITY;
+            v[u] = x != x ? -INFINITY : x;
+            id[u] = e < E ? e : 0x7fffffff;   // padding: loses every tie to a real expert
+        }
+        constexpr int net[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
+                                    {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
+                                    {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+        for (int c = 0; c < 19; ++c) {
+            const int i = net[c][0], j = net[c][1];
+            if (topk_better(v[j], id[j], v[i], id[i])) {
+                const float tv = v[i]; v[i] = v[j]; v[j] = tv;
+                const int ti = id[i]; id[i] = id[j]; id[j] = ti;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {   // K <= 8
+            if (k >= K) break;
+            float bv = v[0];
+            int bi = id[0];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (topk_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            sel[k] = bv;
+            ids[k] = bi;
+            finite = finite && isfinite(bv);
+            if (id[0] == bi) {   // this lane's head was taken
+#pragma unroll
+                for (int u = 0; u < 7; ++u) { v[u] = v[u + 1]; id[u] = id[u + 1]; }
+                v[7] = -INFINITY;
+                id[7] = 0x7fffffff;
+            }
+        }
+        return finite;
+    }
+    unsigned taken = 0u;  // bit j: expert lane + 32 j is already chosen
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {   // K <= 8; fixed bounds keep sel/ids in registers
+        if (k >= K) break;
+        float bv = -INFINITY;
+        int bi = E;  // above every id: any untaken expert beats it
+        for (int e = lane, j = 0; e < E; e += 32, ++j) {
+            if ((taken >> j) & 1u) continue;
+            float v = s[e];
+            if (v != v) v = -INFINITY;
+            if (topk_better(v, e, bv, bi)) { bv = v; bi = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (topk_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        sel[k] = bv;
+        ids[k] = bi;
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        finite = finite && isfinite(bv);
+    }
+    return finite;
 }
 
 template <typename T> struct VecOf;

@@ -11,6 +11,11 @@ cudaError_t decode_layer(const StepArgs &a, cudaStream_t st, int nsm,
                          cudaEvent_t (*ev)[2] = nullptr);
 cudaError_t decode_lm_head(const StepArgs &a, cudaStream_t st, int nsm);
 
+// decode_persistent.cu
+size_t persistent_smem(const Dims &d);
+cudaError_t persistent_setup(const Dims &d, int max_smem, int nsm, bool *ok);
+cudaError_t decode_persistent(const PersistArgs &a, cudaStream_t st, int nsm);
+
 // sampler.cu
 size_t sample_workspace_bytes(int n);
 cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p,
@@ -36,6 +41,7 @@ struct PrefillBufs {
     void *HG;         // [P*K][I] routed SwiGLU hidden, grouped order
     void *HS;         // [P][I] shared SwiGLU hidden
     float *YS;        // [P*K][H] routed expert outputs, token-slot order
+    int *status;      // session status word (set after carving)
 };
 size_t prefill_bytes(const Dims &d, int P);
 void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb);

@@ -51,32 +51,14 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *X, const floa
 
 // Router decision per token: top-k of the scores (ties to the lower id), softmax
 // over the selected scores.  One warp per token.
-__global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E, int K)
+__global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E, int K, int *status)
 {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= n) return;
-    const float *s = S + (size_t)warp * E;
-    unsigned taken = 0u;  // bit j: this lane's j-th expert (e = lane + 32 j) is chosen
     float sel[8];
     int sid[8];
-    for (int k = 0; k < K; ++k) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int e = lane, j = 0; e < E; e += 32, ++j) {
-            if ((taken >> j) & 1u) continue;
-            const float v = s[e];
-            if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        sel[k] = bv;
-        sid[k] = bi;
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    }
+    const bool finite = warp_topk(S + (size_t)warp * E, E, K, sel, sid, lane);
+    if (!finite && lane == 0) atomicCAS(status, 0, DS4G_ENONFINITE);
     if (lane == 0) {
         float sum = 0.f, w[8];
         for (int k = 0; k < K; ++k) { w[k] = expf(sel[k] - sel[0]); sum += w[k]; }
@@ -451,7 +433,7 @@ static cudaError_t chunk_t(const Dims &d, const LayerPtrs *layers, void *const *
         ++launch_count();
         ProbRouter<TW> pr{pb.XN32, (const TW *)w.w_router, pb.S, H, d.E};
         if ((e = gemm_dense<float, TW>(pr, n, d.E, H, st, nsm))) return e;
-        k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K);
+        k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K, pb.status);
         ++launch_count();
         k_group_count<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.cnt);
         ++launch_count();

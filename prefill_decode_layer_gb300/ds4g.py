@@ -13,9 +13,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libds4g.so")
 
 F32, BF16 = 0, 1
-OK, EINVAL, ECONTEXT, ETOKEN, ECUDA, ETIMEOUT, ESIZE = 0, -1, -2, -3, -4, -5, -6
+OK, EINVAL, ECONTEXT, ETOKEN, ECUDA, ETIMEOUT, ESIZE, ENONFINITE = 0, -1, -2, -3, -4, -5, -6, -7
 DEBUG = {"x": 0, "cqkv": 1, "q": 2, "attn": 3, "xmid": 4, "xn2": 5, "scores": 6, "h": 7,
-         "hidden": 8, "prefill_x": 9}
+         "hidden": 8, "prefill_x": 9, "status": 10}
 
 
 KERNEL_KINDS = ("qkv_a", "qkv_b", "attn", "wo", "router", "expert_gu", "expert_down", "lm_head")
@@ -32,7 +32,7 @@ class Config(C.Structure):
                                        "kv_rank", "window", "n_experts", "top_k",
                                        "expert_inter", "vocab")] + \
                [("rope_base", C.c_float), ("rms_eps", C.c_float), ("weight_dtype", C.c_int),
-                ("kv_dtype", C.c_int), ("prefill_chunk", C.c_int)]
+                ("kv_dtype", C.c_int), ("prefill_chunk", C.c_int), ("decode_kernel", C.c_int)]
 
 
 LAYER_FIELDS = ("attn_norm", "wq_a", "wq_b", "wkv_a", "wk_b", "wv_b", "wo", "ffn_norm",
@@ -67,6 +67,8 @@ def lib():
             "ds4g_session_destroy": ([vp], None),
             "ds4g_prefill": ([vp, vp, i32], i32),
             "ds4g_decode_step": ([vp, C.c_int32], i32),
+            "ds4g_decode_layers": ([vp, C.c_int32], i32),
+            "ds4g_session_hidden": ([vp], vp),
             "ds4g_session_common_prefix": ([vp, vp, i32], i32),
             "ds4g_session_truncate": ([vp, i32], i32),
             "ds4g_session_len": ([vp], i32),
@@ -77,6 +79,8 @@ def lib():
             "ds4g_session_debug": ([vp, i32], vp),
             "ds4g_sample_workspace_bytes": ([i32], sz),
             "ds4g_session_launches": ([vp], C.c_uint64),
+            "ds4g_session_status": ([vp], i32),
+            "ds4g_session_set_trace": ([vp, vp, sz], i32),
             "ds4g_session_set_timing": ([vp, i32], i32),
             "ds4g_session_timing": ([vp, vp, vp, i32], i32),
             "ds4g_sample": ([vp, i32, C.c_float, C.c_float, vp, vp, sz, vp], C.c_int32),
@@ -97,7 +101,10 @@ def _check(rc: int, what: str) -> int:
     return rc
 
 
-def config_struct(shape, prefill_chunk: int = 0) -> Config:
+DECODE_AUTO, DECODE_STAGED = 0, 1
+
+
+def config_struct(shape, prefill_chunk: int = 0, decode_kernel: int = DECODE_AUTO) -> Config:
     c = Config()
     for n in ("n_layers", "hidden", "n_heads", "head_dim", "q_rank", "kv_rank", "window",
               "n_experts", "top_k", "expert_inter", "vocab"):
@@ -107,6 +114,7 @@ def config_struct(shape, prefill_chunk: int = 0) -> Config:
     c.weight_dtype = F32 if shape.weight_dtype == "f32" else BF16
     c.kv_dtype = F32 if shape.kv_dtype == "f32" else BF16
     c.prefill_chunk = int(prefill_chunk)
+    c.decode_kernel = int(decode_kernel)
     return c
 
 
@@ -125,9 +133,9 @@ class Model:
     """Weights are device tensors owned by the caller (kept referenced here)."""
 
     def __init__(self, shape, tok_embd: torch.Tensor, lm_head: torch.Tensor, layers: list,
-                 prefill_chunk: int = 0):
+                 prefill_chunk: int = 0, decode_kernel: int = DECODE_AUTO):
         self.shape = shape
-        self.cfg = config_struct(shape, prefill_chunk)
+        self.cfg = config_struct(shape, prefill_chunk, decode_kernel)
         self._keep = (tok_embd, lm_head, layers)
         arr = (LayerWeights * len(layers))()
         for i, w in enumerate(layers):
@@ -174,6 +182,14 @@ class Session:
     def decode(self, token: int) -> int:
         return lib().ds4g_decode_step(self.ptr, int(token))
 
+    def decode_layers(self, token: int) -> int:
+        """One token through every layer without the lm_head."""
+        return lib().ds4g_decode_layers(self.ptr, int(token))
+
+    def hidden(self) -> torch.Tensor:
+        return self._view(lib().ds4g_session_hidden(self.ptr), self.model.shape.hidden,
+                          torch.float32)
+
     def truncate(self, cp: int) -> int:
         return lib().ds4g_session_truncate(self.ptr, int(cp))
 
@@ -211,6 +227,15 @@ class Session:
         n = self.n_ctx * s.head_dim
         return (self._view(k.value, n, dt).view(self.n_ctx, s.head_dim),
                 self._view(v.value, n, dt).view(self.n_ctx, s.head_dim))
+
+    def set_trace(self, buf) -> None:
+        """buf: a device tensor receiving per-CTA stage start times (or None)."""
+        _check(lib().ds4g_session_set_trace(self.ptr, buf.data_ptr() if buf is not None else None,
+                                            buf.numel() * buf.element_size() if buf is not None
+                                            else 0), "ds4g_session_set_trace")
+
+    def status(self) -> int:
+        return lib().ds4g_session_status(self.ptr)
 
     @property
     def launches(self) -> int:

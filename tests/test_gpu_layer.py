@@ -5,21 +5,21 @@ import numpy as np
 import pytest
 
 import synth
-from helpers import (TOL_BF16, LazyOracleModel, OracleKV, gpu_model, kv_to_f64, oracle_embed,
-                     oracle_layer, rel_err, to_np)
+from helpers import (DECODE_KERNELS, TOL_BF16, LazyOracleModel, OracleKV, gpu_model, kv_to_f64,
+                     oracle_embed, oracle_layer, rel_err, to_np)
 
 pytestmark = pytest.mark.gpu
 
 N_PRE = 4096
 
 
-@pytest.fixture(scope="module")
-def layer_setup():
+@pytest.fixture(scope="module", params=DECODE_KERNELS, ids=["persistent", "staged"])
+def layer_setup(request):
     import torch
     import prefill_decode_layer_gb300 as pdl
     from synth import torch_weights as tw
     shape = synth.LAYER
-    gm = gpu_model(shape)
+    gm = gpu_model(shape, decode_kernel=request.param)
     n_ctx = N_PRE + 200
     sess = pdl.Session(gm, n_ctx)
     k, v = sess.kv(0)
@@ -50,7 +50,7 @@ def test_decode_steps_match_oracle(layer_setup):
     ties = 0
     for s, t in enumerate(toks):
         pos = N_PRE + s
-        assert sess.decode(int(t)) == 0
+        assert sess.decode_layers(int(t)) == 0
         x = oracle_embed(om, t)
         tr = oracle_layer(om, kv, 0, pos, x, trace=True)
         torch.cuda.synchronize()
@@ -69,7 +69,8 @@ def test_decode_steps_match_oracle(layer_setup):
             assert ids == list(tr["ids"]), f"step {s}: {ids} vs {list(tr['ids'])}"
             assert rel_err(w, tr["weights"]) <= TOL_BF16
             assert rel_err(to_np(sess.debug("h", (K + 1) * I)), tr["h"]) <= TOL_BF16
-            assert rel_err(to_np(sess.debug("x", H)), x) <= TOL_BF16
+            assert rel_err(to_np(sess.hidden()), x) <= TOL_BF16
         else:
             ties += 1
     assert ties <= 1
+    assert sess.status() == 0

@@ -6,18 +6,18 @@ import pytest
 
 import oracle
 import synth
-from helpers import (TOL_F32, LazyOracleModel, OracleKV, gpu_model, kv_to_f64, oracle_embed,
-                     oracle_layer, oracle_lm_head, rel_err, to_np)
+from helpers import (DECODE_KERNELS, TOL_F32, LazyOracleModel, OracleKV, gpu_model, kv_to_f64,
+                     oracle_embed, oracle_layer, oracle_lm_head, rel_err, to_np)
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def tiny():
+@pytest.fixture(scope="module", params=DECODE_KERNELS, ids=["persistent", "staged"])
+def tiny(request):
     import torch
     torch.cuda.init()
     shape = synth.TINY
-    return shape, gpu_model(shape), LazyOracleModel(shape)
+    return shape, gpu_model(shape, decode_kernel=request.param), LazyOracleModel(shape)
 
 
 def test_tiny_prefill_then_greedy_decode(tiny):
