@@ -263,6 +263,25 @@ int32_t ds4g_sample(const float *logits, int n_vocab, float temperature, float t
 int32_t ds4g_sample_u(const float *logits, int n_vocab, float temperature, float top_p,
                       uint32_t u24, void *workspace, size_t workspace_bytes, void *cuda_stream);
 
+/* Largest vocabulary ds4g_sample_static accepts. */
+#define DS4G_SAMPLE_STATIC_MAX_VOCAB 262144
+
+/* ds4g_sample without a caller workspace.  The pages have no counterpart: this is
+ * a library convenience.  It is for callers that cannot allocate device memory
+ * for a workspace: a host program that only holds a logits pointer produced by
+ * another library (it owns no device allocator), or a decode loop that must not
+ * call cudaMalloc between steps, because cudaMalloc can synchronise the device.
+ * Its scratch is a fixed 16 KB array in the library's device image, which exists
+ * once the module is loaded; the call allocates nothing.  n_vocab above
+ * DS4G_SAMPLE_STATIC_MAX_VOCAB returns DS4G_ESIZE; other arguments and the result
+ * are as for ds4g_sample.  The first call on each device resolves the scratch
+ * address (runtime set-up), so make it before any stream capture.  There is one
+ * scratch per device: calls that overlap in time on one device (two host threads,
+ * or two streams whose calls are not ordered) race on it and give undefined
+ * results.  Synchronises `cuda_stream`. */
+int32_t ds4g_sample_static(const float *logits, int n_vocab, float temperature, float top_p,
+                           uint64_t *rng_state, void *cuda_stream);
+
 const char *ds4g_strerror(int code);
 
 #ifdef __cplusplus

@@ -6,4 +6,4 @@ of the computation runs in its CUDA kernels.  Importing the binding fails loudly
 if the library has not been built.
 """
 from .ds4g import (BF16, DEBUG, F32, Ds4gError, Model, Session, config_struct, lib,  # noqa: F401
-                   sample, sample_u, sample_workspace_bytes, session_bytes)
+                   sample, sample_static, sample_u, sample_workspace_bytes, session_bytes)

@@ -601,6 +601,21 @@ int32_t ds4g_sample_u(const float *logits, int n_vocab, float temperature, float
                          stream);
 }
 
+static_assert(DS4G_SAMPLE_STATIC_MAX_VOCAB == kSampleStaticMaxVocab, "header and library agree");
+
+int32_t ds4g_sample_static(const float *logits, int n_vocab, float temperature, float top_p,
+                           uint64_t *rng_state, void *stream)
+{
+    if (!logits || n_vocab < 1 || temperature != temperature || top_p != top_p) return DS4G_EINVAL;
+    if (n_vocab > DS4G_SAMPLE_STATIC_MAX_VOCAB) return DS4G_ESIZE;
+    if (temperature > 0.f && (!rng_state || *rng_state == 0)) return DS4G_EINVAL;
+    void *scratch = nullptr;
+    if (sample_static_scratch(&scratch)) return DS4G_ECUDA;
+    unsigned u24 = 0;
+    if (temperature > 0.f) u24 = (unsigned)(xorshift64s(rng_state) >> 40);
+    return sample_common(logits, n_vocab, temperature, top_p, u24, scratch, kSampleStaticBytes, stream);
+}
+
 const char *ds4g_strerror(int code)
 {
     switch (code) {

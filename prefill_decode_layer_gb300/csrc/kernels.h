@@ -18,6 +18,11 @@ cudaError_t decode_persistent(const PersistArgs &a, cudaStream_t st, int nsm);
 
 // sampler.cu
 size_t sample_workspace_bytes(int n);
+// Fixed sampler scratch (ds4g_sample_static): vocabularies up to kSampleStaticMaxVocab.
+constexpr int kSampleStaticMaxVocab = 262144;
+constexpr size_t kSampleStaticBytes = 16384;
+constexpr int kMaxDevices = 64;
+cudaError_t sample_static_scratch(void **p);
 cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p,
                           unsigned u24, void *ws, cudaStream_t st, int **result_dev);
 

@@ -17,6 +17,8 @@
 //            R = max(1, ceil(u * kept_total)) (u = k / 2^24 exactly).
 // T <= 0.   argmax: max of (ordered logit bits, inverted index) as one u64.
 #include "common.cuh"
+#include <mutex>
+
 #include "kernels.h"
 
 namespace ds4g {
@@ -340,6 +342,32 @@ cudaError_t sample_launch(const float *logits, int n, float temperature, float t
                                          chunk_ties);
     ++launch_count();
     return cudaGetLastError();
+}
+
+// Fixed scratch for ds4g_sample_static: the workspace of the largest vocabulary it
+// accepts, in device memory that exists from module load (no allocation).
+static __device__ __align__(256) unsigned char g_sample_scratch[kSampleStaticBytes];
+static_assert(kSampleStaticBytes >= sizeof(SampleWS) + ((kSampleStaticMaxVocab + kChunk - 1) / kChunk) * 12 + 256,
+              "static sampler scratch too small for its maximum vocabulary");
+
+// Device address of the fixed scratch on the current device.  The first call per
+// device resolves the symbol (runtime set-up); later calls reuse the cached value.
+cudaError_t sample_static_scratch(void **p)
+{
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        void *a = nullptr;
+        if ((e = cudaGetSymbolAddress(&a, g_sample_scratch))) return e;
+        addr[dev] = a;
+    }
+    *p = addr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace ds4g

@@ -68,6 +68,7 @@ def lib():
             "ds4g_prefill": ([vp, vp, i32], i32),
             "ds4g_decode_step": ([vp, C.c_int32], i32),
             "ds4g_decode_layers": ([vp, C.c_int32], i32),
+            "ds4g_sample_static": ([vp, i32, C.c_float, C.c_float, vp, vp], C.c_int32),
             "ds4g_session_hidden": ([vp], vp),
             "ds4g_session_common_prefix": ([vp, vp, i32], i32),
             "ds4g_session_truncate": ([vp, i32], i32),
@@ -271,6 +272,15 @@ def sample(logits: torch.Tensor, temperature: float, top_p: float, rng_state: in
     tok = lib().ds4g_sample(logits.data_ptr(), logits.numel(), float(temperature), float(top_p),
                             C.byref(st), workspace.data_ptr(), workspace.numel(),
                             _stream_ptr(stream))
+    return tok, st.value
+
+
+def sample_static(logits: torch.Tensor, temperature: float, top_p: float,
+                  rng_state: int | None, stream=None):
+    """ds4g_sample_static: no workspace argument; returns (token, new_rng_state)."""
+    st = C.c_uint64(rng_state or 0)
+    tok = lib().ds4g_sample_static(logits.data_ptr(), logits.numel(), float(temperature),
+                                   float(top_p), C.byref(st), _stream_ptr(stream))
     return tok, st.value
 
 
