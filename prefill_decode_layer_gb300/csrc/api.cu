@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "prefill_tc.h"
 
 using namespace ds4g;
 
@@ -20,6 +21,8 @@ struct ds4g_model {
     const void *lm_head;
     int nsm;
     bool persistent;   // decode steps use the single cooperative launch
+    bool tc;           // prefill GEMMs run on the tensor cores
+    std::vector<TcLayerMaps> tcmaps;   // per layer, when tc
 };
 
 struct ds4g_session {
@@ -32,6 +35,7 @@ struct ds4g_session {
     float2 *rope;
     DecodeBufs b;
     PrefillBufs pb;
+    TcActMaps tcact;            // tensor maps of pb's activations, when the model's prefill is tc
     LayerPtrs *layers_dev;      // [L] device copy of the layer table
     void **kv_dev;              // [2L] device K then V cache pointers
     unsigned *bar;              // grid-barrier arrival counter of the persistent kernel
@@ -219,6 +223,11 @@ int ds4g_model_create(const ds4g_config *cfg, const ds4g_weights *w, ds4g_model 
     m->persistent = false;
     if (!e && cfg->decode_kernel == DS4G_DECODE_AUTO)
         e = persistent_setup(m->d, max_smem, m->nsm, &m->persistent);
+    m->tc = !e && cfg->prefill_kernel == DS4G_PREFILL_AUTO && tc_prefill_eligible(m->d);
+    if (m->tc) {
+        m->tcmaps.resize(m->layers.size());
+        for (size_t l = 0; !e && l < m->layers.size(); ++l) e = tc_layer_maps(m->d, m->layers[l], m->tcmaps[l]);
+    }
     if (e) {
         if (getenv("DS4G_VERBOSE")) fprintf(stderr, "ds4g_model_create: %s\n", cudaGetErrorString(e));
         delete m;
@@ -285,6 +294,10 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     s->kv_host.insert(s->kv_host.end(), s->vc.begin(), s->vc.end());
     prefill_carve(d, prefill_P(m->cfg), base + L.pre, s->pb);
     s->pb.status = s->status;
+    if (m->tc && tc_act_maps(d, s->pb, s->tcact)) {
+        delete s;
+        return DS4G_ECUDA;
+    }
     cudaError_t e = cudaMemsetAsync(base + L.dec, 0, L.pre - L.dec, s->st);
     if (!e) e = cudaMemcpyAsync(s->layers_dev, m->layers.data(), (size_t)d.L * sizeof(LayerPtrs),
                                 cudaMemcpyHostToDevice, s->st);
@@ -326,8 +339,11 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
         const int nc = n - c < P ? n - c : P;
         cudaError_t e = cudaMemcpyAsync(s->pb.tok, tokens + c, (size_t)nc * 4,
                                         cudaMemcpyHostToDevice, s->st);
-        if (!e) e = prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,
-                                  s->m->tok_embd, s->pb, s->len + c, nc, s->st, s->m->nsm);
+        if (!e)
+            e = s->m->tc ? prefill_chunk_tc(d, s->m->layers.data(), s->m->tcmaps.data(), s->tcact, s->kc.data(),
+                                            s->vc.data(), s->rope, s->m->tok_embd, s->pb, s->len + c, nc, s->st)
+                         : prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,
+                                         s->m->tok_embd, s->pb, s->len + c, nc, s->st, s->m->nsm);
         if (!e && c + nc == n) {  // last token's hidden state, then its logits
             e = cudaMemcpyAsync(s->b.x, s->pb.X + (size_t)(nc - 1) * d.H, (size_t)d.H * 4,
                                 cudaMemcpyDeviceToDevice, s->st);

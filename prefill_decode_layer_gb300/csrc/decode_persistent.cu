@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace ds4g {
 
@@ -39,75 +40,9 @@ static constexpr int kCT = kNC * 32;                // consumer threads
 static constexpr int kPThreads = kCT + 32;          // + the producer warp
 static constexpr int kSlot = 16384;                 // bytes per ring slot
 static constexpr int kMaxR = 32;                    // rows per item at most
-static constexpr long long kWaitCycles = 4000000000ll;   // ~2 s at 2 GHz per wait at most
 
-// ------------------------------------------------------------------ PTX helpers
+// ------------------------------------------------------------------ helpers
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ unsigned long long global_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *b)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase of `parity` to complete; false if it gave up or the
-// CTA is aborting.  The bound uses the SM cycle counter, read once per 256 polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag)
-{
-    if (mbar_try_wait(b, parity)) return true;
-    const long long t0 = clock64();
-    for (unsigned n = 1;; ++n) {
-        if (mbar_try_wait(b, parity)) return true;
-        if ((n & 255u) == 0 && (*abort_flag || clock64() - t0 > kWaitCycles)) return false;
-    }
-}
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                         uint64_t pol)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-        : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 // Barrier among the consumer warps only (the producer never joins).
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory"); }
 
@@ -1181,7 +1116,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_decode_persistent(const __grid
         mbar_init(&S.scores_ready, 1);
         mbar_init(&S.ids_ready, 1);
         S.abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_fence_init();
     }
     __syncthreads();   // the only whole-CTA barrier: roles split below
     if ((threadIdx.x >> 5) == kNC)

@@ -17,6 +17,8 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "kernels.h"
+#include "prefill_problems.cuh"
+#include "prefill_tc.h"
 
 namespace ds4g {
 
@@ -135,8 +137,10 @@ __global__ void __launch_bounds__(256) k_group_fill(const int *ids, int nent, co
 
 // Windowed causal multi-query attention for a chunk: CTA (token t, group of heads).
 // The window's K/V rows are staged once in shared memory for all heads of the group.
-template <typename TA, typename TKV>
-__global__ void __launch_bounds__(256) k_attn_prefill(const TA *Q, TA *O, const TKV *kc,
+// HILO: the output is written as BF16 hi/lo pairs (O and Olo) for the tensor-core
+// W_o GEMM instead of in the activation type.
+template <typename TA, typename TKV, bool HILO = false>
+__global__ void __launch_bounds__(256) k_attn_prefill(const TA *Q, void *Ov, bf16 *Olo, const TKV *kc,
                                                       const TKV *vc, int p0, Dims d, int hg)
 {
     extern __shared__ __align__(16) unsigned char sm[];
@@ -196,142 +200,19 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const TA *Q, TA *O, const 
         for (int i = lane; i < HD; i += 32) {
             float acc = 0.f;
             for (int j = 0; j < n; ++j) acc = fmaf(p[j], to_f32<TKV>(Vs[(size_t)j * HD + i]), acc);
-            O[(size_t)t * d.QD + (size_t)h * HD + i] = from_f32<TA>(acc * inv);
+            const size_t oi = (size_t)t * d.QD + (size_t)h * HD + i;
+            if constexpr (HILO) {
+                const float ov = acc * inv;
+                const bf16 hv = __float2bfloat16_rn(ov);
+                static_cast<bf16 *>(Ov)[oi] = hv;
+                Olo[oi] = __float2bfloat16_rn(ov - __bfloat162float(hv));
+            } else {
+                static_cast<TA *>(Ov)[oi] = from_f32<TA>(acc * inv);
+            }
         }
         __syncwarp();
     }
 }
-
-// ------------------------------------------------------------------ GEMM problems
-// Each problem maps rows of A, rows of W (an [N][K] row-major operand) and a 4-wide
-// column group of outputs; see gemm.cuh for the kernels that drive them.
-
-template <typename TA, typename TW>
-struct ProbQKVA {  // C = XN [W_qa; W_kva]^T
-    const TA *XN; const TW *wqa, *wkva; TA *C; int H, RQ, ldc;
-    __device__ const TA *a_row(int m, int) const { return XN + (size_t)m * H; }
-    __device__ const TW *w_row(int n, int) const {
-        return n < RQ ? wqa + (size_t)n * H : wkva + (size_t)(n - RQ) * H;
-    }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) C[(size_t)m * ldc + n + j] = from_f32<TA>(v[j]);
-    }
-};
-
-template <typename TA, typename TW>
-struct ProbQB {  // Q = RoPE(C[:, :RQ] W_qb^T)
-    const TA *C; const TW *wqb; TA *Q; const float2 *rope; int ldc, RQ, QD, HD, p0;
-    __device__ const TA *a_row(int m, int) const { return C + (size_t)m * ldc; }
-    __device__ const TW *w_row(int n, int) const { return wqb + (size_t)n * RQ; }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-        const float2 *rp = rope + (size_t)(p0 + m) * (HD / 2);
-#pragma unroll
-        for (int j = 0; j < 4; j += 2) {
-            const float2 cs = rp[((n + j) % HD) / 2];
-            Q[(size_t)m * QD + n + j] = from_f32<TA>(v[j] * cs.x - v[j + 1] * cs.y);
-            Q[(size_t)m * QD + n + j + 1] = from_f32<TA>(v[j] * cs.y + v[j + 1] * cs.x);
-        }
-    }
-};
-
-template <typename TA, typename TW, typename TKV>
-struct ProbKVB {  // K = RoPE(C[:, RQ:] W_kb^T), V = C[:, RQ:] W_vb^T, appended to the cache
-    const TA *C; const TW *wkb, *wvb; TKV *kc, *vc; const float2 *rope; int ldc, RQ, RKV, HD, p0;
-    __device__ const TA *a_row(int m, int) const { return C + (size_t)m * ldc + RQ; }
-    __device__ const TW *w_row(int n, int) const {
-        return n < HD ? wkb + (size_t)n * RKV : wvb + (size_t)(n - HD) * RKV;
-    }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-        const size_t row = (size_t)(p0 + m) * HD;
-        if (n < HD) {
-            const float2 *rp = rope + (size_t)(p0 + m) * (HD / 2);
-#pragma unroll
-            for (int j = 0; j < 4; j += 2) {
-                const float2 cs = rp[(n + j) / 2];
-                kc[row + n + j] = from_f32<TKV>(v[j] * cs.x - v[j + 1] * cs.y);
-                kc[row + n + j + 1] = from_f32<TKV>(v[j] * cs.y + v[j + 1] * cs.x);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) vc[row + n - HD + j] = from_f32<TKV>(v[j]);
-        }
-    }
-};
-
-template <typename TA, typename TW>
-struct ProbWO {  // X += O W_o^T
-    const TA *O; const TW *wo; float *X; int QD, H;
-    __device__ const TA *a_row(int m, int) const { return O + (size_t)m * QD; }
-    __device__ const TW *w_row(int n, int) const { return wo + (size_t)n * QD; }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) X[(size_t)m * H + n + j] += v[j];
-    }
-};
-
-template <typename TW>
-struct ProbRouter {  // S = XN W_r^T from f32 activations (f32 scores)
-    const float *XN; const TW *wr; float *S; int H, E;
-    __device__ const float *a_row(int m, int) const { return XN + (size_t)m * H; }
-    __device__ const TW *w_row(int n, int) const { return wr + (size_t)n * H; }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) S[(size_t)m * E + n + j] = v[j];
-    }
-};
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
-
-// Gate/up with SwiGLU; W rows interleaved (gate_i, up_i) so an output pair is local.
-template <typename TA, typename TW, bool GROUPED>
-struct ProbGU {
-    const TA *XN; const int *rows; const TW *wg, *wu; TA *Hout; int H, I, K;
-    size_t estride;  // elements between experts' matrices (I * H)
-    __device__ const TA *a_row(int m, int) const {
-        return XN + (size_t)(GROUPED ? rows[m] / K : m) * H;
-    }
-    __device__ const TW *w_row(int n, int e) const {
-        const TW *b = (n & 1) ? wu : wg;
-        return b + (GROUPED ? (size_t)e * estride : 0) + (size_t)(n >> 1) * H;
-    }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-        Hout[(size_t)m * I + (n >> 1)] = from_f32<TA>(silu_mul(v[0], v[1]));
-        Hout[(size_t)m * I + (n >> 1) + 1] = from_f32<TA>(silu_mul(v[2], v[3]));
-    }
-};
-
-template <typename TA, typename TW>
-struct ProbDown {  // YS[token*K + slot] = HG W_d(e)^T, grouped rows
-    const TA *HG; const int *rows; const TW *wd; float *YS; int H, I;
-    __device__ const TA *a_row(int m, int) const { return HG + (size_t)m * I; }
-    __device__ const TW *w_row(int n, int e) const {
-        return wd + (size_t)e * H * I + (size_t)n * I;
-    }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-        float *y = YS + (size_t)rows[m] * H + n;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) y[j] = v[j];
-    }
-};
-
-template <typename TA, typename TW>
-struct ProbSharedDown {  // X += HS W_sd^T + sum_s w[s] YS[token, s]  (slot order, then shared)
-    const TA *HS; const TW *wsd; const float *YS; const float *wts; float *X; int H, I, K;
-    __device__ const TA *a_row(int m, int) const { return HS + (size_t)m * I; }
-    __device__ const TW *w_row(int n, int) const { return wsd + (size_t)n * I; }
-    __device__ void store4(int m, int n, const float (&v)[4], int) const {
-        float r[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s = 0; s < K; ++s) {
-            const float w = wts[(size_t)m * K + s];
-            const float *y = YS + ((size_t)m * K + s) * H + n;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) r[j] = fmaf(w, y[j], r[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) X[(size_t)m * H + n + j] += r[j] + v[j];
-    }
-};
 
 // ------------------------------------------------------------------ host side
 
@@ -393,10 +274,28 @@ static size_t attn_prefill_smem(const Dims &d)
 
 cudaError_t prefill_setup(const Dims &d, int max_smem)
 {
-    return d.kvdt == DS4G_BF16
-               ? allow_max_dyn_smem((const void *)k_attn_prefill<float, bf16>, max_smem)
-               : allow_max_dyn_smem((const void *)k_attn_prefill<float, float>, max_smem);
+    cudaError_t e = d.kvdt == DS4G_BF16
+                        ? allow_max_dyn_smem((const void *)k_attn_prefill<float, bf16>, max_smem)
+                        : allow_max_dyn_smem((const void *)k_attn_prefill<float, float>, max_smem);
+    if (e) return e;
+    return d.kvdt == DS4G_BF16 ? allow_max_dyn_smem((const void *)k_attn_prefill<float, bf16, true>, max_smem)
+                               : allow_max_dyn_smem((const void *)k_attn_prefill<float, float, true>, max_smem);
 }
+
+template <typename TKV>
+cudaError_t attn_prefill_hilo(const Dims &d, const float *Q, bf16 *o_hi, bf16 *o_lo, const TKV *kc,
+                              const TKV *vc, int p0, int n, cudaStream_t st)
+{
+    const int hg = d.NH < 16 ? d.NH : 16;
+    k_attn_prefill<float, TKV, true><<<dim3(n, (d.NH + hg - 1) / hg), 256, attn_prefill_smem(d), st>>>(
+        Q, o_hi, o_lo, kc, vc, p0, d, hg);
+    ++launch_count();
+    return cudaGetLastError();
+}
+template cudaError_t attn_prefill_hilo<bf16>(const Dims &, const float *, bf16 *, bf16 *, const bf16 *,
+                                             const bf16 *, int, int, cudaStream_t);
+template cudaError_t attn_prefill_hilo<float>(const Dims &, const float *, bf16 *, bf16 *, const float *,
+                                              const float *, int, int, cudaStream_t);
 
 template <typename TA, typename TW, typename TKV>
 static cudaError_t chunk_t(const Dims &d, const LayerPtrs *layers, void *const *kcs,
@@ -424,7 +323,7 @@ static cudaError_t chunk_t(const Dims &d, const LayerPtrs *layers, void *const *
         if ((e = gemm_dense<TA, TW>(pk, n, 2 * d.HD, d.RKV, st, nsm))) return e;
         const int hg = d.NH < 16 ? d.NH : 16;
         k_attn_prefill<TA, TKV><<<dim3(n, (d.NH + hg - 1) / hg), 256, attn_prefill_smem(d), st>>>(
-            Q, O, kc, vc, p0, d, hg);
+            Q, O, nullptr, kc, vc, p0, d, hg);
         ++launch_count();
         if ((e = cudaGetLastError())) return e;
         ProbWO<TA, TW> po{O, (const TW *)w.wo, pb.X, d.QD, H};

@@ -1,0 +1,41 @@
+// Tensor-core form of the layer-major prefill (prefill_tc.cu): TMA tensor maps of
+// one layer's weights and of a session's prefill activations, and the chunk pass.
+#pragma once
+
+#include <cuda.h>
+
+#include "kernels.h"
+
+namespace ds4g {
+
+struct TcLayerMaps {   // boxes: 64 columns x 128 rows (64 rows for gate/up)
+    CUtensorMap wqa, wkva, wqb, wkb, wvb, wo, wr, wsg, wsu, wsd, wg, wu, wd;
+};
+struct TcActPtrs {     // hi/lo BF16 halves of the prefill activation buffers
+    bf16 *xn_hi, *xn_lo, *c_hi, *c_lo, *o_hi, *o_lo, *xg_hi, *xg_lo, *hg_hi, *hg_lo, *hs_hi, *hs_lo;
+};
+struct TcActMaps {     // boxes: 64 columns x 128 token rows
+    CUtensorMap xn_hi, xn_lo, c_hi, c_lo, o_hi, o_lo, xg_hi, xg_lo, hg_hi, hg_lo, hs_hi, hs_lo;
+};
+
+// Shapes the tensor-core form covers: BF16 weights; every weight piece a multiple
+// of 128 rows (64 for the expert gate/up) and every reduction a multiple of 64.
+bool tc_prefill_eligible(const Dims &d);
+cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m);
+TcActPtrs tc_act_ptrs(const Dims &d, const PrefillBufs &pb);
+cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m);
+cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
+                             const TcActMaps &am, void *const *kc, void *const *vc, const float2 *rope,
+                             const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n, cudaStream_t st);
+
+// prefill.cu kernels the tensor-core form shares
+__global__ void k_embed_rows(const uint16_t *table, const int *tok, float *X, int H);
+__global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E, int K, int *status);
+__global__ void k_group_count(const int *ids, int nent, int *cnt);
+__global__ void k_group_scan(const int *cnt, int E, int bm, int *off, int *tiles);
+__global__ void k_group_fill(const int *ids, int nent, const int *off, int *rows);
+template <typename TKV>
+cudaError_t attn_prefill_hilo(const Dims &d, const float *Q, bf16 *o_hi, bf16 *o_lo, const TKV *kc,
+                              const TKV *vc, int p0, int n, cudaStream_t st);
+
+}  // namespace ds4g

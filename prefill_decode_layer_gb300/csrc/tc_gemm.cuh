@@ -1,0 +1,266 @@
+// Tensor-core GEMM for the layer-major prefill (sm_103a, tcgen05 + TMA).
+//
+//   out[token][n] = sum_k W[n][k] * (Xhi[token][k] + Xlo[token][k])
+//
+// W is a BF16 weight matrix ([out][in], K contiguous).  The activations are
+// carried as two BF16 arrays: hi = bf16(x) and lo = bf16(x - hi), so that every
+// product is taken with about 16 significant bits of x and accumulated in FP32.
+// With single BF16 activations the prefill's hidden states drift by about 0.5 %
+// per layer, which flips router top-6 decisions (the 6th-to-7th score gaps are
+// small); the split keeps the decisions of an FP32 computation.
+//
+// Orientation: the weight rows are the MMA's M side (128 rows per tile) and the
+// tokens its N side (128 per tile), so a tile of W is multiplied with the hi and
+// the lo tile of the same tokens: two MMAs per 16-wide K step into one FP32
+// accumulator in tensor memory (128 lanes x 128 columns).
+//
+// One CTA computes one 128 x 128 output tile with 192 threads:
+//   warp 0 lane 0   TMA producer: per 64-wide K stage, the W tile (16 KB) and the
+//                   hi and lo token tiles (16 KB each), 128-byte swizzled, into a
+//                   4-stage shared-memory ring (full / empty mbarriers);
+//   warp 1          allocates the accumulator in TMEM; lane 0 issues the MMAs and
+//                   commits each stage back to the producer, then the tile to the
+//                   epilogue;
+//   warps 2-5       epilogue: TMEM -> registers -> a [token][feature] FP32 tile in
+//                   shared memory (the ring, no longer needed) -> the problem's
+//                   store functor, four adjacent features (or gate/up pairs) at a
+//                   time, so RoPE pairs and SwiGLU pairs are local to one call.
+// Every wait is bounded; a CTA that gives up raises DS4G_ETIMEOUT in *status,
+// drains its copies in flight, frees its TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace ds4g {
+namespace tc {
+
+static constexpr int BM = 128;      // weight rows per tile (MMA M)
+static constexpr int BN = 128;      // tokens per tile (MMA N)
+static constexpr int BK = 64;       // K per stage: one 128-byte swizzle row of BF16
+static constexpr int STAGES = 4;
+static constexpr int THREADS = 192;
+static constexpr uint32_t TILE_A = BM * BK * 2;              // 16 KB
+static constexpr uint32_t TILE_B = BN * BK * 2;              // 16 KB
+static constexpr uint32_t STAGE_BYTES = TILE_A + 2 * TILE_B;  // 48 KB
+static constexpr int EPI_PITCH = BM + 4;                     // floats per staged token row
+static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+static_assert((size_t)BN * EPI_PITCH * 4 <= (size_t)STAGES * STAGE_BYTES, "epilogue tile fits the ring");
+
+// What a launch computes.  Dense: token rows [0, m_tok), output tile rows
+// blockIdx.x * BM.  Grouped (tiles != nullptr): work item blockIdx.y is
+// (expert e, first grouped row r0) from the tile list, rows [r0, off[e+1]) of the
+// grouped activations, and expert e's weight rows start at e * n_out.
+struct Args {
+    int n_out;        // weight rows (per expert when grouped); a multiple of BM (BM/2 for gu)
+    int k;            // reduction length, a multiple of BK
+    int x_col0;       // first activation column read (a multiple of 8)
+    int piece_rows;   // dense: rows of map w0 before map w1 starts (0: w0 only)
+    int m_tok;        // dense: token rows
+    const int *tiles; // grouped: [0] = count, then (expert, first row) pairs
+    const int *off;   // grouped: expert row offsets [E + 1]
+    int *status;      // DS4G_ETIMEOUT on a wait that gave up
+};
+
+// GU: tile rows 0-63 come from w0 (gate rows) and 64-127 from w1 (the same up
+// rows); the epilogue then receives (gate, up) pairs through Epi::store_gu4.
+template <class Epi, bool GU>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
+              const __grid_constant__ CUtensorMap xhi, const __grid_constant__ CUtensorMap xlo,
+              const Args a, const Epi epi)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *accf = empty + STAGES;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(accf + 1);
+    int *abort_flag = reinterpret_cast<int *>(tslot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int e = 0, r0, rend;
+    if (a.tiles) {
+        const int t = blockIdx.y;
+        if (t >= a.tiles[0]) return;   // uniform over the CTA, before any barrier
+        e = a.tiles[1 + 2 * t];
+        r0 = a.tiles[2 + 2 * t];
+        rend = min(r0 + BN, a.off[e + 1]);
+    } else {
+        r0 = blockIdx.y * BN;
+        rend = min(r0 + BN, a.m_tok);
+    }
+    const int mb = blockIdx.x;
+    const int nk = a.k / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accf, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, BN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    volatile int *ab = abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            tma_prefetch_desc(&w0);
+            tma_prefetch_desc(&w1);
+            tma_prefetch_desc(&xhi);
+            tma_prefetch_desc(&xlo);
+            const void *wm = &w0;
+            int wrow;
+            if (GU) {
+                wrow = e * a.n_out + mb * (BM / 2);
+            } else if (a.piece_rows > 0 && mb * BM >= a.piece_rows) {
+                wm = &w1;
+                wrow = mb * BM - a.piece_rows;
+            } else {
+                wrow = e * a.n_out + mb * BM;
+            }
+            int issued = 0;
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % STAGES;
+                if (!mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, ab)) {
+                    *abort_flag = 1;
+                    atomicExch(a.status, DS4G_ETIMEOUT);
+                    break;
+                }
+                unsigned char *st = sm + s * STAGE_BYTES;
+                mbar_expect_tx(&full[s], STAGE_BYTES);
+                const int kx = i * BK;
+                if (GU) {
+                    tma_load_2d(st, &w0, kx, wrow, &full[s]);
+                    tma_load_2d(st + TILE_A / 2, &w1, kx, wrow, &full[s]);
+                } else {
+                    tma_load_2d(st, wm, kx, wrow, &full[s]);
+                }
+                tma_load_2d(st + TILE_A, &xhi, a.x_col0 + kx, r0, &full[s]);
+                tma_load_2d(st + TILE_A + TILE_B, &xlo, a.x_col0 + kx, r0, &full[s]);
+                ++issued;
+            }
+            // no copy may still be in flight when the CTA exits
+            const int n = issued < STAGES ? issued : STAGES;
+            for (int q = 1; q <= n; ++q) {
+                const int i = issued - q;
+                volatile int never = 0;
+                mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &never);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % STAGES;
+                if (!mbar_wait(&full[s], (i / STAGES) & 1, ab)) {
+                    *abort_flag = 1;
+                    atomicExch(a.status, DS4G_ETIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(sm + s * STAGE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = sdesc_kmajor_sw128(sa + kk * 32);
+                    const uint64_t bh = sdesc_kmajor_sw128(sa + TILE_A + kk * 32);
+                    const uint64_t bl = sdesc_kmajor_sw128(sa + TILE_A + TILE_B + kk * 32);
+                    tc_mma_bf16(tmem, ad, bh, idesc, (i | kk) != 0);
+                    tc_mma_bf16(tmem, ad, bl, idesc, 1u);
+                }
+                tc_commit(&empty[s]);   // the stage is free once these MMAs complete
+            }
+            tc_commit(accf);            // the tile is complete once every MMA is
+        }
+    } else {
+        // ---------------- epilogue (warps 2-5)
+        const int q = warp & 3;   // TMEM lane quarter this warp may access
+        const bool ok = mbar_wait(accf, 0, ab);
+        if (!ok) {
+            *abort_flag = 1;
+            atomicExch(a.status, DS4G_ETIMEOUT);
+        }
+        tc_fence_after();
+        float *stg = reinterpret_cast<float *>(sm);   // [BN tokens][EPI_PITCH]
+        if (ok && !*ab) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+                const int f = 32 * q + lane;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) stg[(c0 + j) * EPI_PITCH + f] = v[j];
+            }
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (ok && !*ab) {
+            const int t0 = threadIdx.x - 64;   // 0..127
+            if constexpr (GU) {
+                // features 0-63: gate rows, 64-127: the matching up rows
+                for (int idx = t0; idx < BN * (BM / 8); idx += 128) {
+                    const int t = idx / (BM / 8), j = (idx % (BM / 8)) * 4;
+                    const int m = r0 + t;
+                    if (m >= rend) continue;
+                    const float *row = stg + t * EPI_PITCH;
+                    const float4 g = *reinterpret_cast<const float4 *>(row + j);
+                    const float4 u = *reinterpret_cast<const float4 *>(row + BM / 2 + j);
+                    const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {u.x, u.y, u.z, u.w};
+                    epi.store_gu4(m, mb * (BM / 2) + j, gv, uv, e);
+                }
+            } else {
+                for (int idx = t0; idx < BN * (BM / 4); idx += 128) {
+                    const int t = idx / (BM / 4), j = (idx % (BM / 4)) * 4;
+                    const int m = r0 + t;
+                    if (m >= rend) continue;
+                    const float4 v4 = *reinterpret_cast<const float4 *>(stg + t * EPI_PITCH + j);
+                    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+                    epi.store4(m, mb * BM + j, v, e);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, BN);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+// Tensor map of a row-major BF16 matrix [rows][cols] (row stride ld elements) read
+// in boxes of 64 columns x box_rows rows with the 128-byte swizzle; rows beyond
+// `rows` read as zeros.
+cudaError_t make_map_bf16(CUtensorMap *m, const void *base, int rows, int cols, int ld, int box_rows);
+
+template <bool GU, class Epi>
+static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
+                          const CUtensorMap &xlo, const Args &a, const Epi &epi, int grid_x, int grid_y,
+                          cudaStream_t st)
+{
+    if (grid_x <= 0 || grid_y <= 0) return cudaSuccess;
+    static bool attr_set = false;   // per instantiation; set before the first launch
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES);
+        if (e) return e;
+        attr_set = true;
+    }
+    k_tc_gemm<Epi, GU><<<dim3(grid_x, grid_y), THREADS, SMEM_BYTES, st>>>(w0, w1, xhi, xlo, a, epi);
+    ++launch_count();
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace ds4g

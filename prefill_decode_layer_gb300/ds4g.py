@@ -32,7 +32,8 @@ class Config(C.Structure):
                                        "kv_rank", "window", "n_experts", "top_k",
                                        "expert_inter", "vocab")] + \
                [("rope_base", C.c_float), ("rms_eps", C.c_float), ("weight_dtype", C.c_int),
-                ("kv_dtype", C.c_int), ("prefill_chunk", C.c_int), ("decode_kernel", C.c_int)]
+                ("kv_dtype", C.c_int), ("prefill_chunk", C.c_int), ("decode_kernel", C.c_int),
+                ("prefill_kernel", C.c_int)]
 
 
 LAYER_FIELDS = ("attn_norm", "wq_a", "wq_b", "wkv_a", "wk_b", "wv_b", "wo", "ffn_norm",
@@ -103,9 +104,11 @@ def _check(rc: int, what: str) -> int:
 
 
 DECODE_AUTO, DECODE_STAGED = 0, 1
+PREFILL_AUTO, PREFILL_SIMT = 0, 1
 
 
-def config_struct(shape, prefill_chunk: int = 0, decode_kernel: int = DECODE_AUTO) -> Config:
+def config_struct(shape, prefill_chunk: int = 0, decode_kernel: int = DECODE_AUTO,
+                  prefill_kernel: int = PREFILL_AUTO) -> Config:
     c = Config()
     for n in ("n_layers", "hidden", "n_heads", "head_dim", "q_rank", "kv_rank", "window",
               "n_experts", "top_k", "expert_inter", "vocab"):
@@ -116,6 +119,7 @@ def config_struct(shape, prefill_chunk: int = 0, decode_kernel: int = DECODE_AUT
     c.kv_dtype = F32 if shape.kv_dtype == "f32" else BF16
     c.prefill_chunk = int(prefill_chunk)
     c.decode_kernel = int(decode_kernel)
+    c.prefill_kernel = int(prefill_kernel)
     return c
 
 
@@ -134,9 +138,10 @@ class Model:
     """Weights are device tensors owned by the caller (kept referenced here)."""
 
     def __init__(self, shape, tok_embd: torch.Tensor, lm_head: torch.Tensor, layers: list,
-                 prefill_chunk: int = 0, decode_kernel: int = DECODE_AUTO):
+                 prefill_chunk: int = 0, decode_kernel: int = DECODE_AUTO,
+                 prefill_kernel: int = PREFILL_AUTO):
         self.shape = shape
-        self.cfg = config_struct(shape, prefill_chunk, decode_kernel)
+        self.cfg = config_struct(shape, prefill_chunk, decode_kernel, prefill_kernel)
         self._keep = (tok_embd, lm_head, layers)
         arr = (LayerWeights * len(layers))()
         for i, w in enumerate(layers):

@@ -45,12 +45,12 @@ def kv_to_f64(shape, arr: np.ndarray) -> np.ndarray:
 
 # ----------------------------------------------------------------------------- GPU side
 
-def gpu_model(shape, seed=0, prefill_chunk=0, decode_kernel=0):
+def gpu_model(shape, seed=0, prefill_chunk=0, decode_kernel=0, prefill_kernel=0):
     import prefill_decode_layer_gb300 as pdl
     from synth import torch_weights as tw
     emb, lm, layers = tw.dev_model(shape, seed)
     return pdl.Model(shape, emb, lm, layers, prefill_chunk=prefill_chunk,
-                     decode_kernel=decode_kernel)
+                     decode_kernel=decode_kernel, prefill_kernel=prefill_kernel)
 
 
 DECODE_KERNELS = [0, 1]   # persistent single launch (when available), one kernel per stage

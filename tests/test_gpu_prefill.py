@@ -12,16 +12,22 @@ from helpers import (TOL_BF16, LazyOracleModel, OracleKV, gpu_model, kv_to_f64, 
 
 pytestmark = pytest.mark.gpu
 
+# Two small BF16 shapes: the first takes the SIMT GEMMs (head_dim 64, 32 experts),
+# the second the tensor-core GEMMs (every weight piece a multiple of 128 rows).
 SMALL = synth.LAYER.with_(name="small_bf16", n_layers=2, hidden=512, n_heads=8, head_dim=64,
                           q_rank=128, kv_rank=64, window=16, n_experts=32, top_k=4,
                           expert_inter=128, vocab=1000, gain_sigma=0.1)
+SMALL_TC = synth.LAYER.with_(name="small_bf16_tc", n_layers=2, hidden=512, n_heads=8, head_dim=128,
+                             q_rank=256, kv_rank=128, window=16, n_experts=128, top_k=4,
+                             expert_inter=128, vocab=1000, gain_sigma=0.1)
 
 
-@pytest.fixture(scope="module")
-def small():
+@pytest.fixture(scope="module", params=[SMALL, SMALL_TC], ids=["simt", "tensor_core"])
+def small(request):
     import torch
     torch.cuda.init()
-    return gpu_model(SMALL, prefill_chunk=32), LazyOracleModel(SMALL).full()
+    shape = request.param
+    return gpu_model(shape, prefill_chunk=32), LazyOracleModel(shape).full(), shape
 
 
 def kv_np(sess, layer, n):
@@ -32,7 +38,7 @@ def kv_np(sess, layer, n):
 def test_small_prefill_ragged_chunks_match_oracle(small):
     import torch
     import prefill_decode_layer_gb300 as pdl
-    gm, om = small
+    gm, om, SMALL = small
     toks = synth.host_tokens(100, SMALL.vocab, stream=21)   # chunks 32, 32, 32, 4
     sess = pdl.Session(gm, 160)
     assert sess.prefill(toks) == 0
@@ -59,7 +65,7 @@ def test_small_prefill_ragged_chunks_match_oracle(small):
 def test_chunk_size_invariance_bitwise(small):
     import torch
     import prefill_decode_layer_gb300 as pdl
-    gm, _ = small
+    gm, _, SMALL = small
     big = pdl.Model(SMALL, *gm._keep, prefill_chunk=0)
     toks = synth.host_tokens(77, SMALL.vocab, stream=23)
     a = pdl.Session(gm, 128)
@@ -75,7 +81,7 @@ def test_chunk_size_invariance_bitwise(small):
 def test_truncate_then_suffix_equals_scratch_bitwise(small):
     import torch
     import prefill_decode_layer_gb300 as pdl
-    gm, _ = small
+    gm, _, SMALL = small
     common = synth.host_tokens(70, SMALL.vocab, stream=24)
     live_tail = synth.host_tokens(20, SMALL.vocab, stream=25)
     new_tail = synth.host_tokens(9, SMALL.vocab, stream=26)
@@ -106,7 +112,7 @@ def test_truncate_then_suffix_equals_scratch_bitwise(small):
 
 def test_session_errors(small):
     import prefill_decode_layer_gb300 as pdl
-    gm, _ = small
+    gm, _, SMALL = small
     s = pdl.Session(gm, 16)
     assert s.prefill([1, 2, SMALL.vocab]) == pdl.ds4g.ETOKEN and s.len == 0
     assert s.prefill(list(range(16))) == pdl.ds4g.ECONTEXT and s.len == 0
@@ -116,6 +122,24 @@ def test_session_errors(small):
     assert s.decode(-1) == pdl.ds4g.ETOKEN
     assert s.truncate(16) == pdl.ds4g.EINVAL and s.truncate(15) == 0 and s.len == 15
     assert s.truncate(0) == 0 and s.len == 0
+
+
+def test_tensor_core_and_simt_prefill_agree():
+    """The two GEMM forms of the prefill on the same BF16 model: hidden states and
+    KV within the BF16 tolerance (their activations are rounded differently)."""
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    tcm = gpu_model(SMALL_TC, prefill_chunk=64)
+    simt = pdl.Model(SMALL_TC, *tcm._keep, prefill_chunk=64, prefill_kernel=pdl.ds4g.PREFILL_SIMT)
+    toks = synth.host_tokens(150, SMALL_TC.vocab, stream=27)
+    a, b = pdl.Session(tcm, 200), pdl.Session(simt, 200)
+    assert a.prefill(toks) == 0 and b.prefill(toks) == 0
+    torch.cuda.synchronize()
+    assert a.status() == 0 and b.status() == 0
+    assert rel_err(to_np(a.logits()), to_np(b.logits())) <= TOL_BF16
+    for l in range(SMALL_TC.n_layers):
+        assert rel_err(to_np(a.kv(l)[0][:150]), to_np(b.kv(l)[0][:150])) <= TOL_BF16
+        assert rel_err(to_np(a.kv(l)[1][:150]), to_np(b.kv(l)[1][:150])) <= TOL_BF16
 
 
 def test_full_width_8_layer_prefill_first_positions():
