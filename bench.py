@@ -233,7 +233,10 @@ def workload_config(m):
 # decode-small: the same layer with 32 routed experts and a 8192-token vocabulary,
 #   so that a multi-pass ncu capture holds about 1 GB on the device while every step
 #   still streams more weight bytes (about 265 MB) than the 129 MB L2.
-CASES = {"decode-full": dict(), "decode-small": dict(n_experts=32, vocab=8192)}
+# prefill-full: the layer-major prefill workload (8 full-width layers, 4096 tokens),
+#   each step truncates the session to 0 and prefills the same prompt again.
+CASES = {"decode-full": dict(), "decode-small": dict(n_experts=32, vocab=8192),
+         "prefill-full": dict(n_layers=8)}
 
 
 def run_case(args):
@@ -241,6 +244,18 @@ def run_case(args):
     import prefill_decode_layer_gb300 as pdl
     from synth import torch_weights as tw
     shape = synth.LAYER.with_(**CASES[args.case])
+    if args.case.startswith("prefill"):
+        emb, lm, layers = tw.dev_model(shape)
+        m = pdl.Model(shape, emb, lm, layers)
+        s = pdl.Session(m, 4096 + 8)
+        toks = synth.host_tokens(4096, shape.vocab, stream=41)
+        for i in range(args.warmup + args.steps):
+            assert s.truncate(0) == 0 and s.prefill(toks) == 0
+        torch.cuda.synchronize()
+        assert s.status() == 0
+        print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup,
+                          "launches": int(s.launches)}), flush=True)
+        return
     emb, lm, layers = tw.dev_model(shape)
     m = pdl.Model(shape, emb, lm, layers)
     n_pre = 4096

@@ -225,6 +225,7 @@ int ds4g_model_create(const ds4g_config *cfg, const ds4g_weights *w, ds4g_model 
         e = persistent_setup(m->d, max_smem, m->nsm, &m->persistent);
     m->tc = !e && cfg->prefill_kernel == DS4G_PREFILL_AUTO && tc_prefill_eligible(m->d);
     if (m->tc) {
+        e = attn_mma_setup(m->d, max_smem);
         m->tcmaps.resize(m->layers.size());
         for (size_t l = 0; !e && l < m->layers.size(); ++l) e = tc_layer_maps(m->d, m->layers[l], m->tcmaps[l]);
     }
@@ -341,7 +342,8 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
                                         cudaMemcpyHostToDevice, s->st);
         if (!e)
             e = s->m->tc ? prefill_chunk_tc(d, s->m->layers.data(), s->m->tcmaps.data(), s->tcact, s->kc.data(),
-                                            s->vc.data(), s->rope, s->m->tok_embd, s->pb, s->len + c, nc, s->st)
+                                            s->vc.data(), s->rope, s->m->tok_embd, s->pb, s->len + c, nc, s->st,
+                                            s->m->nsm)
                          : prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,
                                          s->m->tok_embd, s->pb, s->len + c, nc, s->st, s->m->nsm);
         if (!e && c + nc == n) {  // last token's hidden state, then its logits

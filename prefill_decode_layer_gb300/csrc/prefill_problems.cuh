@@ -3,6 +3,8 @@
 // one row (store4).  The tensor-core GEMM (prefill_tc.cu) reuses the epilogues.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace ds4g {
@@ -29,12 +31,17 @@ struct ProbQB {  // Q = RoPE(C[:, :RQ] W_qb^T)
     __device__ const TA *a_row(int m, int) const { return C + (size_t)m * ldc; }
     __device__ const TW *w_row(int n, int) const { return wqb + (size_t)n * RQ; }
     __device__ void store4(int m, int n, const float (&v)[4], int) const {
-        const float2 *rp = rope + (size_t)(p0 + m) * (HD / 2);
-#pragma unroll
-        for (int j = 0; j < 4; j += 2) {
-            const float2 cs = rp[((n + j) % HD) / 2];
-            Q[(size_t)m * QD + n + j] = from_f32<TA>(v[j] * cs.x - v[j + 1] * cs.y);
-            Q[(size_t)m * QD + n + j + 1] = from_f32<TA>(v[j] * cs.y + v[j + 1] * cs.x);
+        // two RoPE pairs: (cos, sin) of pair (n % HD) / 2 and the next, one 16-byte load
+        const float4 cs = *reinterpret_cast<const float4 *>(rope + (size_t)(p0 + m) * (HD / 2) + (n % HD) / 2);
+        const float r0 = v[0] * cs.x - v[1] * cs.y, r1 = v[0] * cs.y + v[1] * cs.x;
+        const float r2 = v[2] * cs.z - v[3] * cs.w, r3 = v[2] * cs.w + v[3] * cs.z;
+        if constexpr (std::is_same<TA, float>::value) {
+            *reinterpret_cast<float4 *>(Q + (size_t)m * QD + n) = make_float4(r0, r1, r2, r3);
+        } else {
+            Q[(size_t)m * QD + n] = from_f32<TA>(r0);
+            Q[(size_t)m * QD + n + 1] = from_f32<TA>(r1);
+            Q[(size_t)m * QD + n + 2] = from_f32<TA>(r2);
+            Q[(size_t)m * QD + n + 3] = from_f32<TA>(r3);
         }
     }
 };
@@ -69,8 +76,10 @@ struct ProbWO {  // X += O W_o^T
     __device__ const TA *a_row(int m, int) const { return O + (size_t)m * QD; }
     __device__ const TW *w_row(int n, int) const { return wo + (size_t)n * QD; }
     __device__ void store4(int m, int n, const float (&v)[4], int) const {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) X[(size_t)m * H + n + j] += v[j];
+        float4 *x = reinterpret_cast<float4 *>(X + (size_t)m * H + n);
+        float4 r = *x;
+        r.x += v[0]; r.y += v[1]; r.z += v[2]; r.w += v[3];
+        *x = r;
     }
 };
 
@@ -113,9 +122,7 @@ struct ProbDown {  // YS[token*K + slot] = HG W_d(e)^T, grouped rows
         return wd + (size_t)e * H * I + (size_t)n * I;
     }
     __device__ void store4(int m, int n, const float (&v)[4], int) const {
-        float *y = YS + (size_t)rows[m] * H + n;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) y[j] = v[j];
+        *reinterpret_cast<float4 *>(YS + (size_t)rows[m] * H + n) = make_float4(v[0], v[1], v[2], v[3]);
     }
 };
 
@@ -128,12 +135,16 @@ struct ProbSharedDown {  // X += HS W_sd^T + sum_s w[s] YS[token, s]  (slot orde
         float r[4] = {0.f, 0.f, 0.f, 0.f};
         for (int s = 0; s < K; ++s) {
             const float w = wts[(size_t)m * K + s];
-            const float *y = YS + ((size_t)m * K + s) * H + n;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) r[j] = fmaf(w, y[j], r[j]);
+            const float4 y = *reinterpret_cast<const float4 *>(YS + ((size_t)m * K + s) * H + n);
+            r[0] = fmaf(w, y.x, r[0]);
+            r[1] = fmaf(w, y.y, r[1]);
+            r[2] = fmaf(w, y.z, r[2]);
+            r[3] = fmaf(w, y.w, r[3]);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) X[(size_t)m * H + n + j] += r[j] + v[j];
+        float4 *x = reinterpret_cast<float4 *>(X + (size_t)m * H + n);
+        float4 o = *x;
+        o.x += r[0] + v[0]; o.y += r[1] + v[1]; o.z += r[2] + v[2]; o.w += r[3] + v[3];
+        *x = o;
     }
 };
 

@@ -10,6 +10,8 @@
 // by the routed gate/up GEMM) lives in the routed-output buffer, which is written
 // only afterwards.  Weight tensor maps are built once per model, activation maps
 // once per session.
+#include <type_traits>
+
 #include "kernels.h"
 #include "prefill_problems.cuh"
 #include "prefill_tc.h"
@@ -58,18 +60,326 @@ __global__ void __launch_bounds__(256) k_gather_rows(const bf16 *hi, const bf16 
     }
 }
 
-// ------------------------------------------------------------------ epilogues
+// ------------------------------------------------------------------ attention on the tensor cores
+//
+// Windowed causal MQA for a chunk with warp-level BF16 MMAs (m16n8k16, FP32
+// accumulation).  All heads of a token share one K/V window, so a warp takes 16
+// heads of one token as the 16 rows of its tiles: S = Q K^T over the window's keys,
+// a row softmax in registers, O = P V.  Q and P enter the MMAs as hi/lo BF16 pairs
+// (two MMAs each), K and V are BF16 already.  A CTA serves 16 consecutive tokens:
+// the union of their windows (at most W + 15 keys) is staged once in shared memory
+// (rows padded by 16 bytes so that ldmatrix rows fall in distinct banks, plus 16
+// zero rows for the padding of the last 16-key step).  Head dimension 128, window
+// <= 128.
 
-struct EpiHiLo {   // out[m][n..n+3] as hi/lo BF16
+static constexpr int kAttnTB = 16;                     // tokens per CTA
+static constexpr int kAttnHD = 128;                    // head dimension of this kernel
+static constexpr int kAttnMaxW = 128;                  // largest window
+static constexpr int kAttnPitch = kAttnHD + 8;         // bf16 per staged K/V row
+static constexpr int kAttnMaxT = kAttnMaxW / 8 + 2;    // 8-key tiles a window can touch (even)
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)   // a in the low half
+{
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+    return lo | (hi << 16);
+}
+__device__ __forceinline__ void split_pack(float a, float b, uint32_t &hi, uint32_t &lo)
+{
+    const bf16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+    hi = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
+    lo = pack_bf16(a - __bfloat162float(ha), b - __bfloat162float(hb));
+}
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+size_t attn_mma_smem(const Dims &d)
+{
+    const int rows = d.W + kAttnTB - 1 + 15 + 16;   // window union, alignment, padding
+    return 2 * (size_t)rows * kAttnPitch * 2;
+}
+
+__global__ void __launch_bounds__(256) k_attn_prefill_mma(const float *Q, bf16 *o_hi, bf16 *o_lo,
+                                                          const bf16 *kc, const bf16 *vc, int p0, int n,
+                                                          Dims d)
+{
+    extern __shared__ __align__(16) unsigned char sm_attn[];
+    const int W = d.W, NH = d.NH, QD = d.QD;
+    const int t0 = blockIdx.x * kAttnTB;
+    const int tend = min(t0 + kAttnTB, n);
+    // Staged keys [kbase, kend), kbase a multiple of 16.  Tiles start at absolute key
+    // positions that are multiples of 16, so a token's sums run in the same order
+    // however the prompt was cut into chunks (batch-invariant results); a window's
+    // last 16-key step may run up to 15 rows past the keys: 16 zero rows follow.
+    const int kbase = (max(0, p0 + t0 - W + 1) / 16) * 16, kend = p0 + tend;
+    const int nrows = kend - kbase + 16;
+    bf16 *Ks = reinterpret_cast<bf16 *>(sm_attn);
+    bf16 *Vs = Ks + (size_t)nrows * kAttnPitch;
+    for (int i = threadIdx.x; i < nrows * (kAttnHD / 8); i += blockDim.x) {
+        const int r = i / (kAttnHD / 8), c = (i % (kAttnHD / 8)) * 8;
+        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+        if (kbase + r < kend) {
+            kv = *reinterpret_cast<const uint4 *>(kc + (size_t)(kbase + r) * kAttnHD + c);
+            vv = *reinterpret_cast<const uint4 *>(vc + (size_t)(kbase + r) * kAttnHD + c);
+        }
+        *reinterpret_cast<uint4 *>(Ks + (size_t)r * kAttnPitch + c) = kv;
+        *reinterpret_cast<uint4 *>(Vs + (size_t)r * kAttnPitch + c) = vv;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c2 = (lane & 3) * 2;
+    const int ngroups = (NH + 15) / 16;
+    const float scale = rsqrtf((float)kAttnHD);
+    for (int item = warp; item < (tend - t0) * ngroups; item += 8) {
+        const int t = t0 + item / ngroups, h0 = (item % ngroups) * 16;
+        const int pos = p0 + t, klo = max(0, pos - W + 1);
+        const int ra = h0 + g, rb = h0 + g + 8;   // the two query rows (heads) of this thread
+        // S = Q K^T over 8-key tiles [s0, s0 + 8 * nt) of the staged rows
+        const int s0 = (klo / 16) * 16 - kbase;
+        const int nt = ((pos - kbase + 1 - s0 + 15) / 16) * 2;   // even
+        float S[kAttnMaxT][4];
+#pragma unroll
+        for (int j = 0; j < kAttnMaxT; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
+        const float *qa = Q + (size_t)t * QD + (size_t)ra * kAttnHD;
+        const float *qb = Q + (size_t)t * QD + (size_t)rb * kAttnHD;
+#pragma unroll 1
+        for (int k0 = 0; k0 < kAttnHD; k0 += 16) {
+            uint32_t ah[4], al[4];
+            {
+                float2 x0 = make_float2(0.f, 0.f), x1 = x0, x2 = x0, x3 = x0;
+                if (ra < NH) {
+                    x0 = *reinterpret_cast<const float2 *>(qa + k0 + c2);
+                    x2 = *reinterpret_cast<const float2 *>(qa + k0 + 8 + c2);
+                }
+                if (rb < NH) {
+                    x1 = *reinterpret_cast<const float2 *>(qb + k0 + c2);
+                    x3 = *reinterpret_cast<const float2 *>(qb + k0 + 8 + c2);
+                }
+                split_pack(x0.x * scale, x0.y * scale, ah[0], al[0]);
+                split_pack(x1.x * scale, x1.y * scale, ah[1], al[1]);
+                split_pack(x2.x * scale, x2.y * scale, ah[2], al[2]);
+                split_pack(x3.x * scale, x3.y * scale, ah[3], al[3]);
+            }
+#pragma unroll
+            for (int j = 0; j < kAttnMaxT; j += 2) {
+                if (j < nt) {
+                    // keys s0 + 8j .. +15, dims k0 .. k0+15: matrices (keys 0-7, dims 0-7),
+                    // (keys 0-7, dims 8-15), (keys 8-15, dims 0-7), (keys 8-15, dims 8-15)
+                    uint32_t b[4];
+                    const int kr = s0 + 8 * j + (lane & 7) + ((lane >> 4) << 3);
+                    const int kcol = k0 + ((lane >> 3) & 1) * 8;
+                    ldsm_x4(b, Ks + (size_t)kr * kAttnPitch + kcol);
+                    mma_16816(S[j], ah, b[0], b[1]);
+                    mma_16816(S[j], al, b[0], b[1]);
+                    mma_16816(S[j + 1], ah, b[2], b[3]);
+                    mma_16816(S[j + 1], al, b[2], b[3]);
+                }
+            }
+        }
+        // mask to the window, then row max / exp / sum (rows ra: S[.][0..1], rb: S[.][2..3])
+        float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kAttnMaxT; ++j) {
+            const int kabs = kbase + s0 + 8 * j + c2;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const bool ok = j < nt && kabs + u >= klo && kabs + u <= pos;
+                if (!ok) {
+                    S[j][u] = -INFINITY;
+                    S[j][2 + u] = -INFINITY;
+                }
+                ma = fmaxf(ma, S[j][u]);
+                mb = fmaxf(mb, S[j][2 + u]);
+            }
+        }
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        float suma = 0.f, sumb = 0.f;
+#pragma unroll
+        for (int j = 0; j < kAttnMaxT; ++j) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                S[j][u] = S[j][u] == -INFINITY ? 0.f : __expf(S[j][u] - ma);
+                S[j][2 + u] = S[j][2 + u] == -INFINITY ? 0.f : __expf(S[j][2 + u] - mb);
+                suma += S[j][u];
+                sumb += S[j][2 + u];
+            }
+        }
+        suma += __shfl_xor_sync(0xffffffffu, suma, 1);
+        suma += __shfl_xor_sync(0xffffffffu, suma, 2);
+        sumb += __shfl_xor_sync(0xffffffffu, sumb, 1);
+        sumb += __shfl_xor_sync(0xffffffffu, sumb, 2);
+        // O = P V, 16 keys per step; P's C-fragment layout is the A-fragment layout
+        float O[kAttnHD / 8][4];
+#pragma unroll
+        for (int q = 0; q < kAttnHD / 8; ++q) O[q][0] = O[q][1] = O[q][2] = O[q][3] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kAttnMaxT; j += 2) {
+            if (j < nt) {
+                uint32_t ph[4], pl[4];
+                split_pack(S[j][0], S[j][1], ph[0], pl[0]);
+                split_pack(S[j][2], S[j][3], ph[1], pl[1]);
+                split_pack(S[j + 1][0], S[j + 1][1], ph[2], pl[2]);
+                split_pack(S[j + 1][2], S[j + 1][3], ph[3], pl[3]);
+#pragma unroll
+                for (int q = 0; q < kAttnHD / 8; q += 2) {
+                    // keys s0 + 8j .. +15 x dims 8q .. 8q+15, transposed: matrices (keys 0-7,
+                    // dims 0-7), (keys 8-15, dims 0-7), (keys 0-7, dims 8-15), (keys 8-15, dims 8-15)
+                    uint32_t b[4];
+                    const int vr = s0 + 8 * j + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int vcol = 8 * q + ((lane >> 4) << 3);
+                    ldsm_x4_t(b, Vs + (size_t)vr * kAttnPitch + vcol);
+                    mma_16816(O[q], ph, b[0], b[1]);
+                    mma_16816(O[q], pl, b[0], b[1]);
+                    mma_16816(O[q + 1], ph, b[2], b[3]);
+                    mma_16816(O[q + 1], pl, b[2], b[3]);
+                }
+            }
+        }
+        const float ia = 1.f / suma, ib = 1.f / sumb;
+#pragma unroll
+        for (int q = 0; q < kAttnHD / 8; ++q) {
+            const int dcol = 8 * q + c2;
+            uint32_t h, l;
+            if (ra < NH) {
+                split_pack(O[q][0] * ia, O[q][1] * ia, h, l);
+                const size_t oi = (size_t)t * QD + (size_t)ra * kAttnHD + dcol;
+                *reinterpret_cast<uint32_t *>(o_hi + oi) = h;
+                *reinterpret_cast<uint32_t *>(o_lo + oi) = l;
+            }
+            if (rb < NH) {
+                split_pack(O[q][2] * ib, O[q][3] * ib, h, l);
+                const size_t oi = (size_t)t * QD + (size_t)rb * kAttnHD + dcol;
+                *reinterpret_cast<uint32_t *>(o_hi + oi) = h;
+                *reinterpret_cast<uint32_t *>(o_lo + oi) = l;
+            }
+        }
+    }
+}
+
+bool attn_mma_eligible(const Dims &d) { return d.HD == kAttnHD && d.W <= kAttnMaxW && d.kvdt == DS4G_BF16; }
+
+cudaError_t attn_mma_setup(const Dims &d, int max_smem)
+{
+    if (!attn_mma_eligible(d)) return cudaSuccess;
+    if (attn_mma_smem(d) > (size_t)max_smem) return cudaErrorInvalidValue;
+    return allow_max_dyn_smem((const void *)k_attn_prefill_mma, max_smem);
+}
+
+// ------------------------------------------------------------------ epilogues
+// Functors of the tensor-core GEMM: load4 fetches what a 4-feature store needs
+// from global memory (issued in batches by the GEMM), store4 writes.
+
+struct EpiHiLo {   // out[m][n..n+3] as hi/lo BF16 (the next GEMM's input)
     bf16 *hi, *lo;
     int ld;
-    __device__ void store4(int m, int n, const float (&v)[4], int) const
+    using Aux = tc::NoAux;
+    __device__ Aux load4(int, int, int) const { return {}; }
+    __device__ void store4(int m, int n, const float (&v)[4], const Aux &, int) const
     {
         __align__(8) bf16 h[4], l[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) split_hilo(v[j], h[j], l[j]);
         *reinterpret_cast<uint2 *>(hi + (size_t)m * ld + n) = *reinterpret_cast<const uint2 *>(h);
         *reinterpret_cast<uint2 *>(lo + (size_t)m * ld + n) = *reinterpret_cast<const uint2 *>(l);
+    }
+};
+
+__device__ __forceinline__ float4 rope_pairs(const float2 *rope, int pos, int HD, int n)
+{   // (cos, sin) of the RoPE pairs (n % HD)/2 and the next one
+    return *reinterpret_cast<const float4 *>(rope + (size_t)pos * (HD / 2) + (n % HD) / 2);
+}
+
+struct EpiQRope {   // Q[m][n..n+3] = RoPE(q) in FP32 (the attention's input)
+    float *Q;
+    const float2 *rope;
+    int QD, HD, p0;
+    using Aux = float4;
+    __device__ Aux load4(int m, int n, int) const { return rope_pairs(rope, p0 + m, HD, n); }
+    __device__ void store4(int m, int n, const float (&v)[4], const Aux &cs, int) const
+    {
+        *reinterpret_cast<float4 *>(Q + (size_t)m * QD + n) =
+            make_float4(v[0] * cs.x - v[1] * cs.y, v[0] * cs.y + v[1] * cs.x, v[2] * cs.z - v[3] * cs.w,
+                        v[2] * cs.w + v[3] * cs.z);
+    }
+};
+
+template <typename TKV>
+struct EpiKVRope {   // features [0, HD): K with RoPE, [HD, 2HD): V; appended at p0 + m
+    TKV *kc, *vc;
+    const float2 *rope;
+    int HD, p0;
+    using Aux = float4;
+    __device__ Aux load4(int m, int n, int) const
+    {
+        return n < HD ? rope_pairs(rope, p0 + m, HD, n) : make_float4(1.f, 0.f, 1.f, 0.f);
+    }
+    __device__ void store4(int m, int n, const float (&v)[4], const Aux &cs, int) const
+    {
+        const size_t row = (size_t)(p0 + m) * HD;
+        if (n < HD) {
+            kc[row + n] = from_f32<TKV>(v[0] * cs.x - v[1] * cs.y);
+            kc[row + n + 1] = from_f32<TKV>(v[0] * cs.y + v[1] * cs.x);
+            kc[row + n + 2] = from_f32<TKV>(v[2] * cs.z - v[3] * cs.w);
+            kc[row + n + 3] = from_f32<TKV>(v[2] * cs.w + v[3] * cs.z);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) vc[row + n - HD + j] = from_f32<TKV>(v[j]);
+        }
+    }
+};
+
+struct EpiAddX {   // residual: X[m][n..n+3] += v
+    float *X;
+    int H;
+    using Aux = float4;
+    __device__ Aux load4(int m, int n, int) const { return *reinterpret_cast<const float4 *>(X + (size_t)m * H + n); }
+    __device__ void store4(int m, int n, const float (&v)[4], const Aux &x, int) const
+    {
+        *reinterpret_cast<float4 *>(X + (size_t)m * H + n) = make_float4(x.x + v[0], x.y + v[1], x.z + v[2], x.w + v[3]);
+    }
+};
+
+struct EpiScores {   // router scores S[m][n..n+3] in FP32
+    float *S;
+    int E;
+    using Aux = tc::NoAux;
+    __device__ Aux load4(int, int, int) const { return {}; }
+    __device__ void store4(int m, int n, const float (&v)[4], const Aux &, int) const
+    {
+        *reinterpret_cast<float4 *>(S + (size_t)m * E + n) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+
+struct EpiRoutedRows {   // routed expert output of grouped row m into its (token, slot) row
+    float *YS;
+    const int *rows;
+    int H;
+    using Aux = int;
+    __device__ Aux load4(int m, int, int) const { return rows[m]; }
+    __device__ void store4(int, int n, const float (&v)[4], const Aux &r, int) const
+    {
+        *reinterpret_cast<float4 *>(YS + (size_t)r * H + n) = make_float4(v[0], v[1], v[2], v[3]);
     }
 };
 
@@ -85,6 +395,34 @@ struct EpiSwiGLU {   // h[m][i..i+3] = silu(gate) * up, as hi/lo BF16
         *reinterpret_cast<uint2 *>(lo + (size_t)m * ld + i) = *reinterpret_cast<const uint2 *>(l);
     }
 };
+
+// x[t] += sum over slots s (in order) of w[t][s] * YS[t*K + s]: the selected experts'
+// outputs, after the shared expert's down projection was added by its GEMM.
+__global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, const float *wts, int H, int K)
+{
+    const int t = blockIdx.x;
+    float w[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) w[s] = s < K ? wts[(size_t)t * K + s] : 0.f;
+    for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
+        float4 y[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < K) y[s] = *reinterpret_cast<const float4 *>(YS + ((size_t)t * K + s) * H + i);
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < K) {
+                r.x = fmaf(w[s], y[s].x, r.x);
+                r.y = fmaf(w[s], y[s].y, r.y);
+                r.z = fmaf(w[s], y[s].z, r.z);
+                r.w = fmaf(w[s], y[s].w, r.w);
+            }
+        float4 *x = reinterpret_cast<float4 *>(X + (size_t)t * H + i);
+        const float4 xv = *x;
+        *x = make_float4(xv.x + r.x, xv.y + r.y, xv.z + r.z, xv.w + r.w);
+    }
+}
 
 // ------------------------------------------------------------------ maps and eligibility
 
@@ -159,15 +497,13 @@ template <typename TKV>
 static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
                               const TcActMaps &am, void *const *kcs, void *const *vcs, const float2 *rope,
                               const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n,
-                              cudaStream_t st)
+                              cudaStream_t st, int nsm)
 {
     cudaError_t e;
     const int H = d.H, K = d.K, nent = n * K, I = d.I;
     const TcActPtrs ap = tc_act_ptrs(d, pb);
     const int ny = (n + tc::BN - 1) / tc::BN;
     const int max_tiles = nent / tc::BN + d.E + 1;
-    tc::Args a{};
-    a.status = pb.status;
     k_embed_rows<<<n, 256, 0, st>>>(tok_embd, pb.tok, pb.X, H);
     ++launch_count();
     if ((e = cudaGetLastError())) return e;
@@ -175,32 +511,46 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         const LayerPtrs &w = layers[l];
         const TcLayerMaps &m = lm[l];
         TKV *kc = (TKV *)kcs[l], *vc = (TKV *)vcs[l];
-        // attention half
-        k_rmsnorm_hilo<<<n, 256, 0, st>>>(pb.X, w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
-        ++launch_count();
-        a = tc::Args{};
+        tc::Args a{};
         a.status = pb.status;
         a.m_tok = n;
-        a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ;
-        if ((e = tc::launch<false>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a,
-                                   EpiHiLo{ap.c_hi, ap.c_lo, d.RQ + d.RKV}, (d.RQ + d.RKV) / tc::BM, ny, st)))
+        // ---- attention half
+        k_rmsnorm_hilo<<<n, 256, 0, st>>>(pb.X, w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
+        ++launch_count();
+        a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ, a.x_col0 = 0;
+        if ((e = tc::launch<false>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a, EpiHiLo{ap.c_hi, ap.c_lo, d.RQ + d.RKV},
+                                   (d.RQ + d.RKV) / tc::BM, ny, nsm, st)))
             return e;
         a.n_out = d.QD, a.k = d.RQ, a.piece_rows = 0, a.x_col0 = 0;
-        ProbQB<float, bf16> pq{nullptr, nullptr, (float *)pb.Q, rope, 0, d.RQ, d.QD, d.HD, p0};
-        if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a, pq, d.QD / tc::BM, ny, st))) return e;
+        if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a, EpiQRope{(float *)pb.Q, rope, d.QD, d.HD, p0},
+                                   d.QD / tc::BM, ny, nsm, st)))
+            return e;
         a.n_out = 2 * d.HD, a.k = d.RKV, a.piece_rows = d.HD, a.x_col0 = d.RQ;
-        ProbKVB<float, bf16, TKV> pk{nullptr, nullptr, nullptr, kc, vc, rope, 0, d.RQ, d.RKV, d.HD, p0};
-        if ((e = tc::launch<false>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, pk, 2 * d.HD / tc::BM, ny, st))) return e;
-        if ((e = attn_prefill_hilo<TKV>(d, (const float *)pb.Q, ap.o_hi, ap.o_lo, kc, vc, p0, n, st))) return e;
+        if ((e = tc::launch<false>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, EpiKVRope<TKV>{kc, vc, rope, d.HD, p0},
+                                   2 * d.HD / tc::BM, ny, nsm, st)))
+            return e;
+        if constexpr (std::is_same<TKV, bf16>::value) {
+            if (attn_mma_eligible(d)) {
+                k_attn_prefill_mma<<<(n + kAttnTB - 1) / kAttnTB, 256, attn_mma_smem(d), st>>>(
+                    (const float *)pb.Q, ap.o_hi, ap.o_lo, kc, vc, p0, n, d);
+                ++launch_count();
+                if ((e = cudaGetLastError())) return e;
+            } else if ((e = attn_prefill_hilo<TKV>(d, (const float *)pb.Q, ap.o_hi, ap.o_lo, kc, vc, p0, n, st))) {
+                return e;
+            }
+        } else if ((e = attn_prefill_hilo<TKV>(d, (const float *)pb.Q, ap.o_hi, ap.o_lo, kc, vc, p0, n, st))) {
+            return e;
+        }
         a.n_out = H, a.k = d.QD, a.piece_rows = 0, a.x_col0 = 0;
-        ProbWO<float, bf16> po{nullptr, nullptr, pb.X, d.QD, H};
-        if ((e = tc::launch<false>(m.wo, m.wo, am.o_hi, am.o_lo, a, po, H / tc::BM, ny, st))) return e;
-        // MoE half
+        if ((e = tc::launch<false>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, H / tc::BM, ny, nsm, st)))
+            return e;
+        // ---- MoE half
         k_rmsnorm_hilo<<<n, 256, 0, st>>>(pb.X, w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
         ++launch_count();
         a.n_out = d.E, a.k = H;
-        ProbRouter<bf16> pr{nullptr, nullptr, pb.S, H, d.E};
-        if ((e = tc::launch<false>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, pr, d.E / tc::BM, ny, st))) return e;
+        if ((e = tc::launch<false>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, d.E / tc::BM, ny, nsm,
+                                   st)))
+            return e;
         k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K, pb.status);
         ++launch_count();
         k_group_count<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.cnt);
@@ -217,30 +567,34 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         g.status = pb.status;
         g.n_out = I, g.k = H, g.tiles = pb.tiles, g.off = pb.off;
         if ((e = tc::launch<true>(m.wg, m.wu, am.xg_hi, am.xg_lo, g, EpiSwiGLU{ap.hg_hi, ap.hg_lo, I},
-                                  I / (tc::BM / 2), max_tiles, st)))
+                                  I / (tc::BM / 2), max_tiles, nsm, st)))
             return e;
         a.n_out = I, a.k = H;
         if ((e = tc::launch<true>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, ap.hs_lo, I},
-                                  I / (tc::BM / 2), ny, st)))
+                                  I / (tc::BM / 2), ny, nsm, st)))
             return e;
-        // routed down (grouped) into per-(token, slot) rows, then the shared down
-        // projection whose epilogue adds the weighted routed rows and the residual
+        // routed down (grouped) into per-(token, slot) rows; the shared expert's down
+        // projection into the residual; then the weighted routed rows, slot order
         g.n_out = H, g.k = I;
-        ProbDown<float, bf16> pd{nullptr, pb.rows, nullptr, pb.YS, H, I};
-        if ((e = tc::launch<false>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, pd, H / tc::BM, max_tiles, st))) return e;
+        if ((e = tc::launch<false>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H},
+                                   H / tc::BM, max_tiles, nsm, st)))
+            return e;
         a.n_out = H, a.k = I;
-        ProbSharedDown<float, bf16> psd{nullptr, nullptr, pb.YS, pb.wts, pb.X, H, I, K};
-        if ((e = tc::launch<false>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, psd, H / tc::BM, ny, st))) return e;
+        if ((e = tc::launch<false>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, H / tc::BM, ny, nsm, st)))
+            return e;
+        k_moe_combine<<<n, 256, 0, st>>>(pb.X, pb.YS, pb.wts, H, K);
+        ++launch_count();
     }
     return cudaGetLastError();
 }
 
 cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
                              const TcActMaps &am, void *const *kc, void *const *vc, const float2 *rope,
-                             const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n, cudaStream_t st)
+                             const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n, cudaStream_t st,
+                             int nsm)
 {
-    return d.kvdt == DS4G_BF16 ? chunk_tc_t<bf16>(d, layers, lm, am, kc, vc, rope, tok_embd, pb, p0, n, st)
-                               : chunk_tc_t<float>(d, layers, lm, am, kc, vc, rope, tok_embd, pb, p0, n, st);
+    return d.kvdt == DS4G_BF16 ? chunk_tc_t<bf16>(d, layers, lm, am, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
+                               : chunk_tc_t<float>(d, layers, lm, am, kc, vc, rope, tok_embd, pb, p0, n, st, nsm);
 }
 
 }  // namespace ds4g

@@ -21,12 +21,16 @@ struct TcActMaps {     // boxes: 64 columns x 128 token rows
 // Shapes the tensor-core form covers: BF16 weights; every weight piece a multiple
 // of 128 rows (64 for the expert gate/up) and every reduction a multiple of 64.
 bool tc_prefill_eligible(const Dims &d);
+// Tensor-core attention for the prefill (head dim 128, window <= 128, BF16 KV).
+bool attn_mma_eligible(const Dims &d);
+cudaError_t attn_mma_setup(const Dims &d, int max_smem);
 cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m);
 TcActPtrs tc_act_ptrs(const Dims &d, const PrefillBufs &pb);
 cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m);
 cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
                              const TcActMaps &am, void *const *kc, void *const *vc, const float2 *rope,
-                             const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n, cudaStream_t st);
+                             const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n, cudaStream_t st,
+                             int nsm);
 
 // prefill.cu kernels the tensor-core form shares
 __global__ void k_embed_rows(const uint16_t *table, const int *tok, float *X, int H);

@@ -14,19 +14,24 @@
 // the lo tile of the same tokens: two MMAs per 16-wide K step into one FP32
 // accumulator in tensor memory (128 lanes x 128 columns).
 //
-// One CTA computes one 128 x 128 output tile with 192 threads:
+// Persistent: one CTA per SM walks the output tiles (weight-row block fastest, so
+// CTAs running together share a token tile in L2) with 192 threads:
 //   warp 0 lane 0   TMA producer: per 64-wide K stage, the W tile (16 KB) and the
 //                   hi and lo token tiles (16 KB each), 128-byte swizzled, into a
-//                   4-stage shared-memory ring (full / empty mbarriers);
-//   warp 1          allocates the accumulator in TMEM; lane 0 issues the MMAs and
-//                   commits each stage back to the producer, then the tile to the
-//                   epilogue;
-//   warps 2-5       epilogue: TMEM -> registers -> a [token][feature] FP32 tile in
-//                   shared memory (the ring, no longer needed) -> the problem's
-//                   store functor, four adjacent features (or gate/up pairs) at a
-//                   time, so RoPE pairs and SwiGLU pairs are local to one call.
-// Every wait is bounded; a CTA that gives up raises DS4G_ETIMEOUT in *status,
-// drains its copies in flight, frees its TMEM and returns.
+//                   4-stage shared-memory ring (full / empty mbarriers) that runs
+//                   on across tile boundaries;
+//   warp 1          allocates two accumulators in TMEM (2 x 128 columns); lane 0
+//                   issues the MMAs of tile i into accumulator i % 2 as soon as the
+//                   epilogue has drained it, and commits each stage back to the
+//                   producer and each tile to the epilogue;
+//   warps 2-5       epilogue, overlapping the next tile's MMAs: TMEM -> registers ->
+//                   a [token][feature] FP32 half tile in shared memory -> the
+//                   problem's functor, four adjacent features (or gate/up pairs) at
+//                   a time, so RoPE pairs and SwiGLU pairs are local to one call.
+//                   A functor's global loads (load4) are issued eight at a time
+//                   before the matching stores.
+// Every wait is bounded; a CTA that gives up raises DS4G_ETIMEOUT in *status, lets
+// its MMAs and copies finish, frees its TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -45,16 +50,18 @@ static constexpr int THREADS = 192;
 static constexpr uint32_t TILE_A = BM * BK * 2;              // 16 KB
 static constexpr uint32_t TILE_B = BN * BK * 2;              // 16 KB
 static constexpr uint32_t STAGE_BYTES = TILE_A + 2 * TILE_B;  // 48 KB
+static constexpr int HALF = BN / 2;                          // tokens staged at once
 static constexpr int EPI_PITCH = BM + 4;                     // floats per staged token row
-static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
-static_assert((size_t)BN * EPI_PITCH * 4 <= (size_t)STAGES * STAGE_BYTES, "epilogue tile fits the ring");
+static constexpr uint32_t EPI_BYTES = HALF * EPI_PITCH * 4;  // 33 KB
+static constexpr int EPI_BATCH = 8;                          // functor loads in flight
+static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 256;
 
-// What a launch computes.  Dense: token rows [0, m_tok), output tile rows
-// blockIdx.x * BM.  Grouped (tiles != nullptr): work item blockIdx.y is
-// (expert e, first grouped row r0) from the tile list, rows [r0, off[e+1]) of the
-// grouped activations, and expert e's weight rows start at e * n_out.
+// What a launch computes.  Dense: token rows [0, m_tok) in tiles of BN.  Grouped
+// (tiles != nullptr): token tile j is (expert e, first grouped row r0) from the
+// tile list, rows [r0, off[e+1]) of the grouped activations, and expert e's weight
+// rows start at e * n_out.  Weight-row blocks: n_out / BM (n_out / (BM/2) for GU).
 struct Args {
-    int n_out;        // weight rows (per expert when grouped); a multiple of BM (BM/2 for gu)
+    int n_out;        // weight rows (per expert when grouped)
     int k;            // reduction length, a multiple of BK
     int x_col0;       // first activation column read (a multiple of 8)
     int piece_rows;   // dense: rows of map w0 before map w1 starts (0: w0 only)
@@ -64,8 +71,11 @@ struct Args {
     int *status;      // DS4G_ETIMEOUT on a wait that gave up
 };
 
+struct NoAux {};
+
 // GU: tile rows 0-63 come from w0 (gate rows) and 64-127 from w1 (the same up
 // rows); the epilogue then receives (gate, up) pairs through Epi::store_gu4.
+// Otherwise Epi provides  Aux load4(m, n, e)  and  store4(m, n, v[4], aux, e).
 template <class Epi, bool GU>
 __global__ void __launch_bounds__(THREADS, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
@@ -74,42 +84,58 @@ __global__ void __launch_bounds__(THREADS, 1)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES);
+    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // [HALF][EPI_PITCH]
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + EPI_BYTES);
     uint64_t *empty = full + STAGES;
-    uint64_t *accf = empty + STAGES;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(accf + 1);
+    uint64_t *accf = empty + STAGES;   // [2] accumulator ready (MMA commit)
+    uint64_t *acce = accf + 2;         // [2] accumulator drained (128 epilogue threads)
+    uint64_t *done = acce + 2;         // every MMA of this CTA completed
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    int e = 0, r0, rend;
-    if (a.tiles) {
-        const int t = blockIdx.y;
-        if (t >= a.tiles[0]) return;   // uniform over the CTA, before any barrier
-        e = a.tiles[1 + 2 * t];
-        r0 = a.tiles[2 + 2 * t];
-        rend = min(r0 + BN, a.off[e + 1]);
-    } else {
-        r0 = blockIdx.y * BN;
-        rend = min(r0 + BN, a.m_tok);
-    }
-    const int mb = blockIdx.x;
+    const int mtiles = GU ? a.n_out / (BM / 2) : a.n_out / BM;
+    const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BN - 1) / BN;
+    const int total = mtiles * ntiles;
     const int nk = a.k / BK;
+    // tile -> (weight block mb, expert e, first token row r0, end row)
+    auto tile_of = [&](int tau, int &mb, int &e, int &r0, int &rend) {
+        mb = tau % mtiles;
+        const int j = tau / mtiles;
+        if (a.tiles) {
+            e = a.tiles[1 + 2 * j];
+            r0 = a.tiles[2 + 2 * j];
+            rend = min(r0 + BN, a.off[e + 1]);
+        } else {
+            e = 0;
+            r0 = j * BN;
+            rend = min(r0 + BN, a.m_tok);
+        }
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accf, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 128);
+        }
+        mbar_init(done, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 1) tmem_alloc(tslot, BN);
+    if (warp == 1) tmem_alloc(tslot, 2 * BN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     volatile int *ab = abort_flag;
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        atomicExch(a.status, DS4G_ETIMEOUT);
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -118,41 +144,45 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_prefetch_desc(&w1);
             tma_prefetch_desc(&xhi);
             tma_prefetch_desc(&xlo);
-            const void *wm = &w0;
-            int wrow;
-            if (GU) {
-                wrow = e * a.n_out + mb * (BM / 2);
-            } else if (a.piece_rows > 0 && mb * BM >= a.piece_rows) {
-                wm = &w1;
-                wrow = mb * BM - a.piece_rows;
-            } else {
-                wrow = e * a.n_out + mb * BM;
-            }
-            int issued = 0;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % STAGES;
-                if (!mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, ab)) {
-                    *abort_flag = 1;
-                    atomicExch(a.status, DS4G_ETIMEOUT);
-                    break;
-                }
-                unsigned char *st = sm + s * STAGE_BYTES;
-                mbar_expect_tx(&full[s], STAGE_BYTES);
-                const int kx = i * BK;
+            unsigned it = 0;
+            bool ok = true;
+            for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
+                int mb, e, r0, rend;
+                tile_of(tau, mb, e, r0, rend);
+                const void *wm = &w0;
+                int wrow;
                 if (GU) {
-                    tma_load_2d(st, &w0, kx, wrow, &full[s]);
-                    tma_load_2d(st + TILE_A / 2, &w1, kx, wrow, &full[s]);
+                    wrow = e * a.n_out + mb * (BM / 2);
+                } else if (a.piece_rows > 0 && mb * BM >= a.piece_rows) {
+                    wm = &w1;
+                    wrow = mb * BM - a.piece_rows;
                 } else {
-                    tma_load_2d(st, wm, kx, wrow, &full[s]);
+                    wrow = e * a.n_out + mb * BM;
                 }
-                tma_load_2d(st + TILE_A, &xhi, a.x_col0 + kx, r0, &full[s]);
-                tma_load_2d(st + TILE_A + TILE_B, &xlo, a.x_col0 + kx, r0, &full[s]);
-                ++issued;
+                for (int i = 0; i < nk; ++i, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, ab)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    unsigned char *st = sm + s * STAGE_BYTES;
+                    mbar_expect_tx(&full[s], STAGE_BYTES);
+                    const int kx = i * BK;
+                    if (GU) {
+                        tma_load_2d(st, &w0, kx, wrow, &full[s]);
+                        tma_load_2d(st + TILE_A / 2, &w1, kx, wrow, &full[s]);
+                    } else {
+                        tma_load_2d(st, wm, kx, wrow, &full[s]);
+                    }
+                    tma_load_2d(st + TILE_A, &xhi, a.x_col0 + kx, r0, &full[s]);
+                    tma_load_2d(st + TILE_A + TILE_B, &xlo, a.x_col0 + kx, r0, &full[s]);
+                }
             }
             // no copy may still be in flight when the CTA exits
-            const int n = issued < STAGES ? issued : STAGES;
-            for (int q = 1; q <= n; ++q) {
-                const int i = issued - q;
+            const unsigned n = it < (unsigned)STAGES ? it : (unsigned)STAGES;
+            for (unsigned q = 1; q <= n; ++q) {
+                const unsigned i = it - q;
                 volatile int never = 0;
                 mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &never);
             }
@@ -161,71 +191,107 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             // ---------------- MMA issuer
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % STAGES;
-                if (!mbar_wait(&full[s], (i / STAGES) & 1, ab)) {
-                    *abort_flag = 1;
-                    atomicExch(a.status, DS4G_ETIMEOUT);
+            unsigned it = 0, tc = 0;
+            bool ok = true;
+            for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x, ++tc) {
+                const int b = tc & 1;
+                if (!mbar_wait(&acce[b], ((tc >> 1) & 1) ^ 1, ab)) {
+                    give_up();
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(sm + s * STAGE_BYTES);
+                const uint32_t acc = tmem + (uint32_t)(b * BN);
+                for (int i = 0; i < nk; ++i, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(&full[s], (it / STAGES) & 1, ab)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(sm + s * STAGE_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t ad = sdesc_kmajor_sw128(sa + kk * 32);
-                    const uint64_t bh = sdesc_kmajor_sw128(sa + TILE_A + kk * 32);
-                    const uint64_t bl = sdesc_kmajor_sw128(sa + TILE_A + TILE_B + kk * 32);
-                    tc_mma_bf16(tmem, ad, bh, idesc, (i | kk) != 0);
-                    tc_mma_bf16(tmem, ad, bl, idesc, 1u);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = sdesc_kmajor_sw128(sa + kk * 32);
+                        const uint64_t bh = sdesc_kmajor_sw128(sa + TILE_A + kk * 32);
+                        const uint64_t bl = sdesc_kmajor_sw128(sa + TILE_A + TILE_B + kk * 32);
+                        tc_mma_bf16(acc, ad, bh, idesc, (i | kk) != 0);
+                        tc_mma_bf16(acc, ad, bl, idesc, 1u);
+                    }
+                    tc_commit(&empty[s]);   // the stage is free once these MMAs complete
                 }
-                tc_commit(&empty[s]);   // the stage is free once these MMAs complete
+                if (ok) tc_commit(&accf[b]);   // the tile is complete once every MMA is
             }
-            tc_commit(accf);            // the tile is complete once every MMA is
+            // TMEM may be freed only after every MMA issued here has completed
+            tc_commit(done);
+            volatile int never = 0;
+            mbar_wait(done, 0, &never);
         }
     } else {
         // ---------------- epilogue (warps 2-5)
-        const int q = warp & 3;   // TMEM lane quarter this warp may access
-        const bool ok = mbar_wait(accf, 0, ab);
-        if (!ok) {
-            *abort_flag = 1;
-            atomicExch(a.status, DS4G_ETIMEOUT);
-        }
-        tc_fence_after();
-        float *stg = reinterpret_cast<float *>(sm);   // [BN tokens][EPI_PITCH]
-        if (ok && !*ab) {
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                float v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-                const int f = 32 * q + lane;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) stg[(c0 + j) * EPI_PITCH + f] = v[j];
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int et = threadIdx.x - 64;   // 0..127
+        unsigned tc = 0;
+        for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
+            int mb, e, r0, rend;
+            tile_of(tau, mb, e, r0, rend);
+            const int b = tc & 1;
+            if (!mbar_wait(&accf[b], (tc >> 1) & 1, ab)) {
+                give_up();
+                break;
             }
-        }
-        asm volatile("bar.sync 2, 128;" ::: "memory");
-        if (ok && !*ab) {
-            const int t0 = threadIdx.x - 64;   // 0..127
-            if constexpr (GU) {
-                // features 0-63: gate rows, 64-127: the matching up rows
-                for (int idx = t0; idx < BN * (BM / 8); idx += 128) {
-                    const int t = idx / (BM / 8), j = (idx % (BM / 8)) * 4;
-                    const int m = r0 + t;
-                    if (m >= rend) continue;
-                    const float *row = stg + t * EPI_PITCH;
-                    const float4 g = *reinterpret_cast<const float4 *>(row + j);
-                    const float4 u = *reinterpret_cast<const float4 *>(row + BM / 2 + j);
-                    const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {u.x, u.y, u.z, u.w};
-                    epi.store_gu4(m, mb * (BM / 2) + j, gv, uv, e);
+            tc_fence_after();
+            for (int h = 0; h < 2; ++h) {
+                // accumulator columns (tokens) h*HALF .. +HALF-1 into stg[token][feature]
+#pragma unroll 1
+                for (int c0 = 0; c0 < HALF; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + h * HALF + c0), v);
+                    const int f = 32 * q + lane;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) stg[(c0 + j) * EPI_PITCH + f] = v[j];
                 }
-            } else {
-                for (int idx = t0; idx < BN * (BM / 4); idx += 128) {
-                    const int t = idx / (BM / 4), j = (idx % (BM / 4)) * 4;
-                    const int m = r0 + t;
-                    if (m >= rend) continue;
-                    const float4 v4 = *reinterpret_cast<const float4 *>(stg + t * EPI_PITCH + j);
-                    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-                    epi.store4(m, mb * BM + j, v, e);
+                if (h == 1) {   // the accumulator is drained: the next tile may use it
+                    tc_fence_before();
+                    mbar_arrive(&acce[b]);
                 }
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+                const int tbase = r0 + h * HALF;
+                if constexpr (GU) {
+                    // features 0-63: gate rows, 64-127: the matching up rows
+                    for (int idx = et; idx < HALF * (BM / 8); idx += 128) {
+                        const int t = idx / (BM / 8), j = (idx % (BM / 8)) * 4;
+                        const int m = tbase + t;
+                        if (m >= rend) continue;
+                        const float *row = stg + t * EPI_PITCH;
+                        const float4 g = *reinterpret_cast<const float4 *>(row + j);
+                        const float4 u = *reinterpret_cast<const float4 *>(row + BM / 2 + j);
+                        const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {u.x, u.y, u.z, u.w};
+                        epi.store_gu4(m, mb * (BM / 2) + j, gv, uv, e);
+                    }
+                } else {
+                    constexpr int NI = HALF * (BM / 4) / 128;   // items per thread (16)
+#pragma unroll 1
+                    for (int i0 = 0; i0 < NI; i0 += EPI_BATCH) {
+                        typename Epi::Aux aux[EPI_BATCH];
+#pragma unroll
+                        for (int u = 0; u < EPI_BATCH; ++u) {
+                            const int idx = et + 128 * (i0 + u);
+                            const int t = idx / (BM / 4), j = (idx % (BM / 4)) * 4;
+                            if (tbase + t < rend) aux[u] = epi.load4(tbase + t, mb * BM + j, e);
+                        }
+#pragma unroll
+                        for (int u = 0; u < EPI_BATCH; ++u) {
+                            const int idx = et + 128 * (i0 + u);
+                            const int t = idx / (BM / 4), j = (idx % (BM / 4)) * 4;
+                            if (tbase + t >= rend) continue;
+                            const float4 v4 = *reinterpret_cast<const float4 *>(stg + t * EPI_PITCH + j);
+                            const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+                            epi.store4(tbase + t, mb * BM + j, v, aux[u], e);
+                        }
+                    }
+                }
+                asm volatile("bar.sync 2, 128;" ::: "memory");   // stg is rewritten next
             }
         }
     }
@@ -233,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, BN);
+        tmem_dealloc(tmem, 2 * BN);
     }
 }
 
@@ -244,12 +310,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 // `rows` read as zeros.
 cudaError_t make_map_bf16(CUtensorMap *m, const void *base, int rows, int cols, int ld, int box_rows);
 
+// ntile_bound: token tiles at most (dense: exact; grouped: the tile list's bound).
 template <bool GU, class Epi>
 static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
-                          const CUtensorMap &xlo, const Args &a, const Epi &epi, int grid_x, int grid_y,
-                          cudaStream_t st)
+                          const CUtensorMap &xlo, const Args &a, const Epi &epi, int mtiles, int ntile_bound,
+                          int nsm, cudaStream_t st)
 {
-    if (grid_x <= 0 || grid_y <= 0) return cudaSuccess;
+    const long long work = (long long)mtiles * ntile_bound;
+    if (work <= 0) return cudaSuccess;
     static bool attr_set = false;   // per instantiation; set before the first launch
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -257,7 +325,8 @@ static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CU
         if (e) return e;
         attr_set = true;
     }
-    k_tc_gemm<Epi, GU><<<dim3(grid_x, grid_y), THREADS, SMEM_BYTES, st>>>(w0, w1, xhi, xlo, a, epi);
+    const int grid = (int)(work < nsm ? work : nsm);
+    k_tc_gemm<Epi, GU><<<grid, THREADS, SMEM_BYTES, st>>>(w0, w1, xhi, xlo, a, epi);
     ++launch_count();
     return cudaGetLastError();
 }
