@@ -216,6 +216,9 @@ __device__ __forceinline__ bool warp_topk(const float *s, int E, int K, float *s
     return finite;
 }
 
+// SwiGLU of one gate/up pair: silu(g) * u.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
 template <typename T> struct VecOf;
 template <> struct VecOf<bf16> { static constexpr int n = 8; };
 template <> struct VecOf<float> { static constexpr int n = 4; };

@@ -94,7 +94,6 @@ struct ProbRouter {  // S = XN W_r^T from f32 activations (f32 scores)
     }
 };
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 // Gate/up with SwiGLU; W rows interleaved (gate_i, up_i) so an output pair is local.
 template <typename TA, typename TW, bool GROUPED>

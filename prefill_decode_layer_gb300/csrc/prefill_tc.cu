@@ -27,24 +27,39 @@ __device__ __forceinline__ void split_hilo(float v, bf16 &h, bf16 &l)
     l = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
-// RMSNorm of each residual row into hi/lo BF16 (one CTA per token row).
-__global__ void __launch_bounds__(256) k_rmsnorm_hilo(const float *X, const float *g, bf16 *hi, bf16 *lo,
-                                                      int H, float eps)
+// RMSNorm of each residual row into hi/lo BF16: one CTA per token row, H/4 threads
+// (at most 1024), each keeping its float4s in registers between the two passes.
+__global__ void __launch_bounds__(1024) k_rmsnorm_hilo(const float *X, const float *g, bf16 *hi, bf16 *lo,
+                                                       int H, float eps)
 {
     __shared__ float red[32];
-    const int t = blockIdx.x;
-    const float *x = X + (size_t)t * H;
+    const int t = blockIdx.x, nv = H / 4;
+    const float4 *x = reinterpret_cast<const float4 *>(X + (size_t)t * H);
+    float4 v[4];
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        v[u] = i < nv ? x[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss = fmaf(v[u].x, v[u].x, fmaf(v[u].y, v[u].y, fmaf(v[u].z, v[u].z, fmaf(v[u].w, v[u].w, ss))));
+    }
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / (float)H + eps);
-    for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        bf16 h, l;
-        split_hilo(x[i] * inv * g[i], h, l);
-        hi[(size_t)t * H + i] = h;
-        lo[(size_t)t * H + i] = l;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = threadIdx.x + u * blockDim.x;
+        if (i >= nv) continue;
+        const float4 gv = reinterpret_cast<const float4 *>(g)[i];
+        __align__(8) bf16 h[4], l[4];
+        split_hilo(v[u].x * inv * gv.x, h[0], l[0]);
+        split_hilo(v[u].y * inv * gv.y, h[1], l[1]);
+        split_hilo(v[u].z * inv * gv.z, h[2], l[2]);
+        split_hilo(v[u].w * inv * gv.w, h[3], l[3]);
+        *reinterpret_cast<uint2 *>(hi + (size_t)t * H + 4 * i) = *reinterpret_cast<const uint2 *>(h);
+        *reinterpret_cast<uint2 *>(lo + (size_t)t * H + 4 * i) = *reinterpret_cast<const uint2 *>(l);
     }
 }
+static int rmsnorm_threads(int H) { return H / 4 < 1024 ? ((H / 4 + 31) / 32) * 32 : 1024; }
 
 // Grouped copy of the MoE input: row r <- token rows[r] / K (16-byte chunks).
 __global__ void __launch_bounds__(256) k_gather_rows(const bf16 *hi, const bf16 *lo, const int *rows, int K,
@@ -383,16 +398,15 @@ struct EpiRoutedRows {   // routed expert output of grouped row m into its (toke
     }
 };
 
-struct EpiSwiGLU {   // h[m][i..i+3] = silu(gate) * up, as hi/lo BF16
+struct EpiSwiGLU {   // h[m][i] = silu(gate) * up as hi/lo BF16
     bf16 *hi, *lo;
     int ld;
-    __device__ void store_gu4(int m, int i, const float (&g)[4], const float (&u)[4], int) const
+    __device__ void store_h(int m, int i, float h, int) const
     {
-        __align__(8) bf16 h[4], l[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) split_hilo(silu_mul(g[j], u[j]), h[j], l[j]);
-        *reinterpret_cast<uint2 *>(hi + (size_t)m * ld + i) = *reinterpret_cast<const uint2 *>(h);
-        *reinterpret_cast<uint2 *>(lo + (size_t)m * ld + i) = *reinterpret_cast<const uint2 *>(l);
+        bf16 hv, lv;
+        split_hilo(h, hv, lv);
+        hi[(size_t)m * ld + i] = hv;
+        lo[(size_t)m * ld + i] = lv;
     }
 };
 
@@ -428,8 +442,8 @@ __global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, 
 
 bool tc_prefill_eligible(const Dims &d)
 {
-    return d.wdt == DS4G_BF16 && d.H % 128 == 0 && d.RQ % 128 == 0 && d.RKV % 128 == 0 &&
-           d.QD % 128 == 0 && d.HD % 128 == 0 && d.E % 128 == 0 && d.I % 64 == 0;
+    return d.wdt == DS4G_BF16 && d.H % 128 == 0 && d.H <= 16384 && d.RQ % 128 == 0 && d.RKV % 128 == 0 &&
+           d.QD % 128 == 0 && d.HD % 128 == 0 && d.E % 128 == 0 && d.I % 128 == 0;
 }
 
 cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m)
@@ -444,11 +458,11 @@ cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m)
     if ((e = make_map_bf16(&m.wvb, w.wv_b, d.HD, d.RKV, d.RKV, 128))) return e;
     if ((e = make_map_bf16(&m.wo, w.wo, H, d.QD, d.QD, 128))) return e;
     if ((e = make_map_bf16(&m.wr, w.w_router, E, H, H, 128))) return e;
-    if ((e = make_map_bf16(&m.wsg, w.ws_gate, I, H, H, 64))) return e;
-    if ((e = make_map_bf16(&m.wsu, w.ws_up, I, H, H, 64))) return e;
+    if ((e = make_map_bf16(&m.wsg, w.ws_gate, I, H, H, 128))) return e;
+    if ((e = make_map_bf16(&m.wsu, w.ws_up, I, H, H, 128))) return e;
     if ((e = make_map_bf16(&m.wsd, w.ws_down, H, I, I, 128))) return e;
-    if ((e = make_map_bf16(&m.wg, w.w_gate, E * I, H, H, 64))) return e;
-    if ((e = make_map_bf16(&m.wu, w.w_up, E * I, H, H, 64))) return e;
+    if ((e = make_map_bf16(&m.wg, w.w_gate, E * I, H, H, 128))) return e;
+    if ((e = make_map_bf16(&m.wu, w.w_up, E * I, H, H, 128))) return e;
     return make_map_bf16(&m.wd, w.w_down, E * H, I, I, 128);
 }
 
@@ -515,7 +529,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         a.status = pb.status;
         a.m_tok = n;
         // ---- attention half
-        k_rmsnorm_hilo<<<n, 256, 0, st>>>(pb.X, w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
+        k_rmsnorm_hilo<<<n, rmsnorm_threads(H), 0, st>>>(pb.X, w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
         ++launch_count();
         a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ, a.x_col0 = 0;
         if ((e = tc::launch<false>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a, EpiHiLo{ap.c_hi, ap.c_lo, d.RQ + d.RKV},
@@ -545,7 +559,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         if ((e = tc::launch<false>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, H / tc::BM, ny, nsm, st)))
             return e;
         // ---- MoE half
-        k_rmsnorm_hilo<<<n, 256, 0, st>>>(pb.X, w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
+        k_rmsnorm_hilo<<<n, rmsnorm_threads(H), 0, st>>>(pb.X, w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
         ++launch_count();
         a.n_out = d.E, a.k = H;
         if ((e = tc::launch<false>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, d.E / tc::BM, ny, nsm,
@@ -567,11 +581,11 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         g.status = pb.status;
         g.n_out = I, g.k = H, g.tiles = pb.tiles, g.off = pb.off;
         if ((e = tc::launch<true>(m.wg, m.wu, am.xg_hi, am.xg_lo, g, EpiSwiGLU{ap.hg_hi, ap.hg_lo, I},
-                                  I / (tc::BM / 2), max_tiles, nsm, st)))
+                                  I / tc::BM, max_tiles, nsm, st)))
             return e;
         a.n_out = I, a.k = H;
         if ((e = tc::launch<true>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, ap.hs_lo, I},
-                                  I / (tc::BM / 2), ny, nsm, st)))
+                                  I / tc::BM, ny, nsm, st)))
             return e;
         // routed down (grouped) into per-(token, slot) rows; the shared expert's down
         // projection into the residual; then the weighted routed rows, slot order

@@ -8,7 +8,7 @@
 
 namespace ds4g {
 
-struct TcLayerMaps {   // boxes: 64 columns x 128 rows (64 rows for gate/up)
+struct TcLayerMaps {   // boxes: 64 columns x 128 rows
     CUtensorMap wqa, wkva, wqb, wkb, wvb, wo, wr, wsg, wsu, wsd, wg, wu, wd;
 };
 struct TcActPtrs {     // hi/lo BF16 halves of the prefill activation buffers
@@ -19,7 +19,7 @@ struct TcActMaps {     // boxes: 64 columns x 128 token rows
 };
 
 // Shapes the tensor-core form covers: BF16 weights; every weight piece a multiple
-// of 128 rows (64 for the expert gate/up) and every reduction a multiple of 64.
+// of 128 rows and every reduction a multiple of 64.
 bool tc_prefill_eligible(const Dims &d);
 // Tensor-core attention for the prefill (head dim 128, window <= 128, BF16 KV).
 bool attn_mma_eligible(const Dims &d);

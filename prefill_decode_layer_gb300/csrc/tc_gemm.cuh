@@ -26,10 +26,12 @@
 //                   producer and each tile to the epilogue;
 //   warps 2-5       epilogue, overlapping the next tile's MMAs: TMEM -> registers ->
 //                   a [token][feature] FP32 half tile in shared memory -> the
-//                   problem's functor, four adjacent features (or gate/up pairs) at
-//                   a time, so RoPE pairs and SwiGLU pairs are local to one call.
-//                   A functor's global loads (load4) are issued eight at a time
-//                   before the matching stores.
+//                   problem's functor, four adjacent features at a time, so RoPE
+//                   pairs are local to one call; a functor's global loads (load4)
+//                   are issued eight at a time before the matching stores.
+// Gate/up tiles (GU) hold 128 gate rows and the same 128 up rows in two
+// accumulators that share each token tile; SwiGLU is applied straight from the
+// two accumulators (a feature's gate and up sit in the same TMEM lane).
 // Every wait is bounded; a CTA that gives up raises DS4G_ETIMEOUT in *status, lets
 // its MMAs and copies finish, frees its TMEM and returns.
 #pragma once
@@ -42,24 +44,35 @@
 namespace ds4g {
 namespace tc {
 
-static constexpr int BM = 128;      // weight rows per tile (MMA M)
+static constexpr int BM = 128;      // weight rows per accumulator (MMA M)
 static constexpr int BN = 128;      // tokens per tile (MMA N)
 static constexpr int BK = 64;       // K per stage: one 128-byte swizzle row of BF16
-static constexpr int STAGES = 4;
 static constexpr int THREADS = 192;
 static constexpr uint32_t TILE_A = BM * BK * 2;              // 16 KB
 static constexpr uint32_t TILE_B = BN * BK * 2;              // 16 KB
-static constexpr uint32_t STAGE_BYTES = TILE_A + 2 * TILE_B;  // 48 KB
 static constexpr int HALF = BN / 2;                          // tokens staged at once
 static constexpr int EPI_PITCH = BM + 4;                     // floats per staged token row
 static constexpr uint32_t EPI_BYTES = HALF * EPI_PITCH * 4;  // 33 KB
 static constexpr int EPI_BATCH = 8;                          // functor loads in flight
-static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 256;
+
+// Tile geometry.  Plain: 128 weight rows, one accumulator, 4 stages of 48 KB and a
+// staged epilogue.  Gate/up (GU): 128 gate rows and the same 128 up rows, two
+// accumulators sharing every token tile (the activations are read half as often),
+// 3 stages of 64 KB, and SwiGLU straight from the two accumulators.
+template <bool GU> struct Geo {
+    static constexpr int NACC = GU ? 2 : 1;
+    static constexpr uint32_t XOFF = NACC * TILE_A;          // token tiles after the W tiles
+    static constexpr uint32_t STAGE = XOFF + 2 * TILE_B;
+    static constexpr int STAGES = GU ? 3 : 4;
+    static constexpr uint32_t TMEM_COLS = 2 * NACC * BN;     // two tiles in flight
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (GU ? 0 : EPI_BYTES) + 256;
+};
 
 // What a launch computes.  Dense: token rows [0, m_tok) in tiles of BN.  Grouped
 // (tiles != nullptr): token tile j is (expert e, first grouped row r0) from the
 // tile list, rows [r0, off[e+1]) of the grouped activations, and expert e's weight
-// rows start at e * n_out.  Weight-row blocks: n_out / BM (n_out / (BM/2) for GU).
+// rows start at e * n_out.  Weight-row blocks: n_out / BM (for GU, n_out is the
+// number of gate rows = up rows).
 struct Args {
     int n_out;        // weight rows (per expert when grouped)
     int k;            // reduction length, a multiple of BK
@@ -73,8 +86,8 @@ struct Args {
 
 struct NoAux {};
 
-// GU: tile rows 0-63 come from w0 (gate rows) and 64-127 from w1 (the same up
-// rows); the epilogue then receives (gate, up) pairs through Epi::store_gu4.
+// GU: the tile's gate rows come from w0 and its up rows from w1 (same row index);
+// the epilogue calls Epi::store_h(m, i, silu(gate) * up, e) per element.
 // Otherwise Epi provides  Aux load4(m, n, e)  and  store4(m, n, v[4], aux, e).
 template <class Epi, bool GU>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -82,10 +95,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               const __grid_constant__ CUtensorMap xhi, const __grid_constant__ CUtensorMap xlo,
               const Args a, const Epi epi)
 {
+    using G = Geo<GU>;
+    constexpr int STAGES = G::STAGES;
+    constexpr uint32_t STAGE_BYTES = G::STAGE;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // [HALF][EPI_PITCH]
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + EPI_BYTES);
+    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // [HALF][EPI_PITCH] (plain)
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + (GU ? 0 : EPI_BYTES));
     uint64_t *empty = full + STAGES;
     uint64_t *accf = empty + STAGES;   // [2] accumulator ready (MMA commit)
     uint64_t *acce = accf + 2;         // [2] accumulator drained (128 epilogue threads)
@@ -94,7 +110,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int mtiles = GU ? a.n_out / (BM / 2) : a.n_out / BM;
+    const int mtiles = a.n_out / BM;
     const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BN - 1) / BN;
     const int total = mtiles * ntiles;
     const int nk = a.k / BK;
@@ -126,7 +142,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 1) tmem_alloc(tslot, 2 * BN);
+    if (warp == 1) tmem_alloc(tslot, G::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -152,7 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const void *wm = &w0;
                 int wrow;
                 if (GU) {
-                    wrow = e * a.n_out + mb * (BM / 2);
+                    wrow = e * a.n_out + mb * BM;
                 } else if (a.piece_rows > 0 && mb * BM >= a.piece_rows) {
                     wm = &w1;
                     wrow = mb * BM - a.piece_rows;
@@ -171,12 +187,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int kx = i * BK;
                     if (GU) {
                         tma_load_2d(st, &w0, kx, wrow, &full[s]);
-                        tma_load_2d(st + TILE_A / 2, &w1, kx, wrow, &full[s]);
+                        tma_load_2d(st + TILE_A, &w1, kx, wrow, &full[s]);
                     } else {
                         tma_load_2d(st, wm, kx, wrow, &full[s]);
                     }
-                    tma_load_2d(st + TILE_A, &xhi, a.x_col0 + kx, r0, &full[s]);
-                    tma_load_2d(st + TILE_A + TILE_B, &xlo, a.x_col0 + kx, r0, &full[s]);
+                    tma_load_2d(st + G::XOFF, &xhi, a.x_col0 + kx, r0, &full[s]);
+                    tma_load_2d(st + G::XOFF + TILE_B, &xlo, a.x_col0 + kx, r0, &full[s]);
                 }
             }
             // no copy may still be in flight when the CTA exits
@@ -200,7 +216,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)(b * BN);
+                const uint32_t acc = tmem + (uint32_t)(b * G::NACC * BN);
                 for (int i = 0; i < nk; ++i, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(&full[s], (it / STAGES) & 1, ab)) {
@@ -212,11 +228,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sa = smem_u32(sm + s * STAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = sdesc_kmajor_sw128(sa + kk * 32);
-                        const uint64_t bh = sdesc_kmajor_sw128(sa + TILE_A + kk * 32);
-                        const uint64_t bl = sdesc_kmajor_sw128(sa + TILE_A + TILE_B + kk * 32);
-                        tc_mma_bf16(acc, ad, bh, idesc, (i | kk) != 0);
-                        tc_mma_bf16(acc, ad, bl, idesc, 1u);
+                        const uint64_t bh = sdesc_kmajor_sw128(sa + G::XOFF + kk * 32);
+                        const uint64_t bl = sdesc_kmajor_sw128(sa + G::XOFF + TILE_B + kk * 32);
+#pragma unroll
+                        for (int r = 0; r < G::NACC; ++r) {   // gate (and up) accumulators
+                            const uint64_t ad = sdesc_kmajor_sw128(sa + r * TILE_A + kk * 32);
+                            tc_mma_bf16(acc + r * BN, ad, bh, idesc, (i | kk) != 0);
+                            tc_mma_bf16(acc + r * BN, ad, bl, idesc, 1u);
+                        }
                     }
                     tc_commit(&empty[s]);   // the stage is free once these MMAs complete
                 }
@@ -241,6 +260,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
+            if constexpr (GU) {
+                // gate and up of feature f = this thread's lane, 32 tokens at a time
+                const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN);
+                const int i = mb * BM + 32 * q + lane;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    float g[32], u[32];
+                    tmem_ld32(lane_base + (uint32_t)c0, g);
+                    tmem_ld32(lane_base + (uint32_t)(BN + c0), u);
+                    if (c0 == BN - 32) {   // the accumulators are drained
+                        tc_fence_before();
+                        mbar_arrive(&acce[b]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {   // static indices keep g, u in registers
+                        const int m = r0 + c0 + j;
+                        if (m < rend) epi.store_h(m, i, silu_mul(g[j], u[j]), e);
+                    }
+                }
+            } else {
             for (int h = 0; h < 2; ++h) {
                 // accumulator columns (tokens) h*HALF .. +HALF-1 into stg[token][feature]
 #pragma unroll 1
@@ -257,19 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 asm volatile("bar.sync 2, 128;" ::: "memory");
                 const int tbase = r0 + h * HALF;
-                if constexpr (GU) {
-                    // features 0-63: gate rows, 64-127: the matching up rows
-                    for (int idx = et; idx < HALF * (BM / 8); idx += 128) {
-                        const int t = idx / (BM / 8), j = (idx % (BM / 8)) * 4;
-                        const int m = tbase + t;
-                        if (m >= rend) continue;
-                        const float *row = stg + t * EPI_PITCH;
-                        const float4 g = *reinterpret_cast<const float4 *>(row + j);
-                        const float4 u = *reinterpret_cast<const float4 *>(row + BM / 2 + j);
-                        const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {u.x, u.y, u.z, u.w};
-                        epi.store_gu4(m, mb * (BM / 2) + j, gv, uv, e);
-                    }
-                } else {
+                {
                     constexpr int NI = HALF * (BM / 4) / 128;   // items per thread (16)
 #pragma unroll 1
                     for (int i0 = 0; i0 < NI; i0 += EPI_BATCH) {
@@ -293,13 +320,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 asm volatile("bar.sync 2, 128;" ::: "memory");   // stg is rewritten next
             }
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 2 * BN);
+        tmem_dealloc(tmem, G::TMEM_COLS);
     }
 }
 
@@ -321,12 +349,12 @@ static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CU
     static bool attr_set = false;   // per instantiation; set before the first launch
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
+                                             (int)Geo<GU>::SMEM);
         if (e) return e;
         attr_set = true;
     }
     const int grid = (int)(work < nsm ? work : nsm);
-    k_tc_gemm<Epi, GU><<<grid, THREADS, SMEM_BYTES, st>>>(w0, w1, xhi, xlo, a, epi);
+    k_tc_gemm<Epi, GU><<<grid, THREADS, Geo<GU>::SMEM, st>>>(w0, w1, xhi, xlo, a, epi);
     ++launch_count();
     return cudaGetLastError();
 }
