@@ -203,7 +203,9 @@ enum {
     DS4G_DBG_HIDDEN = 8,  /* f32 [H] final hidden state (same as DS4G_DBG_X) */
     DS4G_DBG_PREFILL_X = 9, /* f32 [prefill_chunk][H] final hidden states of the last
                                prefill chunk (row t = t-th token of that chunk) */
-    DS4G_DBG_STATUS = 10    /* int32 raw device status word (0: no device-side error) */
+    DS4G_DBG_STATUS = 10,   /* int32 raw device status word (0: no device-side error) */
+    DS4G_DBG_PREFILL_LAYER_X = 11 /* f32 [L+1][H]: the last prefilled token's residual
+                                     entering each layer, then its final hidden state */
 };
 const void *ds4g_session_debug(const ds4g_session *s, int which);
 

@@ -137,6 +137,7 @@ Layout layout(const ds4g_config &c, int n_ctx)
     o += al(64);                                       // barrier + status
     o += al((size_t)d.L * sizeof(LayerPtrs));          // layer table
     o += al((size_t)2 * d.L * sizeof(void *));         // K/V pointer table
+    o += al((size_t)(d.L + 1) * d.H * 4);              // prefill: last token entering each layer
     L.pre = o;
     o += prefill_bytes(d, prefill_P(c));
     L.total = o;
@@ -291,10 +292,12 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     b.status = s->status;
     s->layers_dev = (LayerPtrs *)take((size_t)d.L * sizeof(LayerPtrs));
     s->kv_dev = (void **)take((size_t)2 * d.L * sizeof(void *));
+    float *layer_x = (float *)take((size_t)(d.L + 1) * d.H * 4);
     s->kv_host.assign(s->kc.begin(), s->kc.end());
     s->kv_host.insert(s->kv_host.end(), s->vc.begin(), s->vc.end());
     prefill_carve(d, prefill_P(m->cfg), base + L.pre, s->pb);
     s->pb.status = s->status;
+    s->pb.layer_x = layer_x;
     if (m->tc && tc_act_maps(d, s->pb, s->tcact)) {
         delete s;
         return DS4G_ECUDA;
@@ -338,6 +341,7 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
     const int P = s->pb.P;
     for (int c = 0; c < n; c += P) {
         const int nc = n - c < P ? n - c : P;
+        s->pb.rec_row = c + nc == n ? nc - 1 : -1;   // record the last token's layer inputs
         cudaError_t e = cudaMemcpyAsync(s->pb.tok, tokens + c, (size_t)nc * 4,
                                         cudaMemcpyHostToDevice, s->st);
         if (!e)
@@ -505,6 +509,7 @@ const void *ds4g_session_debug(const ds4g_session *s, int which)
     case DS4G_DBG_HIDDEN: return s->b.x;
     case DS4G_DBG_PREFILL_X: return s->pb.X;
     case DS4G_DBG_STATUS: return s->status;
+    case DS4G_DBG_PREFILL_LAYER_X: return s->pb.layer_x;
     default: return nullptr;
     }
 }

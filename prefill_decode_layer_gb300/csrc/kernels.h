@@ -47,6 +47,8 @@ struct PrefillBufs {
     void *HS;         // [P][I] shared SwiGLU hidden
     float *YS;        // [P*K][H] routed expert outputs, token-slot order
     int *status;      // session status word (set after carving)
+    float *layer_x;   // [L+1][H]: residual of chunk row rec_row entering each layer, then final
+    int rec_row;      // chunk row to record (-1: none)
 };
 size_t prefill_bytes(const Dims &d, int P);
 void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb);

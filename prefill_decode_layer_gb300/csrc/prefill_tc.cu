@@ -521,7 +521,12 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
     k_embed_rows<<<n, 256, 0, st>>>(tok_embd, pb.tok, pb.X, H);
     ++launch_count();
     if ((e = cudaGetLastError())) return e;
-    for (int l = 0; l < d.L; ++l) {
+    for (int l = 0; l <= d.L; ++l) {
+        if (pb.rec_row >= 0 && pb.layer_x &&
+            (e = cudaMemcpyAsync(pb.layer_x + (size_t)l * H, pb.X + (size_t)pb.rec_row * H, (size_t)H * 4,
+                                 cudaMemcpyDeviceToDevice, st)))
+            return e;
+        if (l == d.L) break;
         const LayerPtrs &w = layers[l];
         const TcLayerMaps &m = lm[l];
         TKV *kc = (TKV *)kcs[l], *vc = (TKV *)vcs[l];

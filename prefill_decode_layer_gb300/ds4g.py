@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "libds4g.so")
 F32, BF16 = 0, 1
 OK, EINVAL, ECONTEXT, ETOKEN, ECUDA, ETIMEOUT, ESIZE, ENONFINITE = 0, -1, -2, -3, -4, -5, -6, -7
 DEBUG = {"x": 0, "cqkv": 1, "q": 2, "attn": 3, "xmid": 4, "xn2": 5, "scores": 6, "h": 7,
-         "hidden": 8, "prefill_x": 9, "status": 10}
+         "hidden": 8, "prefill_x": 9, "status": 10, "prefill_layer_x": 11}
 
 
 KERNEL_KINDS = ("qkv_a", "qkv_b", "attn", "wo", "router", "expert_gu", "expert_down", "lm_head")
