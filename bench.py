@@ -77,13 +77,13 @@ def peaks():
 
 def ncu_traffic(kernel: str):
     """DRAM bytes (read + write) per launch from the committed ncu summary, if it was
-    taken on the current kernel source (same digest of decode_persistent.cu and
-    common.cuh), else None."""
+    taken on the current kernel source (same digest of decode_persistent.cu,
+    common.cuh and sm100.cuh), else None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     csrc = os.path.join(ROOT, "prefill_decode_layer_gb300", "csrc")
     try:
         h = hashlib.sha1()
-        for name in ("decode_persistent.cu", "common.cuh"):
+        for name in ("decode_persistent.cu", "common.cuh", "sm100.cuh"):
             h.update(open(os.path.join(csrc, name), "rb").read())
         digest = h.hexdigest()[:12]
         for line in open(path):
@@ -235,8 +235,11 @@ def workload_config(m):
 #   still streams more weight bytes (about 265 MB) than the 129 MB L2.
 # prefill-full: the layer-major prefill workload (8 full-width layers, 4096 tokens),
 #   each step truncates the session to 0 and prefills the same prompt again.
+# prefill-small: one full-width layer with 128 routed experts and 2048 tokens (about
+#   3 GB on the device; still 96 tokens per expert, as in prefill-full).
 CASES = {"decode-full": dict(), "decode-small": dict(n_experts=32, vocab=8192),
-         "prefill-full": dict(n_layers=8)}
+         "prefill-full": dict(n_layers=8), "prefill-small": dict(n_layers=1, n_experts=128)}
+PREFILL_TOKENS = {"prefill-full": 4096, "prefill-small": 2048}
 
 
 def run_case(args):
@@ -247,8 +250,9 @@ def run_case(args):
     if args.case.startswith("prefill"):
         emb, lm, layers = tw.dev_model(shape)
         m = pdl.Model(shape, emb, lm, layers)
-        s = pdl.Session(m, 4096 + 8)
-        toks = synth.host_tokens(4096, shape.vocab, stream=41)
+        nt = PREFILL_TOKENS[args.case]
+        s = pdl.Session(m, nt + 8)
+        toks = synth.host_tokens(nt, shape.vocab, stream=41)
         for i in range(args.warmup + args.steps):
             assert s.truncate(0) == 0 and s.prefill(toks) == 0
         torch.cuda.synchronize()
