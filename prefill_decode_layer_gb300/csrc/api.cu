@@ -40,6 +40,7 @@ struct ds4g_session {
     void **kv_dev;              // [2L] device K then V cache pointers
     unsigned *bar;              // grid-barrier arrival counter of the persistent kernel
     unsigned bar_count = 0;     // its value after every launch so far (host copy)
+    unsigned kv_count = 0;      // K/V-row counter (bar[1]) after every launch so far
     int *status;                // device status word
     std::vector<void *> kv_host;
     uint64_t launches = 0;
@@ -385,13 +386,15 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
         pa.logits = logits ? 1 : 0;
         pa.bar = s->bar;
         pa.bar_base = s->bar_count;
+        pa.kv_base = s->kv_count;
         pa.status = s->status;
         pa.trace = s->trace;
         pa.trace_events = s->trace_events;
         if (decode_persistent(pa, s->st, s->m->nsm)) return DS4G_ECUDA;
-        // grid barriers per launch: six inside every layer, one between layers and
-        // one before the lm_head
-        s->bar_count += (unsigned)(7 * d.L - 1 + pa.logits) * (unsigned)s->m->nsm;
+        // grid barriers per launch: five inside every layer, one between layers and
+        // one before the lm_head; two K/V-row publications per layer
+        s->bar_count += (unsigned)(6 * d.L - 1 + pa.logits) * (unsigned)s->m->nsm;
+        s->kv_count += 2u * (unsigned)d.L;
         s->hist[s->len] = token;
         s->len += 1;
         return DS4G_OK;
@@ -527,6 +530,7 @@ int ds4g_session_status(ds4g_session *s)
         e = cudaMemsetAsync(s->bar, 0, 64, s->st);
         if (!e) e = cudaStreamSynchronize(s->st);
         s->bar_count = 0;
+        s->kv_count = 0;
         if (e) return DS4G_ECUDA;
         return st == DS4G_ENONFINITE ? DS4G_ENONFINITE : DS4G_ETIMEOUT;
     }

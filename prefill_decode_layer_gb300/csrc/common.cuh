@@ -68,8 +68,9 @@ struct PersistArgs {
     const uint16_t *tok_embd;
     const void *lm_head;
     int pos, token, logits;
-    unsigned *bar;             // grid-barrier arrival counter (only grows)
+    unsigned *bar;             // [0] grid-barrier arrivals, [1] K/V rows published (both only grow)
     unsigned bar_base;         // its value when this launch starts
+    unsigned kv_base;          // value of the K/V-row counter (bar[1]) when this launch starts
     int *status;               // DS4G_ETIMEOUT if a barrier wait gave up
     unsigned long long *trace; // optional [events][gridDim] stage start times (ns)
     int trace_events;

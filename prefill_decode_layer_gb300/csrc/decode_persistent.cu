@@ -137,6 +137,22 @@ template <typename TW> __device__ __forceinline__ Piece piece(const void *b, int
     return p;
 }
 
+// Stages 2-3 of a layer are one stage.  CTA h < NH computes the queries of head h
+// (its HD rows of W_qb) and attends for that head; CTA NH computes the new K row
+// (W_kb) and CTA NH+1 the new V row (W_vb), and they publish them through the kv
+// counter.  Other CTAs have no work in it.  kind: 0 head, 1 K, 2 V, -1 none.
+__device__ __forceinline__ int qkv_kind(int nh)
+{
+    const int c = blockIdx.x;
+    return c < nh ? 0 : (c == nh ? 1 : (c == nh + 1 ? 2 : -1));
+}
+template <typename TW> __device__ __forceinline__ Piece qkv_piece(const LayerPtrs &w, const Dims &d, int kind)
+{
+    if (kind == 0)
+        return piece<TW>(static_cast<const TW *>(w.wq_b) + (size_t)blockIdx.x * d.HD * d.RQ, d.HD, d.RQ);
+    return piece<TW>(kind == 1 ? w.wk_b : w.wv_b, d.HD, d.RKV);
+}
+
 __device__ __forceinline__ void cta_range(int n, int &lo, int &hi)
 {
     lo = (int)((long long)n * blockIdx.x / gridDim.x);
@@ -525,15 +541,15 @@ __device__ __noinline__ float cload_f16_g(const uint16_t *src, const float *g, f
     return ss;
 }
 
-// Sliding-window MQA for the heads h = blockIdx.x, blockIdx.x + gridDim.x, ...: the
-// K/V rows of the window (positions lo_w .. pos) are read straight from L2 (the
-// current row was written by another CTA of this launch).  Scores: `tpk` adjacent
-// threads share a key, each holding up to eight 16-byte vectors of it in flight.
-// Output: thread t accumulates vector t % nkv of V over the keys j = g, g + G, ...
-// (g = t / nkv), and the G partial sums are added in group order.
+// Sliding-window MQA for head h: the query (after RoPE, times 1/sqrt(HD)) is in
+// att[0, HD); the K/V rows of the window (positions lo_w .. pos) are read straight
+// from L2 (the current row was written by another CTA of this launch).  Scores:
+// `tpk` adjacent threads share a key, each holding up to eight 16-byte vectors of it
+// in flight.  Output: thread t accumulates vector t % nkv of V over the keys
+// j = g, g + G, ... (g = t / nkv), and the G partial sums are added in group order.
 template <typename TKV>
-__device__ __noinline__ void attention_heads(const PersistArgs &a, const TKV *kw, const TKV *vw, int n,
-                                             float *att, float *red)
+__device__ __noinline__ void attention_head(const PersistArgs &a, int h, const TKV *kw, const TKV *vw, int n,
+                                            float *att, float *red)
 {
     const Dims &d = a.d;
     constexpr int KVEC = VecOf<TKV>::n;
@@ -541,104 +557,98 @@ __device__ __noinline__ void attention_heads(const PersistArgs &a, const TKV *kw
     int tpk = 1;
     while (tpk * 8 < nkv) tpk <<= 1;
     const int kpp = kCT / tpk, G = kCT / nkv;
-    float *qs = att;           // [HD]
-    float *ps = qs + HD;       // [W]
-    float *op = ps + d.W;      // [G][HD]
-    const float scale = rsqrtf((float)HD);
+    const float *qs = att;           // [HD]
+    float *ps = att + HD;            // [W]
+    float *op = ps + d.W;            // [G][HD]
     const int t = threadIdx.x, sub = t % tpk, c = t % nkv, g = t / nkv;
     // A window that fits one pass (every key has its threads, every thread at most
-    // eight V rows) issues all of a head's loads - q, K and V - at once.
+    // eight V rows) issues all of its K and V loads at once.
     const bool one_pass = n <= kpp && n <= 8 * G;
-    for (int h = blockIdx.x; h < d.NH; h += gridDim.x) {
-        uint4 kq[8], vq[8];
-        const float qv = t < HD ? __ldcg(a.b.q + (size_t)h * HD + t) : 0.f;   // HD <= 256 < kCT
-        if (one_pass) {
-            const int j = t / tpk;
-            const uint4 *kr = reinterpret_cast<const uint4 *>(kw + (size_t)j * HD);
+    uint4 kq[8], vq[8];
+    if (one_pass) {
+        const int j = t / tpk;
+        const uint4 *kr = reinterpret_cast<const uint4 *>(kw + (size_t)j * HD);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int v = sub + tpk * u;
-                kq[u] = j < n && v < nkv ? __ldcg(kr + v) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int jv = g + k * G;
-                vq[k] = g < G && jv < n ? __ldcg(reinterpret_cast<const uint4 *>(vw + (size_t)jv * HD) + c)
-                                        : make_uint4(0, 0, 0, 0);
-            }
+        for (int u = 0; u < 8; ++u) {
+            const int v = sub + tpk * u;
+            kq[u] = j < n && v < nkv ? __ldcg(kr + v) : make_uint4(0, 0, 0, 0);
         }
-        if (t < HD) qs[t] = qv * scale;
-        csync();
-        float m = -INFINITY;
-        for (int j0 = 0; j0 < n; j0 += kpp) {
-            const int j = j0 + t / tpk;
-            float s = 0.f;
-            if (j < n) {
-                if (!one_pass) {
-                    const uint4 *kr = reinterpret_cast<const uint4 *>(kw + (size_t)j * HD);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int v = sub + tpk * u;
-                        kq[u] = v < nkv ? __ldcg(kr + v) : make_uint4(0, 0, 0, 0);
-                    }
-                }
+        for (int k = 0; k < 8; ++k) {
+            const int jv = g + k * G;
+            vq[k] = g < G && jv < n ? __ldcg(reinterpret_cast<const uint4 *>(vw + (size_t)jv * HD) + c)
+                                    : make_uint4(0, 0, 0, 0);
+        }
+    }
+    float m = -INFINITY;
+    for (int j0 = 0; j0 < n; j0 += kpp) {
+        const int j = j0 + t / tpk;
+        float s = 0.f;
+        if (j < n) {
+            if (!one_pass) {
+                const uint4 *kr = reinterpret_cast<const uint4 *>(kw + (size_t)j * HD);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int v = sub + tpk * u;
-                    if (v < nkv) s = dotv<TKV>(kq[u], qs + v * KVEC, s);
+                    kq[u] = v < nkv ? __ldcg(kr + v) : make_uint4(0, 0, 0, 0);
                 }
             }
-            for (int o = 1; o < tpk; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (j < n) {
-                if (sub == 0) ps[j] = s;
-                m = fmaxf(m, s);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = sub + tpk * u;
+                if (v < nkv) s = dotv<TKV>(kq[u], qs + v * KVEC, s);
             }
         }
-        m = cmax(m, red);
-        float sum = 0.f;
-        for (int j = t; j < n; j += kCT) {
-            const float e = __expf(ps[j] - m);
-            ps[j] = e;
-            sum += e;
+        for (int o = 1; o < tpk; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (j < n) {
+            if (sub == 0) ps[j] = s;
+            m = fmaxf(m, s);
         }
-        sum = csum(sum, red);
-        const float inv = 1.f / sum;
-        if (g < G) {
-            float acc[KVEC];
+    }
+    m = cmax(m, red);
+    float sum = 0.f;
+    for (int j = t; j < n; j += kCT) {
+        const float e = __expf(ps[j] - m);
+        ps[j] = e;
+        sum += e;
+    }
+    sum = csum(sum, red);
+    const float inv = 1.f / sum;
+    if (g < G) {
+        float acc[KVEC];
 #pragma unroll
-            for (int e = 0; e < KVEC; ++e) acc[e] = 0.f;
-            if (one_pass) {
+        for (int e = 0; e < KVEC; ++e) acc[e] = 0.f;
+        if (one_pass) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int jv = g + k * G;
-                    if (jv < n) {
-                        float vv[KVEC];
-                        unpack<TKV>(vq[k], vv);
-                        const float pj = ps[jv];
-#pragma unroll
-                        for (int e = 0; e < KVEC; ++e) acc[e] = fmaf(pj, vv[e], acc[e]);
-                    }
-                }
-            } else {
-                for (int j = g; j < n; j += G) {
+            for (int k = 0; k < 8; ++k) {
+                const int jv = g + k * G;
+                if (jv < n) {
                     float vv[KVEC];
-                    unpack<TKV>(__ldcg(reinterpret_cast<const uint4 *>(vw + (size_t)j * HD) + c), vv);
-                    const float pj = ps[j];
+                    unpack<TKV>(vq[k], vv);
+                    const float pj = ps[jv];
 #pragma unroll
                     for (int e = 0; e < KVEC; ++e) acc[e] = fmaf(pj, vv[e], acc[e]);
                 }
             }
+        } else {
+            for (int j = g; j < n; j += G) {
+                float vv[KVEC];
+                unpack<TKV>(__ldcg(reinterpret_cast<const uint4 *>(vw + (size_t)j * HD) + c), vv);
+                const float pj = ps[j];
 #pragma unroll
-            for (int e = 0; e < KVEC; ++e) op[g * HD + c * KVEC + e] = acc[e];
+                for (int e = 0; e < KVEC; ++e) acc[e] = fmaf(pj, vv[e], acc[e]);
+            }
         }
-        csync();
-        for (int i = t; i < HD; i += kCT) {
-            float acc = 0.f;
-            for (int gg = 0; gg < G; ++gg) acc += op[gg * HD + i];
-            a.b.o[(size_t)h * HD + i] = acc * inv;
-        }
-        csync();
+#pragma unroll
+        for (int e = 0; e < KVEC; ++e) op[g * HD + c * KVEC + e] = acc[e];
     }
+    csync();
+    for (int i = t; i < HD; i += kCT) {
+        float acc = 0.f;
+        for (int gg = 0; gg < G; ++gg) acc += op[gg * HD + i];
+        a.b.o[(size_t)h * HD + i] = acc * inv;
+    }
+    csync();
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -716,6 +726,17 @@ __device__ __forceinline__ void producer_warp(const PersistArgs &a, Shared &S, u
         }
         return true;
     };
+    // every chunk of one piece (a work list owned by this CTA alone)
+    auto stream_all = [&](const Piece &pc) -> bool {
+        for (int j = 0; j < chunks_of(pc); ++j) {
+            const int row0 = j * pc.rpc, nr = min(pc.rpc, pc.rows - row0);
+            const TW *src = static_cast<const TW *>(pc.base) + (size_t)row0 * pc.K;
+            if (!issue(src, (uint32_t)(nr * pc.K * sizeof(TW)), nullptr, 0, 20, pc.base,
+                       (size_t)pc.rows * pc.K * sizeof(TW)))
+                return false;
+        }
+        return true;
+    };
     // gate and up rows i of the shared expert (e < 0) or of expert e
     struct Experts {   // one layer's expert matrices (s: shared expert)
         const void *gate, *up, *down, *s_gate, *s_up, *s_down;
@@ -743,11 +764,10 @@ __device__ __forceinline__ void producer_warp(const PersistArgs &a, Shared &S, u
                 prefetch_l2(w.ffn_norm, H * 4);
             }
             const Piece P1[2] = {piece<TW>(w.wq_a, d.RQ, H), piece<TW>(w.wkv_a, d.RKV, H)};
-            const Piece P2[3] = {piece<TW>(w.wq_b, d.QD, d.RQ), piece<TW>(w.wk_b, d.HD, d.RKV),
-                                 piece<TW>(w.wv_b, d.HD, d.RKV)};
+            const int kind = qkv_kind(d.NH);
             const Piece P4[1] = {piece<TW>(w.wo, H, d.QD)};
             const Piece P5[1] = {piece<TW>(w.w_router, d.E, H)};
-            ok = stream(P1) && stream(P2) && stream(P4) && stream(P5);
+            ok = stream(P1) && (kind < 0 || stream_all(qkv_piece<TW>(w, d, kind))) && stream(P4) && stream(P5);
             for (int i = slo; ok && i < shi; ++i) ok = issue_gu(xp, -1, i);
         }
         // top-k once every CTA has written its router scores for this layer
@@ -832,7 +852,7 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
     float *xs = res_all + kNC * kMaxR;                                     // [vmax]
     float *sc = xs + vmax;                                                 // [E] producer's
     float *ybuf = sc + d.E;   // [(rows blocks per CTA + 1) * (K + 1) * RB] stage-7 results
-    float *att = xs;                                                       // stage 3 scratch
+    float *att = xs + d.RQ + d.RKV;   // stages 2-3: q, scores, partial outputs (after the latents)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // ========================= consumers =========================
     unsigned target = a.bar_base;   // grid-barrier arrivals expected so far
@@ -910,58 +930,94 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
         }
         if (!grid_sync(a, target, S)) return;
 
-        // ---- stage 2: [W_qb; W_kb; W_vb] + RoPE + KV append
+        // ---- stages 2-3: queries of one head + attention (head CTAs); K or V row (two CTAs)
         stamp(a, l * 7 + 1);
         {
-            cload<TW>(a.b.c, xs, d.RQ, d.RQ);
-            cload<TW>(a.b.c + d.RQ, xs + d.RQ, d.RKV, d.RKV);
-            csync();
-            const Piece P[3] = {piece<TW>(w.wq_b, d.QD, d.RQ), piece<TW>(w.wk_b, d.HD, d.RKV),
-                                piece<TW>(w.wv_b, d.HD, d.RKV)};
-            const float2 *rope = a.rope + (size_t)a.pos * (d.HD / 2);
-            int lo, hi;
-            cta_range(total_chunks(P), lo, hi);
-            const unsigned base = it;
-            it = base + (unsigned)(hi - lo);
-            for (int j = lo; j < hi; ++j) {
-                const unsigned idx = base + (unsigned)(j - lo);
-                if ((int)(idx % kNC) != warp) continue;
-                const Chunk c = locate(P, j);
-                const int Kp = P[c.piece].K;
-                const float *x = c.piece == 0 ? xs : xs + d.RQ;
-                if (!consume(idx,
-                             [&](const unsigned char *sl) {
-                                 warp_dots<TW>(reinterpret_cast<const TW *>(sl), c.nrows, Kp, x, res, lane);
-                             },
-                             [&]() {
-                                 for (int q = lane; q < c.nrows / 2; q += 32) {   // row pairs
-                                     const int row = c.row0 + 2 * q;
-                                     float e = res[2 * q], o = res[2 * q + 1];
-                                     if (c.piece < 2) {
-                                         const float2 cs = rope[(row % d.HD) / 2];
-                                         const float re = e * cs.x - o * cs.y, ro = e * cs.y + o * cs.x;
-                                         e = re;
-                                         o = ro;
+            const int kind = qkv_kind(d.NH);
+            float *qs = att;   // [HD] this head's queries after RoPE, times 1/sqrt(HD)
+            if (kind >= 0) {
+                if (kind == 0) cload<TW>(a.b.c, xs, d.RQ, d.RQ);
+                else cload<TW>(a.b.c + d.RQ, xs + d.RQ, d.RKV, d.RKV);
+                csync();
+                const Piece P = qkv_piece<TW>(w, d, kind);
+                const float *x = kind == 0 ? xs : xs + d.RQ;
+                const float2 *rope = a.rope + (size_t)a.pos * (d.HD / 2);
+                const float scale = rsqrtf((float)d.HD);
+                const int nch = chunks_of(P);
+                const unsigned base = it;
+                it = base + (unsigned)nch;
+                for (int j = 0; j < nch; ++j) {
+                    const unsigned idx = base + (unsigned)j;
+                    if ((int)(idx % kNC) != warp) continue;
+                    const int row0 = j * P.rpc, nr = min(P.rpc, P.rows - row0);
+                    if (!consume(idx,
+                                 [&](const unsigned char *sl) {
+                                     warp_dots<TW>(reinterpret_cast<const TW *>(sl), nr, P.K, x, res, lane);
+                                 },
+                                 [&]() {
+                                     for (int q = lane; q < nr / 2; q += 32) {   // row pairs
+                                         const int row = row0 + 2 * q;          // within the head
+                                         float e = res[2 * q], o = res[2 * q + 1];
+                                         if (kind < 2) {
+                                             const float2 cs = rope[row / 2];
+                                             const float re = e * cs.x - o * cs.y, ro = e * cs.y + o * cs.x;
+                                             e = re;
+                                             o = ro;
+                                         }
+                                         if (kind == 0) {
+                                             qs[row] = e * scale;
+                                             qs[row + 1] = o * scale;
+                                             a.b.q[(size_t)blockIdx.x * d.HD + row] = e;   // for inspection
+                                             a.b.q[(size_t)blockIdx.x * d.HD + row + 1] = o;
+                                         } else {
+                                             TKV *dst = (kind == 1 ? kc : vc) + (size_t)a.pos * d.HD;
+                                             dst[row] = from_f32<TKV>(e);
+                                             dst[row + 1] = from_f32<TKV>(o);
+                                         }
                                      }
-                                     if (c.piece == 0) {
-                                         a.b.q[row] = e;
-                                         a.b.q[row + 1] = o;
-                                     } else {
-                                         TKV *dst = (c.piece == 1 ? kc : vc) + (size_t)a.pos * d.HD;
-                                         dst[row] = from_f32<TKV>(e);
-                                         dst[row + 1] = from_f32<TKV>(o);
-                                     }
-                                 }
-                             }))
-                    return;
+                                 }))
+                        return;
+                }
+                csync();
+                if (kind > 0 && threadIdx.x == 0) {   // publish the new K or V row
+                    __threadfence();
+                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.bar + 1) : "memory");
+                }
+            }
+            stamp(a, l * 7 + 2);
+            if (threadIdx.x == 0) {
+                // HBM has little to do while the heads run: bring this CTA's W_o rows that
+                // the ring does not hold yet (those after its first kNSlot) into L2.  (A
+                // bulk prefetch of whole stages early in the layer was slower: it queued
+                // ahead of the stages' own latency-critical loads.)
+                const Piece P[1] = {piece<TW>(w.wo, H, d.QD)};
+                int lo, hi;
+                cta_range(total_chunks(P), lo, hi);
+                if (hi - lo > kNSlot) {
+                    const Chunk c0 = locate(P, lo + kNSlot), c1 = locate(P, hi - 1);
+                    prefetch_range(static_cast<const TW *>(w.wo) + (size_t)c0.row0 * d.QD,
+                                   (size_t)(c1.row0 + c1.nrows - c0.row0) * d.QD * sizeof(TW));
+                }
+            }
+            if (kind == 0) {
+                // wait for this position's K and V rows (two arrivals per layer)
+                if (threadIdx.x == 0) {
+                    const unsigned want = a.kv_base + 2u * (unsigned)(l + 1);
+                    const long long t0 = clock64();
+                    while ((int)(ld_acquire_gpu(a.bar + 1) - want) < 0) {
+                        if (clock64() - t0 > kWaitCycles) {
+                            atomicExch(a.status, DS4G_ETIMEOUT);
+                            S.abort_flag = 1;
+                            break;
+                        }
+                    }
+                }
+                csync();
+                if (*ab) return;
+                attention_head<TKV>(a, blockIdx.x, kc + (size_t)lo_w * d.HD, vc + (size_t)lo_w * d.HD,
+                                    a.pos - lo_w + 1, att, S.red);
             }
         }
-        if (!grid_sync(a, target, S)) return;
-
-        // ---- stage 3: sliding-window MQA, one head per CTA; K/V rows read from L2
-        stamp(a, l * 7 + 2);
-        attention_heads<TKV>(a, kc + (size_t)lo_w * d.HD, vc + (size_t)lo_w * d.HD, a.pos - lo_w + 1, att,
-                             S.red);
         if (!grid_sync(a, target, S)) return;
 
         // ---- stage 4: xm = x + W_o o
@@ -980,6 +1036,19 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
 
         // ---- stage 5: RMSNorm + router scores (xs keeps x * g; inv2 = 1/rms)
         stamp(a, l * 7 + 4);
+        if (threadIdx.x == 0) {   // likewise during the router: the shared expert's rows of
+                                  // stages 6 and 7 (the routed rows wait for the top-k)
+            int slo, shi;
+            cta_range(I, slo, shi);
+            if (shi > slo) {
+                prefetch_range(static_cast<const TW *>(w.ws_gate) + (size_t)slo * H, (size_t)(shi - slo) * H * sizeof(TW));
+                prefetch_range(static_cast<const TW *>(w.ws_up) + (size_t)slo * H, (size_t)(shi - slo) * H * sizeof(TW));
+            }
+            int lo, hi;
+            cta_range(nrb, lo, hi);
+            if (hi > lo)
+                prefetch_range(static_cast<const TW *>(w.ws_down) + (size_t)lo * RB * I, (size_t)(min(H, hi * RB) - lo * RB) * I * sizeof(TW));
+        }
         float inv2;
         {
             float ss = cload_g<TW>(a.b.xm, w.ffn_norm, xs, H);
@@ -1143,7 +1212,8 @@ size_t persistent_smem(const Dims &d)
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     const int ymax = ((nrb + std::max(nsm, 1) - 1) / std::max(nsm, 1) + 1) * (d.K + 1) * RB;
-    const size_t region = std::max((size_t)(vmax + d.E + ymax), (size_t)(d.HD + d.W + kCT * 8)) * 4;
+    const size_t region =
+        std::max((size_t)(vmax + d.E + ymax), (size_t)(d.RQ + d.RKV + d.HD + d.W + kCT * 8)) * 4;
     (void)kvs;
     return (size_t)kNSlot * kSlot + (size_t)kNC * kMaxR * 4 + region;
 }
@@ -1182,7 +1252,8 @@ cudaError_t persistent_setup(const Dims &d, int max_smem, int nsm, bool *ok)
     const bool rows_fit = (size_t)std::max(d.H, d.QD) * wsz <= kSlot && (size_t)d.I * wsz <= kSlot &&
                           2 * (size_t)d.H * wsz <= kSlot &&
                           2 * (size_t)std::max(d.RQ, d.RKV) * wsz <= kSlot;
-    *ok = coop && per_sm >= 1 && nsm > 0 && rows_fit;
+    // one CTA per head plus the K and V writers must exist
+    *ok = coop && per_sm >= 1 && nsm > 0 && rows_fit && d.NH + 2 <= nsm;
     return cudaSuccess;
 }
 
