@@ -255,7 +255,9 @@ template <typename TW> struct ShortRow { static constexpr int NU = 32 / VecOf<TW
 // by one warp; the warp-reduced result of row r goes to res[r] (lane 0).  Lane t
 // takes 16-byte vectors t, t+32, ...
 //  - Short rows (K/VEC <= 32*NU): the lane's x fragments are loaded once into
-//    registers and reused for every row, two rows at a time.
+//    registers and reused for every row, two rows at a time.  (A transposed
+//    butterfly that reduces eight rows at once is faster in isolation but made the
+//    whole decode step slower.)
 //  - Long rows: two rows share each x fragment load; four weight vectors per row
 //    are in flight and two accumulators alternate.
 // Not inlined: every stage runs the same copy, which stays in the instruction cache.
@@ -547,9 +549,9 @@ __device__ __noinline__ float cload_f16_g(const uint16_t *src, const float *g, f
 // `tpk` adjacent threads share a key, each holding up to eight 16-byte vectors of it
 // in flight.  Output: thread t accumulates vector t % nkv of V over the keys
 // j = g, g + G, ... (g = t / nkv), and the G partial sums are added in group order.
-template <typename TKV>
-__device__ __noinline__ void attention_head(const PersistArgs &a, int h, const TKV *kw, const TKV *vw, int n,
-                                            float *att, float *red)
+template <typename TKV, class KvWait>
+__device__ __forceinline__ bool attention_head(const PersistArgs &a, int h, const TKV *kw, const TKV *vw, int n,
+                                               float *att, float *red, KvWait &&kv_wait)
 {
     const Dims &d = a.d;
     constexpr int KVEC = VecOf<TKV>::n;
@@ -562,7 +564,9 @@ __device__ __noinline__ void attention_head(const PersistArgs &a, int h, const T
     float *op = ps + d.W;            // [G][HD]
     const int t = threadIdx.x, sub = t % tpk, c = t % nkv, g = t / nkv;
     // A window that fits one pass (every key has its threads, every thread at most
-    // eight V rows) issues all of its K and V loads at once.
+    // eight V rows) issues all of its K and V loads at once.  The rows before the
+    // current position are final: they are requested before waiting for the current
+    // K and V rows (published by other CTAs of this launch through the kv counter).
     const bool one_pass = n <= kpp && n <= 8 * G;
     uint4 kq[8], vq[8];
     if (one_pass) {
@@ -571,13 +575,31 @@ __device__ __noinline__ void attention_head(const PersistArgs &a, int h, const T
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int v = sub + tpk * u;
-            kq[u] = j < n && v < nkv ? __ldcg(kr + v) : make_uint4(0, 0, 0, 0);
+            kq[u] = j < n - 1 && v < nkv ? __ldcg(kr + v) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int jv = g + k * G;
-            vq[k] = g < G && jv < n ? __ldcg(reinterpret_cast<const uint4 *>(vw + (size_t)jv * HD) + c)
-                                    : make_uint4(0, 0, 0, 0);
+            vq[k] = g < G && jv < n - 1 ? __ldcg(reinterpret_cast<const uint4 *>(vw + (size_t)jv * HD) + c)
+                                        : make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (!kv_wait()) return false;
+    if (one_pass) {   // the current position's rows
+        const int j = t / tpk;
+        if (j == n - 1) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(kw + (size_t)j * HD);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = sub + tpk * u;
+                if (v < nkv) kq[u] = __ldcg(kr + v);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int jv = g + k * G;
+            if (g < G && jv == n - 1)
+                vq[k] = __ldcg(reinterpret_cast<const uint4 *>(vw + (size_t)jv * HD) + c);
         }
     }
     float m = -INFINITY;
@@ -649,6 +671,7 @@ __device__ __noinline__ void attention_head(const PersistArgs &a, int h, const T
         a.b.o[(size_t)h * HD + i] = acc * inv;
     }
     csync();
+    return true;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -1000,22 +1023,25 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                 }
             }
             if (kind == 0) {
-                // wait for this position's K and V rows (two arrivals per layer)
-                if (threadIdx.x == 0) {
-                    const unsigned want = a.kv_base + 2u * (unsigned)(l + 1);
-                    const long long t0 = clock64();
-                    while ((int)(ld_acquire_gpu(a.bar + 1) - want) < 0) {
-                        if (clock64() - t0 > kWaitCycles) {
-                            atomicExch(a.status, DS4G_ETIMEOUT);
-                            S.abort_flag = 1;
-                            break;
+                // waits for this position's K and V rows (two arrivals per layer)
+                auto kv_wait = [&]() -> bool {
+                    if (threadIdx.x == 0) {
+                        const unsigned want = a.kv_base + 2u * (unsigned)(l + 1);
+                        const long long t0 = clock64();
+                        while ((int)(ld_acquire_gpu(a.bar + 1) - want) < 0) {
+                            if (clock64() - t0 > kWaitCycles) {
+                                atomicExch(a.status, DS4G_ETIMEOUT);
+                                S.abort_flag = 1;
+                                break;
+                            }
                         }
                     }
-                }
-                csync();
-                if (*ab) return;
-                attention_head<TKV>(a, blockIdx.x, kc + (size_t)lo_w * d.HD, vc + (size_t)lo_w * d.HD,
-                                    a.pos - lo_w + 1, att, S.red);
+                    csync();
+                    return *ab == 0;
+                };
+                if (!attention_head<TKV>(a, blockIdx.x, kc + (size_t)lo_w * d.HD, vc + (size_t)lo_w * d.HD,
+                                         a.pos - lo_w + 1, att, S.red, kv_wait))
+                    return;
             }
         }
         if (!grid_sync(a, target, S)) return;
