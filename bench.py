@@ -253,12 +253,20 @@ def run_case(args):
         nt = PREFILL_TOKENS[args.case]
         s = pdl.Session(m, nt + 8)
         toks = synth.host_tokens(nt, shape.vocab, stream=41)
+        stream = torch.cuda.current_stream()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                torch.cuda.synchronize()
+                ev0.record(stream)
             assert s.truncate(0) == 0 and s.prefill(toks) == 0
+        ev1.record(stream)
         torch.cuda.synchronize()
         assert s.status() == 0
+        ms = ev0.elapsed_time(ev1) / max(1, args.steps)
         print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup,
-                          "launches": int(s.launches)}), flush=True)
+                          "launches": int(s.launches), "ms_per_prefill": ms,
+                          "tok_per_s": nt / ms * 1e3}), flush=True)
         return
     emb, lm, layers = tw.dev_model(shape)
     m = pdl.Model(shape, emb, lm, layers)

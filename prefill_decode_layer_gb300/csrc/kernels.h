@@ -42,6 +42,7 @@ struct PrefillBufs {
     int *cnt;         // [E] tokens per expert
     int *off;         // [E+1] start of each expert's rows in the grouped order
     int *rows;        // [P*K] grouped order: token * K + slot
+    int *segcnt;      // [ceil(P*K / kSortSeg)][E] per-segment expert counts, then bases
     int *tiles;       // [P*K/16 + E + 1] (expert, first row) work items; tiles[0] = count
     void *HG;         // [P*K][I] routed SwiGLU hidden, grouped order
     void *HS;         // [P][I] shared SwiGLU hidden
@@ -50,6 +51,12 @@ struct PrefillBufs {
     float *layer_x;   // [L+1][H]: residual of chunk row rec_row entering each layer, then final
     int rec_row;      // chunk row to record (-1: none)
 };
+// Entries per segment of the counting sort that groups (token, slot) entries by expert.
+static constexpr int kSortSeg = 512;
+static inline size_t sort_segments(size_t nent) { return (nent + kSortSeg - 1) / kSortSeg; }
+// Stable counting sort of pb.ids[0, nent) by expert into pb.rows, with the expert
+// offsets pb.off[E + 1], counts pb.cnt[E] and the tile list pb.tiles (bm rows a tile).
+cudaError_t group_by_expert(const PrefillBufs &pb, int nent, int E, int bm, cudaStream_t st);
 size_t prefill_bytes(const Dims &d, int P);
 void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb);
 cudaError_t prefill_setup(const Dims &d, int max_smem);

@@ -71,68 +71,149 @@ __global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E
     }
 }
 
-// Stable grouping of the (token, slot) entries by expert.  Pass 1: one CTA per
-// expert counts its entries.
-__global__ void __launch_bounds__(256) k_group_count(const int *ids, int nent, int *cnt)
+// Stable grouping of the (token, slot) entries by expert: a counting sort in three
+// passes over segments of kSortSeg entries.  Entry i = token * K + slot; an
+// expert's rows come out in increasing i, so the grouped order depends only on
+// the ids.  Pass 1: per-segment histograms (shared-memory atomics).
+__global__ void __launch_bounds__(256) k_group_hist(const int *ids, int nent, int E, int *segcnt)
 {
-    __shared__ int red[8];
-    const int e = blockIdx.x;
-    int c = 0;
-    for (int i = threadIdx.x; i < nent; i += blockDim.x) c += (ids[i] == e);
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+    extern __shared__ int hist[];
+    const int seg = blockIdx.x, i0 = seg * kSortSeg, i1 = min(nent, i0 + kSortSeg);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int t = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-        cnt[e] = t;
+    for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+        const int id = ids[i];
+        if ((unsigned)id < (unsigned)E) atomicAdd(&hist[id], 1);
     }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) segcnt[(size_t)seg * E + e] = hist[e];
 }
 
-// Pass 2 (one thread): expert offsets and the (expert, first row) tile list.
-__global__ void k_group_scan(const int *cnt, int E, int bm, int *off, int *tiles)
+// Exclusive scan over the block's threads (blockDim.x a multiple of 32, <= 1024).
+__device__ int block_exclusive_scan(int v, int *tmp, int &total)
 {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    int o = 0, nt = 0;
-    for (int e = 0; e < E; ++e) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) tmp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < nw) tmp[lane] = w;   // inclusive warp totals
+    }
+    __syncthreads();
+    total = tmp[nw - 1];
+    const int r = x - v + (warp ? tmp[warp - 1] : 0);
+    __syncthreads();   // tmp may be reused
+    return r;
+}
+
+// Pass 2 (one CTA): each expert's count and its segments' exclusive prefixes
+// (segcnt is rewritten in place), the expert offsets, and the (expert, first row)
+// tile list, tiles of bm rows that never cross an expert boundary.  Thread t owns
+// the experts [t * per, (t + 1) * per).
+__global__ void __launch_bounds__(1024) k_group_offsets(int *segcnt, int nseg, int E, int bm, int *cnt, int *off,
+                                                        int *tiles)
+{
+    __shared__ int tmp[32];
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+    int rows = 0, ntile = 0;
+    for (int e = e0; e < e1; ++e) {
+        int run = 0;
+        int s = 0;
+        for (; s + 8 <= nseg; s += 8) {   // eight independent loads in flight
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = segcnt[(size_t)(s + j) * E + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                segcnt[(size_t)(s + j) * E + e] = run;
+                run += c[j];
+            }
+        }
+        for (; s < nseg; ++s) {
+            const int c = segcnt[(size_t)s * E + e];
+            segcnt[(size_t)s * E + e] = run;
+            run += c;
+        }
+        cnt[e] = run;
+        rows += run;
+        ntile += (run + bm - 1) / bm;
+    }
+    int nrows, ntiles;
+    int o = block_exclusive_scan(rows, tmp, nrows);
+    int t = block_exclusive_scan(ntile, tmp, ntiles);
+    for (int e = e0; e < e1; ++e) {
+        const int c = cnt[e];
         off[e] = o;
-        for (int r = 0; r < cnt[e]; r += bm) {
-            tiles[1 + 2 * nt] = e;
-            tiles[2 + 2 * nt] = o + r;
-            ++nt;
+        for (int r = 0; r < c; r += bm, ++t) {
+            tiles[1 + 2 * t] = e;
+            tiles[2 + 2 * t] = o + r;
         }
-        o += cnt[e];
+        o += c;
     }
-    off[E] = o;
-    tiles[0] = nt;
+    if (threadIdx.x == 0) {
+        off[E] = nrows;
+        tiles[0] = ntiles;
+    }
 }
 
-// Pass 3: one CTA per expert writes its entries in index (token, slot) order.
-__global__ void __launch_bounds__(256) k_group_fill(const int *ids, int nent, const int *off,
-                                                    int *rows)
+// Pass 3: one warp per segment places its entries in index order.  Lanes holding
+// the same expert find one another with a match, rank by lane, and the group's
+// last lane advances the expert's running base.
+__global__ void __launch_bounds__(32) k_group_place(const int *ids, int nent, int E, const int *segcnt,
+                                                    const int *off, int *rows)
 {
-    __shared__ int wcount[8];
-    __shared__ int base;
-    const int e = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) base = off[e];
-    __syncthreads();
-    for (int i0 = 0; i0 < nent; i0 += blockDim.x) {
-        const int i = i0 + threadIdx.x;
-        const bool m = i < nent && ids[i] == e;
-        const unsigned bal = __ballot_sync(0xffffffffu, m);
-        if (lane == 0) wcount[warp] = __popc(bal);
-        __syncthreads();
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += wcount[w];
-        if (m) rows[base + before + __popc(bal & ((1u << lane) - 1u))] = i;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int t = 0;
-            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += wcount[w];
-            base += t;
+    extern __shared__ int base[];
+    const int seg = blockIdx.x, lane = threadIdx.x;
+    const int i0 = seg * kSortSeg, i1 = min(nent, i0 + kSortSeg);
+    for (int e = lane; e < E; e += 32) base[e] = off[e] + segcnt[(size_t)seg * E + e];
+    __syncwarp();
+    for (int c = i0; c < i1; c += 32) {
+        const int i = c + lane;
+        int id = i < i1 ? ids[i] : -1;
+        const bool ok = (unsigned)id < (unsigned)E;
+        if (!ok) id = -1 - lane;   // matches no other lane
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int b = 0;
+        if (ok) b = base[id];
+        __syncwarp();
+        if (ok) {
+            rows[b + rank] = i;
+            if (rank == __popc(peers) - 1) base[id] = b + rank + 1;
         }
-        __syncthreads();
+        __syncwarp();
     }
+}
+
+cudaError_t group_by_expert(const PrefillBufs &pb, int nent, int E, int bm, cudaStream_t st)
+{
+    const int nseg = (nent + kSortSeg - 1) / kSortSeg;
+    if (nseg == 0) {
+        cudaError_t e = cudaMemsetAsync(pb.tiles, 0, sizeof(int), st);
+        if (e) return e;
+        return cudaMemsetAsync(pb.off, 0, (size_t)(E + 1) * sizeof(int), st);
+    }
+    const size_t sh = (size_t)E * sizeof(int);
+    k_group_hist<<<nseg, 256, sh, st>>>(pb.ids, nent, E, pb.segcnt);
+    ++launch_count();
+    const int thr = E >= 1024 ? 1024 : ((E + 31) / 32) * 32;
+    k_group_offsets<<<1, thr, 0, st>>>(pb.segcnt, nseg, E, bm, pb.cnt, pb.off, pb.tiles);
+    ++launch_count();
+    k_group_place<<<nseg, 32, sh, st>>>(pb.ids, nent, E, pb.segcnt, pb.off, pb.rows);
+    ++launch_count();
+    return cudaGetLastError();
 }
 
 // Windowed causal multi-query attention for a chunk: CTA (token t, group of heads).
@@ -233,6 +314,7 @@ size_t prefill_bytes(const Dims &d, int P)
     b += 2 * align256(PK * 4);                           // ids, wts
     b += align256((size_t)d.E * 4) + align256((size_t)(d.E + 1) * 4);
     b += align256(PK * 4);                               // rows
+    b += align256(sort_segments(PK) * d.E * 4);          // segcnt
     b += align256((PK / 16 + d.E + 2) * 2 * 4);          // tiles
     b += align256(PK * d.I * ta);                        // HG
     b += align256((size_t)P * d.I * ta);                 // HS
@@ -260,6 +342,7 @@ void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb)
     pb.cnt = (int *)take((size_t)d.E * 4);
     pb.off = (int *)take((size_t)(d.E + 1) * 4);
     pb.rows = (int *)take(PK * 4);
+    pb.segcnt = (int *)take(sort_segments(PK) * d.E * 4);
     pb.tiles = (int *)take((PK / 16 + d.E + 2) * 2 * 4);
     pb.HG = take(PK * d.I * ta);
     pb.HS = take((size_t)P * d.I * ta);
@@ -339,13 +422,7 @@ static cudaError_t chunk_t(const Dims &d, const LayerPtrs *layers, void *const *
         if ((e = gemm_dense<float, TW>(pr, n, d.E, H, st, nsm))) return e;
         k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K, pb.status);
         ++launch_count();
-        k_group_count<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.cnt);
-        ++launch_count();
-        k_group_scan<<<1, 32, 0, st>>>(pb.cnt, d.E, kGroupBM, pb.off, pb.tiles);
-        ++launch_count();
-        k_group_fill<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.off, pb.rows);
-        ++launch_count();
-        if ((e = cudaGetLastError())) return e;
+        if ((e = group_by_expert(pb, nent, d.E, kGroupBM, st))) return e;
         const int max_tiles = nent / kGroupBM + d.E + 1;
         ProbGU<TA, TW, true> pg{XN, pb.rows, (const TW *)w.w_gate, (const TW *)w.w_up, HG, H,
                                 d.I, K, (size_t)d.I * H};

@@ -572,12 +572,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             return e;
         k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K, pb.status);
         ++launch_count();
-        k_group_count<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.cnt);
-        ++launch_count();
-        k_group_scan<<<1, 32, 0, st>>>(pb.cnt, d.E, tc::BN, pb.off, pb.tiles);
-        ++launch_count();
-        k_group_fill<<<d.E, 256, 0, st>>>(pb.ids, nent, pb.off, pb.rows);
-        ++launch_count();
+        if ((e = group_by_expert(pb, nent, d.E, tc::BN, st))) return e;
         k_gather_rows<<<nent, 256, 0, st>>>(ap.xn_hi, ap.xn_lo, pb.rows, K, nent, H, ap.xg_hi, ap.xg_lo);
         ++launch_count();
         if ((e = cudaGetLastError())) return e;

@@ -12,7 +12,9 @@
 // Orientation: the weight rows are the MMA's M side (128 rows per tile) and the
 // tokens its N side (128 per tile), so a tile of W is multiplied with the hi and
 // the lo tile of the same tokens: two MMAs per 16-wide K step into one FP32
-// accumulator in tensor memory (128 lanes x 128 columns).
+// accumulator in tensor memory (128 lanes x 128 columns).  A tile that owns fewer
+// than 128 token rows (an expert's last rows, a ragged chunk) runs its MMAs with N
+// = its rows rounded up to 16.
 //
 // Persistent: one CTA per SM walks the output tiles (weight-row block fastest, so
 // CTAs running together share a token tile in L2) with 192 threads:
@@ -206,11 +208,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
             unsigned it = 0, tc = 0;
             bool ok = true;
             for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x, ++tc) {
                 const int b = tc & 1;
+                // MMA N: the tile's token rows rounded up to 16 (a ragged or grouped
+                // tile skips the rows it does not own; their columns are never read)
+                int mb, e, r0, rend;
+                tile_of(tau, mb, e, r0, rend);
+                const int nn = min(BN, max(16, (rend - r0 + 15) & ~15));
+                const uint32_t idesc = idesc_bf16_f32(BM, nn);
                 if (!mbar_wait(&acce[b], ((tc >> 1) & 1) ^ 1, ab)) {
                     give_up();
                     break;
@@ -264,12 +271,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // gate and up of feature f = this thread's lane, 32 tokens at a time
                 const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN);
                 const int i = mb * BM + 32 * q + lane;
+                const int last = max(0, ((rend - r0 - 1) >> 5) << 5);   // first column of the last chunk read
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
+                for (int c0 = 0; c0 <= last; c0 += 32) {
                     float g[32], u[32];
                     tmem_ld32(lane_base + (uint32_t)c0, g);
                     tmem_ld32(lane_base + (uint32_t)(BN + c0), u);
-                    if (c0 == BN - 32) {   // the accumulators are drained
+                    if (c0 == last) {   // the accumulators are drained
                         tc_fence_before();
                         mbar_arrive(&acce[b]);
                     }
