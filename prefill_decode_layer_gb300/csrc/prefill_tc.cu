@@ -398,15 +398,32 @@ struct EpiRoutedRows {   // routed expert output of grouped row m into its (toke
     }
 };
 
-struct EpiSwiGLU {   // h[m][i] = silu(gate) * up as hi/lo BF16
+__device__ __forceinline__ uint32_t pack_bf16x2(bf16 a, bf16 b)
+{
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
+struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16, 16-byte stores
     bf16 *hi, *lo;
     int ld;
-    __device__ void store_h(int m, int i, float h, int) const
+    __device__ void store_row(int m, int i0, const float (&h)[32], int) const
     {
-        bf16 hv, lv;
-        split_hilo(h, hv, lv);
-        hi[(size_t)m * ld + i] = hv;
-        lo[(size_t)m * ld + i] = lv;
+        uint4 *ph = reinterpret_cast<uint4 *>(hi + (size_t)m * ld + i0);
+        uint4 *pl = reinterpret_cast<uint4 *>(lo + (size_t)m * ld + i0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                bf16 h0, l0, h1, l1;
+                split_hilo(h[8 * v + 2 * j], h0, l0);
+                split_hilo(h[8 * v + 2 * j + 1], h1, l1);
+                wh[j] = pack_bf16x2(h0, h1);
+                wl[j] = pack_bf16x2(l0, l1);
+            }
+            ph[v] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            pl[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
     }
 };
 
@@ -491,18 +508,18 @@ cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m)
     const TcActPtrs a = tc_act_ptrs(d, pb);
     const int P = pb.P, PK = pb.P * d.K, RC = d.RQ + d.RKV;
     cudaError_t e;
-    if ((e = make_map_bf16(&m.xn_hi, a.xn_hi, P, d.H, d.H, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.xn_lo, a.xn_lo, P, d.H, d.H, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.c_hi, a.c_hi, P, RC, RC, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.c_lo, a.c_lo, P, RC, RC, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.o_hi, a.o_hi, P, d.QD, d.QD, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.o_lo, a.o_lo, P, d.QD, d.QD, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.xg_hi, a.xg_hi, PK, d.H, d.H, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.xg_lo, a.xg_lo, PK, d.H, d.H, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.hg_hi, a.hg_hi, PK, d.I, d.I, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.hg_lo, a.hg_lo, PK, d.I, d.I, tc::BN))) return e;
-    if ((e = make_map_bf16(&m.hs_hi, a.hs_hi, P, d.I, d.I, tc::BN))) return e;
-    return make_map_bf16(&m.hs_lo, a.hs_lo, P, d.I, d.I, tc::BN);
+    if ((e = make_map_bf16(&m.xn_hi, a.xn_hi, P, d.H, d.H, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.xn_lo, a.xn_lo, P, d.H, d.H, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.c_hi, a.c_hi, P, RC, RC, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.c_lo, a.c_lo, P, RC, RC, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.o_hi, a.o_hi, P, d.QD, d.QD, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.o_lo, a.o_lo, P, d.QD, d.QD, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.xg_hi, a.xg_hi, PK, d.H, d.H, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.xg_lo, a.xg_lo, PK, d.H, d.H, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.hg_hi, a.hg_hi, PK, d.I, d.I, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.hg_lo, a.hg_lo, PK, d.I, d.I, tc::BT))) return e;
+    if ((e = make_map_bf16(&m.hs_hi, a.hs_hi, P, d.I, d.I, tc::BT))) return e;
+    return make_map_bf16(&m.hs_lo, a.hs_lo, P, d.I, d.I, tc::BT);
 }
 
 // ------------------------------------------------------------------ one chunk
@@ -516,8 +533,8 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
     cudaError_t e;
     const int H = d.H, K = d.K, nent = n * K, I = d.I;
     const TcActPtrs ap = tc_act_ptrs(d, pb);
-    const int ny = (n + tc::BN - 1) / tc::BN;
-    const int max_tiles = nent / tc::BN + d.E + 1;
+    const int ny = (n + tc::BT - 1) / tc::BT;
+    const int max_tiles = nent / tc::BT + d.E + 1;
     k_embed_rows<<<n, 256, 0, st>>>(tok_embd, pb.tok, pb.X, H);
     ++launch_count();
     if ((e = cudaGetLastError())) return e;
@@ -538,15 +555,15 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         ++launch_count();
         a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ, a.x_col0 = 0;
         if ((e = tc::launch<false>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a, EpiHiLo{ap.c_hi, ap.c_lo, d.RQ + d.RKV},
-                                   (d.RQ + d.RKV) / tc::BM, ny, nsm, st)))
+                                   ny, nsm, st)))
             return e;
         a.n_out = d.QD, a.k = d.RQ, a.piece_rows = 0, a.x_col0 = 0;
         if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a, EpiQRope{(float *)pb.Q, rope, d.QD, d.HD, p0},
-                                   d.QD / tc::BM, ny, nsm, st)))
+                                   ny, nsm, st)))
             return e;
         a.n_out = 2 * d.HD, a.k = d.RKV, a.piece_rows = d.HD, a.x_col0 = d.RQ;
-        if ((e = tc::launch<false>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, EpiKVRope<TKV>{kc, vc, rope, d.HD, p0},
-                                   2 * d.HD / tc::BM, ny, nsm, st)))
+        if ((e = tc::launch<false>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, EpiKVRope<TKV>{kc, vc, rope, d.HD, p0}, ny,
+                                   nsm, st)))
             return e;
         if constexpr (std::is_same<TKV, bf16>::value) {
             if (attn_mma_eligible(d)) {
@@ -561,18 +578,17 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             return e;
         }
         a.n_out = H, a.k = d.QD, a.piece_rows = 0, a.x_col0 = 0;
-        if ((e = tc::launch<false>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, H / tc::BM, ny, nsm, st)))
+        if ((e = tc::launch<false>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
         // ---- MoE half
         k_rmsnorm_hilo<<<n, rmsnorm_threads(H), 0, st>>>(pb.X, w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
         ++launch_count();
         a.n_out = d.E, a.k = H;
-        if ((e = tc::launch<false>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, d.E / tc::BM, ny, nsm,
-                                   st)))
+        if ((e = tc::launch<false>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, ny, nsm, st)))
             return e;
         k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K, pb.status);
         ++launch_count();
-        if ((e = group_by_expert(pb, nent, d.E, tc::BN, st))) return e;
+        if ((e = group_by_expert(pb, nent, d.E, tc::BT, st))) return e;
         k_gather_rows<<<nent, 256, 0, st>>>(ap.xn_hi, ap.xn_lo, pb.rows, K, nent, H, ap.xg_hi, ap.xg_lo);
         ++launch_count();
         if ((e = cudaGetLastError())) return e;
@@ -580,21 +596,21 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         tc::Args g{};
         g.status = pb.status;
         g.n_out = I, g.k = H, g.tiles = pb.tiles, g.off = pb.off;
-        if ((e = tc::launch<true>(m.wg, m.wu, am.xg_hi, am.xg_lo, g, EpiSwiGLU{ap.hg_hi, ap.hg_lo, I},
-                                  I / tc::BM, max_tiles, nsm, st)))
+        if ((e = tc::launch<true>(m.wg, m.wu, am.xg_hi, am.xg_lo, g, EpiSwiGLU{ap.hg_hi, ap.hg_lo, I}, max_tiles,
+                                  nsm, st)))
             return e;
         a.n_out = I, a.k = H;
-        if ((e = tc::launch<true>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, ap.hs_lo, I},
-                                  I / tc::BM, ny, nsm, st)))
+        if ((e = tc::launch<true>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, ap.hs_lo, I}, ny, nsm,
+                                  st)))
             return e;
         // routed down (grouped) into per-(token, slot) rows; the shared expert's down
         // projection into the residual; then the weighted routed rows, slot order
         g.n_out = H, g.k = I;
-        if ((e = tc::launch<false>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H},
-                                   H / tc::BM, max_tiles, nsm, st)))
+        if ((e = tc::launch<false>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H}, max_tiles,
+                                   nsm, st)))
             return e;
         a.n_out = H, a.k = I;
-        if ((e = tc::launch<false>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, H / tc::BM, ny, nsm, st)))
+        if ((e = tc::launch<false>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
         k_moe_combine<<<n, 256, 0, st>>>(pb.X, pb.YS, pb.wts, H, K);
         ++launch_count();

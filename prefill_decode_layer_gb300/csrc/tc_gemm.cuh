@@ -1,6 +1,6 @@
 // Tensor-core GEMM for the layer-major prefill (sm_103a, tcgen05 + TMA).
 //
-//   out[token][n] = sum_k W[n][k] * (Xhi[token][k] + Xlo[token][k])
+//   out[token][n] = sum_k (Xhi[token][k] + Xlo[token][k]) * W[n][k]
 //
 // W is a BF16 weight matrix ([out][in], K contiguous).  The activations are
 // carried as two BF16 arrays: hi = bf16(x) and lo = bf16(x - hi), so that every
@@ -9,31 +9,34 @@
 // per layer, which flips router top-6 decisions (the 6th-to-7th score gaps are
 // small); the split keeps the decisions of an FP32 computation.
 //
-// Orientation: the weight rows are the MMA's M side (128 rows per tile) and the
-// tokens its N side (128 per tile), so a tile of W is multiplied with the hi and
-// the lo tile of the same tokens: two MMAs per 16-wide K step into one FP32
-// accumulator in tensor memory (128 lanes x 128 columns).  A tile that owns fewer
-// than 128 token rows (an expert's last rows, a ragged chunk) runs its MMAs with N
-// = its rows rounded up to 16.
+// Orientation: 128 tokens are the MMA's M side and WN weight rows (256, or 128 for
+// GEMMs with few output tiles) its N side.  Per 16-wide K step the hi and the lo
+// token tile are each multiplied with the same weight tile into one FP32
+// accumulator in tensor memory (128 lanes = tokens, WN columns = features).  With
+// the weights on the wide side, every byte the tensor core reads from shared
+// memory feeds twice the products of a 128 x 128 tile, which is what bounds these
+// GEMMs (shared-memory bandwidth), not the tensor pipe.
 //
-// Persistent: one CTA per SM walks the output tiles (weight-row block fastest, so
-// CTAs running together share a token tile in L2) with 192 threads:
-//   warp 0 lane 0   TMA producer: per 64-wide K stage, the W tile (16 KB) and the
-//                   hi and lo token tiles (16 KB each), 128-byte swizzled, into a
-//                   4-stage shared-memory ring (full / empty mbarriers) that runs
-//                   on across tile boundaries;
-//   warp 1          allocates two accumulators in TMEM (2 x 128 columns); lane 0
+// Persistent: one CTA per SM walks the output tiles (weight block fastest, so CTAs
+// running together share a token tile in L2) with 192 threads:
+//   warp 0 lane 0   TMA producer: per 64-wide K stage, the weight tile (WN rows, as
+//                   128-row boxes) and the hi and lo token tiles (16 KB each),
+//                   128-byte swizzled, into a shared-memory ring (full / empty
+//                   mbarriers) that runs on across tile boundaries;
+//   warp 1          allocates two accumulators in TMEM (2 x WN columns); lane 0
 //                   issues the MMAs of tile i into accumulator i % 2 as soon as the
 //                   epilogue has drained it, and commits each stage back to the
 //                   producer and each tile to the epilogue;
-//   warps 2-5       epilogue, overlapping the next tile's MMAs: TMEM -> registers ->
-//                   a [token][feature] FP32 half tile in shared memory -> the
-//                   problem's functor, four adjacent features at a time, so RoPE
-//                   pairs are local to one call; a functor's global loads (load4)
-//                   are issued eight at a time before the matching stores.
-// Gate/up tiles (GU) hold 128 gate rows and the same 128 up rows in two
-// accumulators that share each token tile; SwiGLU is applied straight from the
-// two accumulators (a feature's gate and up sit in the same TMEM lane).
+//   warps 2-5       epilogue, overlapping the next tile's MMAs.  Warp q reads TMEM
+//                   lanes 32q.. (its 32 tokens), 32 features at a time, stages them
+//                   as [token][feature] rows in shared memory and hands the
+//                   problem's functor four adjacent features of one token at a
+//                   time (so RoPE pairs are local to one call); a functor's global
+//                   loads (load4) are issued eight at a time before the stores.
+// Gate/up tiles (GU): the weight tile is 128 gate rows followed by the same 128 up
+// rows, so a feature's gate and up sit in the same TMEM lane, 128 columns apart;
+// SwiGLU is applied straight from the accumulator and each thread writes 32
+// adjacent outputs of its token.
 // Every wait is bounded; a CTA that gives up raises DS4G_ETIMEOUT in *status, lets
 // its MMAs and copies finish, frees its TMEM and returns.
 #pragma once
@@ -46,40 +49,39 @@
 namespace ds4g {
 namespace tc {
 
-static constexpr int BM = 128;      // weight rows per accumulator (MMA M)
-static constexpr int BN = 128;      // tokens per tile (MMA N)
+static constexpr int BT = 128;      // tokens per tile (MMA M)
 static constexpr int BK = 64;       // K per stage: one 128-byte swizzle row of BF16
+static constexpr int BOXW = 128;    // weight rows per TMA box
 static constexpr int THREADS = 192;
-static constexpr uint32_t TILE_A = BM * BK * 2;              // 16 KB
-static constexpr uint32_t TILE_B = BN * BK * 2;              // 16 KB
-static constexpr int HALF = BN / 2;                          // tokens staged at once
-static constexpr int EPI_PITCH = BM + 4;                     // floats per staged token row
-static constexpr uint32_t EPI_BYTES = HALF * EPI_PITCH * 4;  // 33 KB
+static constexpr uint32_t TILE_X = BT * BK * 2;              // 16 KB
+static constexpr uint32_t BOX_BYTES = BOXW * BK * 2;         // 16 KB
+static constexpr int CH = 32;                                // features per epilogue chunk
+static constexpr int EPI_PITCH = CH + 4;                     // floats per staged token row
+static constexpr uint32_t EPI_BYTES = BT * EPI_PITCH * 4;    // 18 KB
 static constexpr int EPI_BATCH = 8;                          // functor loads in flight
 
-// Tile geometry.  Plain: 128 weight rows, one accumulator, 4 stages of 48 KB and a
-// staged epilogue.  Gate/up (GU): 128 gate rows and the same 128 up rows, two
-// accumulators sharing every token tile (the activations are read half as often),
-// 3 stages of 64 KB, and SwiGLU straight from the two accumulators.
-template <bool GU> struct Geo {
-    static constexpr int NACC = GU ? 2 : 1;
-    static constexpr uint32_t XOFF = NACC * TILE_A;          // token tiles after the W tiles
-    static constexpr uint32_t STAGE = XOFF + 2 * TILE_B;
-    static constexpr int STAGES = GU ? 3 : 4;
-    static constexpr uint32_t TMEM_COLS = 2 * NACC * BN;     // two tiles in flight
+// Tile geometry.  WN weight rows per tile: 256 -> 3 stages of 64 KB, 128 -> 4
+// stages of 48 KB; plain tiles add the epilogue's staging rows.
+template <bool GU, int WN> struct Geo {
+    static_assert(WN == 128 || WN == 256, "weight tile width");
+    static_assert(!GU || WN == 256, "gate/up tiles hold 128 gate + 128 up rows");
+    static constexpr uint32_t TILE_W = WN * BK * 2;
+    static constexpr uint32_t STAGE = TILE_W + 2 * TILE_X;   // W, X hi, X lo
+    static constexpr int STAGES = WN == 256 ? 3 : 4;
+    static constexpr uint32_t TMEM_COLS = 2 * WN;           // two tiles in flight
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (GU ? 0 : EPI_BYTES) + 256;
 };
 
-// What a launch computes.  Dense: token rows [0, m_tok) in tiles of BN.  Grouped
+// What a launch computes.  Dense: token rows [0, m_tok) in tiles of BT.  Grouped
 // (tiles != nullptr): token tile j is (expert e, first grouped row r0) from the
 // tile list, rows [r0, off[e+1]) of the grouped activations, and expert e's weight
-// rows start at e * n_out.  Weight-row blocks: n_out / BM (for GU, n_out is the
-// number of gate rows = up rows).
+// rows start at e * n_out.  Weight blocks: ceil(n_out / WN); for GU, n_out is the
+// number of gate rows (= up rows) and a block is 128 features.
 struct Args {
     int n_out;        // weight rows (per expert when grouped)
     int k;            // reduction length, a multiple of BK
     int x_col0;       // first activation column read (a multiple of 8)
-    int piece_rows;   // dense: rows of map w0 before map w1 starts (0: w0 only)
+    int piece_rows;   // dense: rows of map w0 before map w1 starts (0: w0 only); a multiple of 128
     int m_tok;        // dense: token rows
     const int *tiles; // grouped: [0] = count, then (expert, first row) pairs
     const int *off;   // grouped: expert row offsets [E + 1]
@@ -89,20 +91,21 @@ struct Args {
 struct NoAux {};
 
 // GU: the tile's gate rows come from w0 and its up rows from w1 (same row index);
-// the epilogue calls Epi::store_h(m, i, silu(gate) * up, e) per element.
-// Otherwise Epi provides  Aux load4(m, n, e)  and  store4(m, n, v[4], aux, e).
-template <class Epi, bool GU>
+// the epilogue calls Epi::store_row(m, i0, h[32], e) with h = silu(gate) * up of
+// features i0 .. i0 + 31 of token m.  Otherwise Epi provides  Aux load4(m, n, e)
+// and  store4(m, n, v[4], aux, e).
+template <class Epi, bool GU, int WN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
               const __grid_constant__ CUtensorMap xhi, const __grid_constant__ CUtensorMap xlo,
               const Args a, const Epi epi)
 {
-    using G = Geo<GU>;
+    using G = Geo<GU, WN>;
     constexpr int STAGES = G::STAGES;
     constexpr uint32_t STAGE_BYTES = G::STAGE;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // [HALF][EPI_PITCH] (plain)
+    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // [BT][EPI_PITCH] (plain)
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + (GU ? 0 : EPI_BYTES));
     uint64_t *empty = full + STAGES;
     uint64_t *accf = empty + STAGES;   // [2] accumulator ready (MMA commit)
@@ -112,8 +115,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int mtiles = a.n_out / BM;
-    const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BN - 1) / BN;
+    const int mtiles = GU ? a.n_out / BOXW : (a.n_out + WN - 1) / WN;
+    const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BT - 1) / BT;
     const int total = mtiles * ntiles;
     const int nk = a.k / BK;
     // tile -> (weight block mb, expert e, first token row r0, end row)
@@ -123,11 +126,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (a.tiles) {
             e = a.tiles[1 + 2 * j];
             r0 = a.tiles[2 + 2 * j];
-            rend = min(r0 + BN, a.off[e + 1]);
+            rend = min(r0 + BT, a.off[e + 1]);
         } else {
             e = 0;
-            r0 = j * BN;
-            rend = min(r0 + BN, a.m_tok);
+            r0 = j * BT;
+            rend = min(r0 + BT, a.m_tok);
         }
     };
 
@@ -167,15 +170,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
                 int mb, e, r0, rend;
                 tile_of(tau, mb, e, r0, rend);
-                const void *wm = &w0;
-                int wrow;
-                if (GU) {
-                    wrow = e * a.n_out + mb * BM;
-                } else if (a.piece_rows > 0 && mb * BM >= a.piece_rows) {
-                    wm = &w1;
-                    wrow = mb * BM - a.piece_rows;
-                } else {
-                    wrow = e * a.n_out + mb * BM;
+                // the tile's weight boxes: (map, first row) of each 128-row box
+                const void *bm[WN / BOXW];
+                int brow[WN / BOXW];
+#pragma unroll
+                for (int h = 0; h < WN / BOXW; ++h) {
+                    if (GU) {
+                        bm[h] = h ? &w1 : &w0;
+                        brow[h] = e * a.n_out + mb * BOXW;
+                    } else {
+                        int row = mb * WN + h * BOXW;
+                        if (row >= a.n_out) row = mb * WN;   // ragged last block: its features are skipped
+                        if (a.piece_rows > 0 && row >= a.piece_rows) {
+                            bm[h] = &w1;
+                            brow[h] = row - a.piece_rows;
+                        } else {
+                            bm[h] = &w0;
+                            brow[h] = e * a.n_out + row;
+                        }
+                    }
                 }
                 for (int i = 0; i < nk; ++i, ++it) {
                     const int s = it % STAGES;
@@ -187,14 +200,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     unsigned char *st = sm + s * STAGE_BYTES;
                     mbar_expect_tx(&full[s], STAGE_BYTES);
                     const int kx = i * BK;
-                    if (GU) {
-                        tma_load_2d(st, &w0, kx, wrow, &full[s]);
-                        tma_load_2d(st + TILE_A, &w1, kx, wrow, &full[s]);
-                    } else {
-                        tma_load_2d(st, wm, kx, wrow, &full[s]);
-                    }
-                    tma_load_2d(st + G::XOFF, &xhi, a.x_col0 + kx, r0, &full[s]);
-                    tma_load_2d(st + G::XOFF + TILE_B, &xlo, a.x_col0 + kx, r0, &full[s]);
+#pragma unroll
+                    for (int h = 0; h < WN / BOXW; ++h) tma_load_2d(st + h * BOX_BYTES, bm[h], kx, brow[h], &full[s]);
+                    tma_load_2d(st + G::TILE_W, &xhi, a.x_col0 + kx, r0, &full[s]);
+                    tma_load_2d(st + G::TILE_W + TILE_X, &xlo, a.x_col0 + kx, r0, &full[s]);
                 }
             }
             // no copy may still be in flight when the CTA exits
@@ -208,22 +217,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(BT, WN);
             unsigned it = 0, tc = 0;
             bool ok = true;
             for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x, ++tc) {
                 const int b = tc & 1;
-                // MMA N: the tile's token rows rounded up to 16 (a ragged or grouped
-                // tile skips the rows it does not own; their columns are never read)
-                int mb, e, r0, rend;
-                tile_of(tau, mb, e, r0, rend);
-                const int nn = min(BN, max(16, (rend - r0 + 15) & ~15));
-                const uint32_t idesc = idesc_bf16_f32(BM, nn);
                 if (!mbar_wait(&acce[b], ((tc >> 1) & 1) ^ 1, ab)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)(b * G::NACC * BN);
+                const uint32_t acc = tmem + (uint32_t)(b * WN);
                 for (int i = 0; i < nk; ++i, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(&full[s], (it / STAGES) & 1, ab)) {
@@ -235,14 +239,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sa = smem_u32(sm + s * STAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t bh = sdesc_kmajor_sw128(sa + G::XOFF + kk * 32);
-                        const uint64_t bl = sdesc_kmajor_sw128(sa + G::XOFF + TILE_B + kk * 32);
-#pragma unroll
-                        for (int r = 0; r < G::NACC; ++r) {   // gate (and up) accumulators
-                            const uint64_t ad = sdesc_kmajor_sw128(sa + r * TILE_A + kk * 32);
-                            tc_mma_bf16(acc + r * BN, ad, bh, idesc, (i | kk) != 0);
-                            tc_mma_bf16(acc + r * BN, ad, bl, idesc, 1u);
-                        }
+                        const uint64_t wd = sdesc_kmajor_sw128(sa + kk * 32);
+                        const uint64_t xh = sdesc_kmajor_sw128(sa + G::TILE_W + kk * 32);
+                        const uint64_t xl = sdesc_kmajor_sw128(sa + G::TILE_W + TILE_X + kk * 32);
+                        tc_mma_bf16(acc, xh, wd, idesc, (i | kk) != 0);
+                        tc_mma_bf16(acc, xl, wd, idesc, 1u);
                     }
                     tc_commit(&empty[s]);   // the stage is free once these MMAs complete
                 }
@@ -255,8 +256,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ---------------- epilogue (warps 2-5)
-        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int q = warp & 3;            // TMEM lane quarter this warp may access: tokens 32q ..
         const int et = threadIdx.x - 64;   // 0..127
+        const int tok = 32 * q + lane;     // this thread's token row in the tile
         unsigned tc = 0;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
             int mb, e, r0, rend;
@@ -267,67 +269,67 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
+            const bool wlive = r0 + 32 * q < rend;   // warp-uniform: any token of this warp in the tile
+            const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * WN);
             if constexpr (GU) {
-                // gate and up of feature f = this thread's lane, 32 tokens at a time
-                const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN);
-                const int i = mb * BM + 32 * q + lane;
-                const int last = max(0, ((rend - r0 - 1) >> 5) << 5);   // first column of the last chunk read
+                // gate columns c, up columns 128 + c of this thread's token
+                const int m = r0 + tok;
 #pragma unroll 1
-                for (int c0 = 0; c0 <= last; c0 += 32) {
+                for (int c0 = 0; c0 < BOXW; c0 += 32) {
                     float g[32], u[32];
-                    tmem_ld32(lane_base + (uint32_t)c0, g);
-                    tmem_ld32(lane_base + (uint32_t)(BN + c0), u);
-                    if (c0 == last) {   // the accumulators are drained
+                    if (wlive) {
+                        tmem_ld32(lane_base + (uint32_t)c0, g);
+                        tmem_ld32(lane_base + (uint32_t)(BOXW + c0), u);
+                    }
+                    if (c0 == BOXW - 32) {   // the accumulator is drained
                         tc_fence_before();
                         mbar_arrive(&acce[b]);
                     }
+                    if (wlive && m < rend) {
+                        float h[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {   // static indices keep g, u in registers
-                        const int m = r0 + c0 + j;
-                        if (m < rend) epi.store_h(m, i, silu_mul(g[j], u[j]), e);
+                        for (int j = 0; j < 32; ++j) h[j] = silu_mul(g[j], u[j]);
+                        epi.store_row(m, mb * BOXW + c0, h, e);
                     }
                 }
             } else {
-            for (int h = 0; h < 2; ++h) {
-                // accumulator columns (tokens) h*HALF .. +HALF-1 into stg[token][feature]
 #pragma unroll 1
-                for (int c0 = 0; c0 < HALF; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + h * HALF + c0), v);
-                    const int f = 32 * q + lane;
+                for (int c = 0; c < WN / CH; ++c) {
+                    // 32 features of this thread's token -> stg[tok][0 .. 31]
+                    if (wlive) {
+                        float v[32];
+                        tmem_ld32(lane_base + (uint32_t)(c * CH), v);
+                        float4 *row = reinterpret_cast<float4 *>(stg + tok * EPI_PITCH);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) stg[(c0 + j) * EPI_PITCH + f] = v[j];
-                }
-                if (h == 1) {   // the accumulator is drained: the next tile may use it
-                    tc_fence_before();
-                    mbar_arrive(&acce[b]);
-                }
-                asm volatile("bar.sync 2, 128;" ::: "memory");
-                const int tbase = r0 + h * HALF;
-                {
-                    constexpr int NI = HALF * (BM / 4) / 128;   // items per thread (16)
-#pragma unroll 1
-                    for (int i0 = 0; i0 < NI; i0 += EPI_BATCH) {
-                        typename Epi::Aux aux[EPI_BATCH];
-#pragma unroll
-                        for (int u = 0; u < EPI_BATCH; ++u) {
-                            const int idx = et + 128 * (i0 + u);
-                            const int t = idx / (BM / 4), j = (idx % (BM / 4)) * 4;
-                            if (tbase + t < rend) aux[u] = epi.load4(tbase + t, mb * BM + j, e);
-                        }
-#pragma unroll
-                        for (int u = 0; u < EPI_BATCH; ++u) {
-                            const int idx = et + 128 * (i0 + u);
-                            const int t = idx / (BM / 4), j = (idx % (BM / 4)) * 4;
-                            if (tbase + t >= rend) continue;
-                            const float4 v4 = *reinterpret_cast<const float4 *>(stg + t * EPI_PITCH + j);
-                            const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-                            epi.store4(tbase + t, mb * BM + j, v, aux[u], e);
-                        }
+                        for (int j = 0; j < CH / 4; ++j)
+                            row[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
+                    if (c == WN / CH - 1) {   // the accumulator is drained: the next tile may use it
+                        tc_fence_before();
+                        mbar_arrive(&acce[b]);
+                    }
+                    asm volatile("bar.sync 2, 128;" ::: "memory");
+                    // (token, 4 features) items: a warp covers 4 tokens x 32 features
+                    static_assert(BT * (CH / 4) == 128 * EPI_BATCH, "one batch of items per chunk");
+                    const int f0 = mb * WN + c * CH;
+                    typename Epi::Aux aux[EPI_BATCH];
+#pragma unroll
+                    for (int u = 0; u < EPI_BATCH; ++u) {
+                        const int idx = et + 128 * u;
+                        const int t = idx >> 3, j = (idx & 7) * 4;
+                        if (r0 + t < rend && f0 + j < a.n_out) aux[u] = epi.load4(r0 + t, f0 + j, e);
+                    }
+#pragma unroll
+                    for (int u = 0; u < EPI_BATCH; ++u) {
+                        const int idx = et + 128 * u;
+                        const int t = idx >> 3, j = (idx & 7) * 4;
+                        if (r0 + t >= rend || f0 + j >= a.n_out) continue;
+                        const float4 v4 = *reinterpret_cast<const float4 *>(stg + t * EPI_PITCH + j);
+                        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+                        epi.store4(r0 + t, f0 + j, v, aux[u], e);
+                    }
+                    asm volatile("bar.sync 2, 128;" ::: "memory");   // stg is rewritten next
                 }
-                asm volatile("bar.sync 2, 128;" ::: "memory");   // stg is rewritten next
-            }
             }
         }
     }
@@ -346,25 +348,41 @@ __global__ void __launch_bounds__(THREADS, 1)
 // `rows` read as zeros.
 cudaError_t make_map_bf16(CUtensorMap *m, const void *base, int rows, int cols, int ld, int box_rows);
 
-// ntile_bound: token tiles at most (dense: exact; grouped: the tile list's bound).
-template <bool GU, class Epi>
-static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
-                          const CUtensorMap &xlo, const Args &a, const Epi &epi, int mtiles, int ntile_bound,
-                          int nsm, cudaStream_t st)
+template <bool GU, int WN, class Epi>
+static cudaError_t launch_wn(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
+                             const CUtensorMap &xlo, const Args &a, const Epi &epi, long long work, int nsm,
+                             cudaStream_t st)
 {
-    const long long work = (long long)mtiles * ntile_bound;
-    if (work <= 0) return cudaSuccess;
     static bool attr_set = false;   // per instantiation; set before the first launch
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Geo<GU>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU, WN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Geo<GU, WN>::SMEM);
         if (e) return e;
         attr_set = true;
     }
     const int grid = (int)(work < nsm ? work : nsm);
-    k_tc_gemm<Epi, GU><<<grid, THREADS, Geo<GU>::SMEM, st>>>(w0, w1, xhi, xlo, a, epi);
+    k_tc_gemm<Epi, GU, WN><<<grid, THREADS, Geo<GU, WN>::SMEM, st>>>(w0, w1, xhi, xlo, a, epi);
     ++launch_count();
     return cudaGetLastError();
+}
+
+// ntile_bound: token tiles at most (dense: exact; grouped: the tile list's bound).
+// Plain GEMMs take 256-row weight tiles when that still gives every SM two tiles,
+// else 128-row tiles (twice the tiles, half the reuse of each token tile).
+template <bool GU, class Epi>
+static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
+                          const CUtensorMap &xlo, const Args &a, const Epi &epi, int ntile_bound, int nsm,
+                          cudaStream_t st)
+{
+    if (ntile_bound <= 0 || a.n_out <= 0) return cudaSuccess;
+    if constexpr (GU) {
+        return launch_wn<true, 256>(w0, w1, xhi, xlo, a, epi, (long long)(a.n_out / BOXW) * ntile_bound, nsm, st);
+    } else {
+        const long long w256 = (long long)((a.n_out + 255) / 256) * ntile_bound;
+        if (w256 >= 2ll * nsm) return launch_wn<false, 256>(w0, w1, xhi, xlo, a, epi, w256, nsm, st);
+        return launch_wn<false, 128>(w0, w1, xhi, xlo, a, epi, (long long)((a.n_out + 127) / 128) * ntile_bound,
+                                     nsm, st);
+    }
 }
 
 }  // namespace tc
