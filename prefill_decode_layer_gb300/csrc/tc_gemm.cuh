@@ -18,7 +18,7 @@
 // GEMMs (shared-memory bandwidth), not the tensor pipe.
 //
 // Persistent: one CTA per SM walks the output tiles (weight block fastest, so CTAs
-// running together share a token tile in L2) with 192 threads:
+// running together share a token tile in L2) with 320 threads:
 //   warp 0 lane 0   TMA producer: per 64-wide K stage, the weight tile (WN rows, as
 //                   128-row boxes) and the hi and lo token tiles (16 KB each),
 //                   128-byte swizzled, into a shared-memory ring (full / empty
@@ -27,12 +27,13 @@
 //                   issues the MMAs of tile i into accumulator i % 2 as soon as the
 //                   epilogue has drained it, and commits each stage back to the
 //                   producer and each tile to the epilogue;
-//   warps 2-5       epilogue, overlapping the next tile's MMAs.  Warp q reads TMEM
-//                   lanes 32q.. (its 32 tokens), 32 features at a time, stages them
-//                   as [token][feature] rows in shared memory and hands the
-//                   problem's functor four adjacent features of one token at a
-//                   time (so RoPE pairs are local to one call); a functor's global
-//                   loads (load4) are issued eight at a time before the stores.
+//   warps 2-9       epilogue, overlapping the next tile's MMAs.  Warp w reads TMEM
+//                   lanes 32 (w % 4).. (its 32 tokens) and every other 32-feature
+//                   chunk, stages a chunk as [token][feature] rows in its own
+//                   shared-memory slice and hands the problem's functor four
+//                   adjacent features of one token at a time (so RoPE pairs are
+//                   local to one call); a functor's global loads (load4) are issued
+//                   eight at a time before the stores.
 // Gate/up tiles (GU): the weight tile is 128 gate rows followed by the same 128 up
 // rows, so a feature's gate and up sit in the same TMEM lane, 128 columns apart;
 // SwiGLU is applied straight from the accumulator and each thread writes 32
@@ -52,12 +53,11 @@ namespace tc {
 static constexpr int BT = 128;      // tokens per tile (MMA M)
 static constexpr int BK = 64;       // K per stage: one 128-byte swizzle row of BF16
 static constexpr int BOXW = 128;    // weight rows per TMA box
-static constexpr int THREADS = 192;
+static constexpr int THREADS = 320;   // producer warp, MMA warp, 8 epilogue warps
 static constexpr uint32_t TILE_X = BT * BK * 2;              // 16 KB
 static constexpr uint32_t BOX_BYTES = BOXW * BK * 2;         // 16 KB
 static constexpr int CH = 32;                                // features per epilogue chunk
-static constexpr int EPI_PITCH = CH + 4;                     // floats per staged token row
-static constexpr uint32_t EPI_BYTES = BT * EPI_PITCH * 4;    // 18 KB
+static constexpr uint32_t EPI_BYTES = 8 * 32 * CH * 4;       // 32 KB: [8 warps][32 tokens][CH]
 static constexpr int EPI_BATCH = 8;                          // functor loads in flight
 
 // Tile geometry.  WN weight rows per tile: 256 -> 3 stages of 64 KB, 128 -> 4
@@ -90,6 +90,20 @@ struct Args {
 
 struct NoAux {};
 
+// A warp's staging rows: token t's 32 features as 8 float4 groups, group g stored at
+// slot g ^ (t & 7), so that eight threads writing (or reading) the same group of
+// eight tokens, or one token's eight groups, hit distinct banks.
+__device__ __forceinline__ void stage_row(float *wstg, int t, const float (&v)[32])
+{
+    float4 *row = reinterpret_cast<float4 *>(wstg + t * CH);
+#pragma unroll
+    for (int g = 0; g < CH / 4; ++g) row[g ^ (t & 7)] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+}
+__device__ __forceinline__ float4 staged(const float *wstg, int t, int g)
+{
+    return reinterpret_cast<const float4 *>(wstg + t * CH)[g ^ (t & 7)];
+}
+
 // GU: the tile's gate rows come from w0 and its up rows from w1 (same row index);
 // the epilogue calls Epi::store_row(m, i0, h[32], e) with h = silu(gate) * up of
 // features i0 .. i0 + 31 of token m.  Otherwise Epi provides  Aux load4(m, n, e)
@@ -105,11 +119,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr uint32_t STAGE_BYTES = G::STAGE;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // [BT][EPI_PITCH] (plain)
+    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // epilogue staging (plain)
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + (GU ? 0 : EPI_BYTES));
     uint64_t *empty = full + STAGES;
     uint64_t *accf = empty + STAGES;   // [2] accumulator ready (MMA commit)
-    uint64_t *acce = accf + 2;         // [2] accumulator drained (128 epilogue threads)
+    uint64_t *acce = accf + 2;         // [2] accumulator drained (256 epilogue threads)
     uint64_t *done = acce + 2;         // every MMA of this CTA completed
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
@@ -141,7 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
-            mbar_init(&acce[b], 128);
+            mbar_init(&acce[b], 256);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -255,10 +269,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(done, 0, &never);
         }
     } else {
-        // ---------------- epilogue (warps 2-5)
-        const int q = warp & 3;            // TMEM lane quarter this warp may access: tokens 32q ..
-        const int et = threadIdx.x - 64;   // 0..127
+        // ---------------- epilogue (warps 2-9): warp w reads TMEM lane quarter w % 4
+        // (tokens 32q ..) and takes every other 32-feature chunk of the tile
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int tok = 32 * q + lane;     // this thread's token row in the tile
+        float *wstg = stg + (warp - 2) * 32 * CH;   // this warp's [32 tokens][CH] staging rows
         unsigned tc = 0;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
             int mb, e, r0, rend;
@@ -275,13 +291,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // gate columns c, up columns 128 + c of this thread's token
                 const int m = r0 + tok;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BOXW; c0 += 32) {
+                for (int c0 = 32 * half; c0 < BOXW; c0 += 64) {
                     float g[32], u[32];
                     if (wlive) {
                         tmem_ld32(lane_base + (uint32_t)c0, g);
                         tmem_ld32(lane_base + (uint32_t)(BOXW + c0), u);
                     }
-                    if (c0 == BOXW - 32) {   // the accumulator is drained
+                    if (c0 + 64 >= BOXW) {   // this warp's share of the accumulator is drained
                         tc_fence_before();
                         mbar_arrive(&acce[b]);
                     }
@@ -294,41 +310,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < WN / CH; ++c) {
-                    // 32 features of this thread's token -> stg[tok][0 .. 31]
-                    if (wlive) {
+                for (int c = half; c < WN / CH; c += 2) {
+                    if (c + 2 >= WN / CH) {   // arrive once this warp's last chunk is read
                         float v[32];
-                        tmem_ld32(lane_base + (uint32_t)(c * CH), v);
-                        float4 *row = reinterpret_cast<float4 *>(stg + tok * EPI_PITCH);
-#pragma unroll
-                        for (int j = 0; j < CH / 4; ++j)
-                            row[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    }
-                    if (c == WN / CH - 1) {   // the accumulator is drained: the next tile may use it
+                        if (wlive) tmem_ld32(lane_base + (uint32_t)(c * CH), v);
                         tc_fence_before();
                         mbar_arrive(&acce[b]);
+                        if (!wlive) break;
+                        stage_row(wstg, lane, v);
+                    } else {
+                        if (!wlive) continue;
+                        float v[32];
+                        tmem_ld32(lane_base + (uint32_t)(c * CH), v);
+                        stage_row(wstg, lane, v);
                     }
-                    asm volatile("bar.sync 2, 128;" ::: "memory");
-                    // (token, 4 features) items: a warp covers 4 tokens x 32 features
-                    static_assert(BT * (CH / 4) == 128 * EPI_BATCH, "one batch of items per chunk");
+                    __syncwarp();
+                    // (token, 4 features) items: an instruction covers 4 tokens x 32 features
                     const int f0 = mb * WN + c * CH;
                     typename Epi::Aux aux[EPI_BATCH];
 #pragma unroll
                     for (int u = 0; u < EPI_BATCH; ++u) {
-                        const int idx = et + 128 * u;
-                        const int t = idx >> 3, j = (idx & 7) * 4;
-                        if (r0 + t < rend && f0 + j < a.n_out) aux[u] = epi.load4(r0 + t, f0 + j, e);
+                        const int idx = lane + 32 * u;
+                        const int t = idx >> 3, j = (idx & 7) * 4, m = r0 + 32 * q + t;
+                        if (m < rend && f0 + j < a.n_out) aux[u] = epi.load4(m, f0 + j, e);
                     }
 #pragma unroll
                     for (int u = 0; u < EPI_BATCH; ++u) {
-                        const int idx = et + 128 * u;
-                        const int t = idx >> 3, j = (idx & 7) * 4;
-                        if (r0 + t >= rend || f0 + j >= a.n_out) continue;
-                        const float4 v4 = *reinterpret_cast<const float4 *>(stg + t * EPI_PITCH + j);
+                        const int idx = lane + 32 * u;
+                        const int t = idx >> 3, j = (idx & 7) * 4, m = r0 + 32 * q + t;
+                        if (m >= rend || f0 + j >= a.n_out) continue;
+                        const float4 v4 = staged(wstg, t, j >> 2);
                         const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-                        epi.store4(r0 + t, f0 + j, v, aux[u], e);
+                        epi.store4(m, f0 + j, v, aux[u], e);
                     }
-                    asm volatile("bar.sync 2, 128;" ::: "memory");   // stg is rewritten next
+                    __syncwarp();   // the staging rows are rewritten next
                 }
             }
         }
