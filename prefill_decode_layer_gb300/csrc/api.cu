@@ -36,6 +36,7 @@ struct ds4g_session {
     DecodeBufs b;
     PrefillBufs pb;
     TcActMaps tcact;            // tensor maps of pb's activations, when the model's prefill is tc
+    std::vector<TcKVMaps> tckv; // per-layer K/V cache maps of the tcgen05 attention (when eligible)
     LayerPtrs *layers_dev;      // [L] device copy of the layer table
     void **kv_dev;              // [2L] device K then V cache pointers
     unsigned *bar;              // grid-barrier arrival counter of the persistent kernel
@@ -228,6 +229,7 @@ int ds4g_model_create(const ds4g_config *cfg, const ds4g_weights *w, ds4g_model 
     m->tc = !e && cfg->prefill_kernel == DS4G_PREFILL_AUTO && tc_prefill_eligible(m->d);
     if (m->tc) {
         e = attn_mma_setup(m->d, max_smem);
+        if (!e) e = attn_tc_setup(m->d, max_smem);
         m->tcmaps.resize(m->layers.size());
         for (size_t l = 0; !e && l < m->layers.size(); ++l) e = tc_layer_maps(m->d, m->layers[l], m->tcmaps[l]);
     }
@@ -303,6 +305,14 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
         delete s;
         return DS4G_ECUDA;
     }
+    if (m->tc && attn_tc_eligible(d)) {
+        s->tckv.resize(d.L);
+        for (int l = 0; l < d.L; ++l)
+            if (attn_tc_kv_maps(d, s->kc[l], s->vc[l], n_ctx, s->tckv[l])) {
+                delete s;
+                return DS4G_ECUDA;
+            }
+    }
     cudaError_t e = cudaMemsetAsync(base + L.dec, 0, L.pre - L.dec, s->st);
     if (!e) e = cudaMemcpyAsync(s->layers_dev, m->layers.data(), (size_t)d.L * sizeof(LayerPtrs),
                                 cudaMemcpyHostToDevice, s->st);
@@ -346,7 +356,8 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
         cudaError_t e = cudaMemcpyAsync(s->pb.tok, tokens + c, (size_t)nc * 4,
                                         cudaMemcpyHostToDevice, s->st);
         if (!e)
-            e = s->m->tc ? prefill_chunk_tc(d, s->m->layers.data(), s->m->tcmaps.data(), s->tcact, s->kc.data(),
+            e = s->m->tc ? prefill_chunk_tc(d, s->m->layers.data(), s->m->tcmaps.data(), s->tcact,
+                                            s->tckv.empty() ? nullptr : s->tckv.data(), s->kc.data(),
                                             s->vc.data(), s->rope, s->m->tok_embd, s->pb, s->len + c, nc, s->st,
                                             s->m->nsm)
                          : prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,

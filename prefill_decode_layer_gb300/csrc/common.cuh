@@ -220,6 +220,19 @@ __device__ __forceinline__ bool warp_topk(const float *s, int E, int K, float *s
 // SwiGLU of one gate/up pair: silu(g) * u.
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
+// An FP32 value as a BF16 pair: hi = bf16(v), lo = bf16(v - hi); hi + lo carries
+// about 16 significant bits of v.
+__device__ __forceinline__ void split_hilo(float v, bf16 &h, bf16 &l)
+{
+    h = __float2bfloat16_rn(v);
+    l = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+// Two BF16 values in one 32-bit word, a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(bf16 a, bf16 b)
+{
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
 template <typename T> struct VecOf;
 template <> struct VecOf<bf16> { static constexpr int n = 8; };
 template <> struct VecOf<float> { static constexpr int n = 4; };

@@ -21,12 +21,6 @@ namespace ds4g {
 
 // ------------------------------------------------------------------ small kernels
 
-__device__ __forceinline__ void split_hilo(float v, bf16 &h, bf16 &l)
-{
-    h = __float2bfloat16_rn(v);
-    l = __float2bfloat16_rn(v - __bfloat162float(h));
-}
-
 // RMSNorm of each residual row into hi/lo BF16: one CTA per token row, H/4 threads
 // (at most 1024), each keeping its float4s in registers between the two passes.
 __global__ void __launch_bounds__(1024) k_rmsnorm_hilo(const float *X, const float *g, bf16 *hi, bf16 *lo,
@@ -339,6 +333,26 @@ struct EpiQRope {   // Q[m][n..n+3] = RoPE(q) in FP32 (the attention's input)
     }
 };
 
+struct EpiQRopeHiLo {   // RoPE(q) as hi/lo BF16 [token][head][dim] rows (the tcgen05 attention's input)
+    bf16 *hi, *lo;
+    const float2 *rope;
+    int QD, HD, p0;
+    using Aux = float4;
+    __device__ Aux load4(int m, int n, int) const { return rope_pairs(rope, p0 + m, HD, n); }
+    __device__ void store4(int m, int n, const float (&v)[4], const Aux &cs, int) const
+    {
+        const float r[4] = {v[0] * cs.x - v[1] * cs.y, v[0] * cs.y + v[1] * cs.x, v[2] * cs.z - v[3] * cs.w,
+                            v[2] * cs.w + v[3] * cs.z};
+        bf16 h[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) split_hilo(r[j], h[j], l[j]);
+        *reinterpret_cast<uint2 *>(hi + (size_t)m * QD + n) =
+            make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+        *reinterpret_cast<uint2 *>(lo + (size_t)m * QD + n) =
+            make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+    }
+};
+
 template <typename TKV>
 struct EpiKVRope {   // features [0, HD): K with RoPE, [HD, 2HD): V; appended at p0 + m
     TKV *kc, *vc;
@@ -397,11 +411,6 @@ struct EpiRoutedRows {   // routed expert output of grouped row m into its (toke
         *reinterpret_cast<float4 *>(YS + (size_t)r * H + n) = make_float4(v[0], v[1], v[2], v[3]);
     }
 };
-
-__device__ __forceinline__ uint32_t pack_bf16x2(bf16 a, bf16 b)
-{
-    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-}
 
 struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16, 16-byte stores
     bf16 *hi, *lo;
@@ -519,14 +528,18 @@ cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m)
     if ((e = make_map_bf16(&m.hg_hi, a.hg_hi, PK, d.I, d.I, tc::BT))) return e;
     if ((e = make_map_bf16(&m.hg_lo, a.hg_lo, PK, d.I, d.I, tc::BT))) return e;
     if ((e = make_map_bf16(&m.hs_hi, a.hs_hi, P, d.I, d.I, tc::BT))) return e;
-    return make_map_bf16(&m.hs_lo, a.hs_lo, P, d.I, d.I, tc::BT);
+    if ((e = make_map_bf16(&m.hs_lo, a.hs_lo, P, d.I, d.I, tc::BT))) return e;
+    if (!attn_tc_eligible(d)) return cudaSuccess;
+    const bf16 *q_hi = (const bf16 *)pb.Q;   // the query buffer as hi then lo BF16 halves
+    return attn_tc_q_maps(d, P, q_hi, q_hi + (size_t)P * d.QD, m.q_hi, m.q_lo);
 }
 
 // ------------------------------------------------------------------ one chunk
 
 template <typename TKV>
 static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
-                              const TcActMaps &am, void *const *kcs, void *const *vcs, const float2 *rope,
+                              const TcActMaps &am, const TcKVMaps *kvm, void *const *kcs, void *const *vcs,
+                              const float2 *rope,
                               const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n,
                               cudaStream_t st, int nsm)
 {
@@ -558,14 +571,24 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
                                    ny, nsm, st)))
             return e;
         a.n_out = d.QD, a.k = d.RQ, a.piece_rows = 0, a.x_col0 = 0;
-        if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a, EpiQRope{(float *)pb.Q, rope, d.QD, d.HD, p0},
-                                   ny, nsm, st)))
+        const bool attn_tc = kvm != nullptr;   // tcgen05 attention: queries as hi/lo BF16
+        if (attn_tc) {
+            bf16 *q_hi = (bf16 *)pb.Q, *q_lo = q_hi + (size_t)pb.P * d.QD;
+            if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
+                                       EpiQRopeHiLo{q_hi, q_lo, rope, d.QD, d.HD, p0}, ny, nsm, st)))
+                return e;
+        } else if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
+                                          EpiQRope{(float *)pb.Q, rope, d.QD, d.HD, p0}, ny, nsm, st))) {
             return e;
+        }
         a.n_out = 2 * d.HD, a.k = d.RKV, a.piece_rows = d.HD, a.x_col0 = d.RQ;
         if ((e = tc::launch<false>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, EpiKVRope<TKV>{kc, vc, rope, d.HD, p0}, ny,
                                    nsm, st)))
             return e;
-        if constexpr (std::is_same<TKV, bf16>::value) {
+        if (attn_tc) {
+            if ((e = attn_prefill_tc(d, am.q_hi, am.q_lo, kvm[l], ap.o_hi, ap.o_lo, p0, n, pb.status, st, nsm)))
+                return e;
+        } else if constexpr (std::is_same<TKV, bf16>::value) {
             if (attn_mma_eligible(d)) {
                 k_attn_prefill_mma<<<(n + kAttnTB - 1) / kAttnTB, 256, attn_mma_smem(d), st>>>(
                     (const float *)pb.Q, ap.o_hi, ap.o_lo, kc, vc, p0, n, d);
@@ -619,12 +642,13 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
 }
 
 cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
-                             const TcActMaps &am, void *const *kc, void *const *vc, const float2 *rope,
-                             const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n, cudaStream_t st,
-                             int nsm)
+                             const TcActMaps &am, const TcKVMaps *kvm, void *const *kc, void *const *vc,
+                             const float2 *rope, const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n,
+                             cudaStream_t st, int nsm)
 {
-    return d.kvdt == DS4G_BF16 ? chunk_tc_t<bf16>(d, layers, lm, am, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
-                               : chunk_tc_t<float>(d, layers, lm, am, kc, vc, rope, tok_embd, pb, p0, n, st, nsm);
+    return d.kvdt == DS4G_BF16
+               ? chunk_tc_t<bf16>(d, layers, lm, am, kvm, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
+               : chunk_tc_t<float>(d, layers, lm, am, nullptr, kc, vc, rope, tok_embd, pb, p0, n, st, nsm);
 }
 
 }  // namespace ds4g

@@ -14,8 +14,11 @@ struct TcLayerMaps {   // boxes: 64 columns x 128 rows
 struct TcActPtrs {     // hi/lo BF16 halves of the prefill activation buffers
     bf16 *xn_hi, *xn_lo, *c_hi, *c_lo, *o_hi, *o_lo, *xg_hi, *xg_lo, *hg_hi, *hg_lo, *hs_hi, *hs_lo;
 };
-struct TcActMaps {     // boxes: 64 columns x 128 token rows
-    CUtensorMap xn_hi, xn_lo, c_hi, c_lo, o_hi, o_lo, xg_hi, xg_lo, hg_hi, hg_lo, hs_hi, hs_lo;
+struct TcActMaps {     // boxes: 64 columns x 128 token rows (q: x 128 [token][head] rows)
+    CUtensorMap xn_hi, xn_lo, c_hi, c_lo, o_hi, o_lo, xg_hi, xg_lo, hg_hi, hg_lo, hs_hi, hs_lo, q_hi, q_lo;
+};
+struct TcKVMaps {      // one layer's K and V cache, boxes: 64 dims x the attention's staged key rows
+    CUtensorMap k, v;
 };
 
 // Shapes the tensor-core form covers: BF16 weights; every weight piece a multiple
@@ -24,13 +27,24 @@ bool tc_prefill_eligible(const Dims &d);
 // Tensor-core attention for the prefill (head dim 128, window <= 128, BF16 KV).
 bool attn_mma_eligible(const Dims &d);
 cudaError_t attn_mma_setup(const Dims &d, int max_smem);
+// Tensor-core attention for the prefill on tcgen05 (attn_tc.cu): head dim 128, NH
+// in {16, 32, 64, 128}, window <= 128, BF16 KV; queries as BF16 hi/lo.
+bool attn_tc_eligible(const Dims &d);
+size_t attn_tc_smem(const Dims &d);
+cudaError_t attn_tc_setup(const Dims &d, int max_smem);
+cudaError_t attn_tc_kv_maps(const Dims &d, const void *kc, const void *vc, int n_ctx, TcKVMaps &m);
+cudaError_t attn_tc_q_maps(const Dims &d, int P, const bf16 *q_hi, const bf16 *q_lo, CUtensorMap &mhi,
+                           CUtensorMap &mlo);
+cudaError_t attn_prefill_tc(const Dims &d, const CUtensorMap &qhi, const CUtensorMap &qlo, const TcKVMaps &kv,
+                            bf16 *o_hi, bf16 *o_lo, int p0, int n, int *status, cudaStream_t st, int nsm);
 cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m);
 TcActPtrs tc_act_ptrs(const Dims &d, const PrefillBufs &pb);
 cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m);
+// kvm: per-layer K/V maps for the tcgen05 attention (nullptr: the warp-MMA one).
 cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
-                             const TcActMaps &am, void *const *kc, void *const *vc, const float2 *rope,
-                             const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n, cudaStream_t st,
-                             int nsm);
+                             const TcActMaps &am, const TcKVMaps *kvm, void *const *kc, void *const *vc,
+                             const float2 *rope, const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n,
+                             cudaStream_t st, int nsm);
 
 // prefill.cu kernels the tensor-core form shares
 __global__ void k_embed_rows(const uint16_t *table, const int *tok, float *X, int H);

@@ -184,5 +184,58 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes into registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory descriptor of a K-major operand without swizzle: 8-row x 16-byte
+// core matrices (128 contiguous bytes each), `lbo` bytes between core matrices
+// adjacent in K and `sbo` bytes between 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_kmajor_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version for tcgen05; swizzle field 0: none
+    return d;
+}
+// Shared-memory descriptor of an MN-major operand with the 128-byte swizzle: rows of
+// 64 BF16 along MN (one row per K index, 128 bytes apart), 8-row groups `sbo` bytes
+// apart along K, and blocks of 64 MN elements `lbo` bytes apart (the layout a TMA
+// box of 64 columns writes).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;   // swizzle: 128 bytes
+    return d;
+}
+// Instruction descriptor as idesc_bf16_f32 with B stored MN-major (transposed).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N)
+{
+    return idesc_bf16_f32(M, N) | (1u << 16);
+}
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// accesses (tensor-core operand reads) of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 }  // namespace ds4g
