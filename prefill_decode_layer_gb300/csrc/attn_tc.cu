@@ -23,12 +23,15 @@
 // zeros), so a token's result does not depend on how the prompt was cut into
 // chunks or blocks.
 //
-// Roles (160 threads, one CTA per SM, persistent over blocks):
-//   warps 0-3        softmax and output of rows 32w .. 32w + 31 (their TMEM lanes);
-//   warp 4 lane 0    TMA and MMA issue.  The next block's Q and K tiles load while
-//                    this block's softmax runs, its V tile while this block's
-//                    output is written; two TMEM buffers (S, then O in the same
-//                    columns) let the next block's S run during this block's output.
+// Roles (544 threads, one CTA per SM, persistent over blocks):
+//   warps 0-15       softmax and output; warp w serves rows 32 (w % 4) .. +31 (its
+//                    TMEM lanes) over every 4th 16-key chunk and one quarter of the
+//                    128 output dims; the four parts of a row combine their maxima
+//                    and sums through shared memory, in a fixed order;
+//   warp 16 lane 0   TMA and MMA issue.  The next block's Q and K tiles load while
+//                    this block's softmax runs and its S is issued as soon as they
+//                    have landed (two TMEM buffers: S, then O in the same columns);
+//                    its V tile loads once this block's O is complete.
 // Every wait is bounded; a CTA that gives up raises DS4G_ETIMEOUT, drains its copies
 // and MMAs, frees its TMEM and returns.
 #include <cuda.h>
@@ -42,7 +45,10 @@ namespace ds4g {
 static constexpr int kTaHD = 128;         // head dimension
 static constexpr int kTaRows = 128;       // query rows per block (MMA M)
 static constexpr int kTaMaxW = 128;       // largest window
-static constexpr int kTaThreads = 160;
+static constexpr int kTaParts = 4;        // softmax warps per TMEM lane quarter (column parts)
+static constexpr int kTaSoft = 128 * kTaParts;   // softmax / output threads
+static constexpr int kTaCtl = kTaSoft / 32;      // the issuing warp
+static constexpr int kTaThreads = kTaSoft + 32;
 static constexpr uint32_t kTaQBox = kTaRows * 64 * 2;   // one 64-dim box of 128 query rows (16 KB)
 
 // Staged key rows for NH heads: the union of 128 / NH windows, from a 16-aligned
@@ -51,7 +57,7 @@ static int ta_key_rows(int W, int NH) { return ((W + kTaRows / NH - 1 + 15) + 15
 
 // Shared-memory layout of one CTA (offsets from the 1024-aligned base).
 struct TaLayout {
-    uint32_t qhi, qlo, k, v, phi, plo, bars, total;
+    uint32_t qhi, qlo, k, v, phi, plo, red, bars, total;
     __host__ __device__ explicit TaLayout(int KR)
     {
         const uint32_t kv = (uint32_t)KR * 128 * 2;   // two 64-dim boxes of KR rows
@@ -62,14 +68,23 @@ struct TaLayout {
         v = k + kv;
         phi = v + kv;
         plo = phi + p;
-        bars = plo + p;
-        total = bars + 256;
+        // the output's staging boxes reuse the P rows: at least 4 boxes of 16 KB
+        red = phi + (2 * p > 4 * kTaQBox ? 2 * p : 4 * kTaQBox);   // [kTaParts][128] row maxima, then sums
+        bars = red + kTaParts * kTaRows * 4;
+        total = bars + 128;
     }
 };
 
+__device__ __forceinline__ float ex2_approx(float x)   // 2^x (hardware approximation)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 bool attn_tc_eligible(const Dims &d)
 {
-    const bool nh_ok = d.NH == 16 || d.NH == 32 || d.NH == 64 || d.NH == 128;
+    const bool nh_ok = d.NH == 64 || d.NH == 128;   // 2 or 1 tokens per 128-row block
     return d.kvdt == DS4G_BF16 && d.HD == kTaHD && nh_ok && d.W >= 1 && d.W <= kTaMaxW;
 }
 
@@ -78,16 +93,18 @@ size_t attn_tc_smem(const Dims &d) { return 1024 + TaLayout(ta_key_rows(d.W, d.N
 __global__ void __launch_bounds__(kTaThreads, 1)
     k_attn_prefill_tc(const __grid_constant__ CUtensorMap qhi, const __grid_constant__ CUtensorMap qlo,
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      bf16 *o_hi, bf16 *o_lo, int p0, int n, int NH, int W, int KR, int *status)
+                      const __grid_constant__ CUtensorMap ohi, const __grid_constant__ CUtensorMap olo, int p0,
+                      int n, int NH, int W, int KR, int *status)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const TaLayout L(KR);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L.bars);
-    uint64_t *bar_qk = bar, *bar_v = bar + 1, *bar_s = bar + 2, *bar_p = bar + 3, *bar_o = bar + 4;
-    uint64_t *bar_oe = bar + 5;   // [2]: TMEM buffer drained by the output threads
-    uint64_t *done = bar + 7;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 8);
+    uint64_t *bar_qk = bar, *bar_v = bar + 1, *bar_p = bar + 2, *bar_o = bar + 3;
+    uint64_t *bar_s = bar + 4;    // [2]: S of TMEM buffer b computed
+    uint64_t *bar_oe = bar + 6;   // [2]: TMEM buffer b drained by the output threads
+    uint64_t *done = bar + 8;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 9);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int TB = kTaRows / NH;   // tokens per block
@@ -104,16 +121,17 @@ __global__ void __launch_bounds__(kTaThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar_qk, 1);
         mbar_init(bar_v, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_p, 128);
+        mbar_init(&bar_s[0], 1);
+        mbar_init(&bar_s[1], 1);
+        mbar_init(bar_p, kTaSoft);
         mbar_init(bar_o, 1);
-        mbar_init(&bar_oe[0], 128);
-        mbar_init(&bar_oe[1], 128);
+        mbar_init(&bar_oe[0], kTaSoft);
+        mbar_init(&bar_oe[1], kTaSoft);
         mbar_init(done, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 4) tmem_alloc(tslot, 512);
+    if (warp == kTaCtl) tmem_alloc(tslot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -124,7 +142,7 @@ __global__ void __launch_bounds__(kTaThreads, 1)
         atomicExch(status, DS4G_ETIMEOUT);
     };
 
-    if (warp == 4) {
+    if (warp == kTaCtl) {
         if (lane == 0) {
             // ---------------- TMA and MMA issue
             tma_prefetch_desc(&qhi);
@@ -149,56 +167,29 @@ __global__ void __launch_bounds__(kTaThreads, 1)
                 tma_load_2d(sm + L.v, &vmap, 0, kbase, bar_v);
                 tma_load_2d(sm + L.v + kvbox, &vmap, 64, kbase, bar_v);
             };
-            unsigned nqk = 0, nv = 0;   // copies issued on bar_qk / bar_v
-            int blk = blockIdx.x;
-            if (blk < nblk) {
-                issue_qk(blk);
-                issue_v(blk);
-                nqk = nv = 1;
-            }
             const uint32_t id_o = idesc_bf16_f32_bmn(kTaRows, kTaHD);
-            for (int it = 0; blk < nblk; blk += gridDim.x, ++it) {
-                const int b = it & 1;
+            // S of block blk (the it-th of this CTA) into TMEM buffer it % 2
+            auto issue_s = [&](int it, int blk) {
                 int kbase, span;
                 block_keys(blk, kbase, span);
-                const int nk16 = (span + 15) / 16 * 16;
-                if (!mbar_wait(bar_qk, it & 1, ab)) {
-                    give_up();
-                    break;
-                }
-                if (it >= 2 && !mbar_wait(&bar_oe[b], ((it >> 1) & 1) ^ 1, ab)) {
-                    give_up();
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)(b * 256);
-                // S = (Qhi + Qlo) K^T: 8 steps of 16 dims
-                const uint32_t id_s = idesc_bf16_f32(kTaRows, nk16);
+                const uint32_t acc = tmem + (uint32_t)((it & 1) * 256);
+                const uint32_t id_s = idesc_bf16_f32(kTaRows, (span + 15) / 16 * 16);
 #pragma unroll
-                for (int ks = 0; ks < kTaHD / 16; ++ks) {
+                for (int ks = 0; ks < kTaHD / 16; ++ks) {   // 16 dims a step
                     const uint32_t qoff = (uint32_t)(ks >> 2) * kTaQBox + (uint32_t)(ks & 3) * 32;
                     const uint64_t kd = sdesc_kmajor_sw128(sbase + L.k + (uint32_t)(ks >> 2) * kvbox +
                                                            (uint32_t)(ks & 3) * 32);
                     tc_mma_bf16(acc, sdesc_kmajor_sw128(sbase + L.qhi + qoff), kd, id_s, ks > 0);
                     tc_mma_bf16(acc, sdesc_kmajor_sw128(sbase + L.qlo + qoff), kd, id_s, 1u);
                 }
-                tc_commit(bar_s);
-                if (!mbar_wait(bar_s, it & 1, ab)) {
-                    give_up();
-                    break;
-                }
-                const int next = blk + gridDim.x;
-                if (next < nblk) {   // the Q and K tiles are free: stage the next block's
-                    issue_qk(next);
-                    ++nqk;
-                }
-                if (!mbar_wait(bar_p, it & 1, ab)) {
-                    give_up();
-                    break;
-                }
-                tc_fence_after();
-                // O = (Phi + Plo) V over 16-key steps, into the columns S held
-                for (int ks = 0; ks < nk16 / 16; ++ks) {
+                tc_commit(&bar_s[it & 1]);
+            };
+            // O of block blk over 16-key steps, into the columns its S held
+            auto issue_pv = [&](int it, int blk) {
+                int kbase, span;
+                block_keys(blk, kbase, span);
+                const uint32_t acc = tmem + (uint32_t)((it & 1) * 256);
+                for (int ks = 0; ks < (span + 15) / 16; ++ks) {
                     const uint64_t vd = sdesc_mnmajor_sw128(sbase + L.v + (uint32_t)ks * 2048, kvbox, 1024);
                     const uint32_t poff = (uint32_t)ks * 256;
                     tc_mma_bf16(acc, sdesc_kmajor_plain(sbase + L.phi + poff, 128, (uint32_t)KR * 16), vd, id_o,
@@ -206,11 +197,59 @@ __global__ void __launch_bounds__(kTaThreads, 1)
                     tc_mma_bf16(acc, sdesc_kmajor_plain(sbase + L.plo + poff, 128, (uint32_t)KR * 16), vd, id_o, 1u);
                 }
                 tc_commit(bar_o);
-                if (!mbar_wait(bar_o, it & 1, ab)) {
+            };
+            unsigned nqk = 0, nv = 0;   // copies issued on bar_qk / bar_v
+            int blk = blockIdx.x;
+            bool ok = true;
+            if (blk < nblk) {
+                issue_qk(blk);
+                issue_v(blk);
+                nqk = nv = 1;
+                ok = mbar_wait(bar_qk, 0, ab);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0, blk);
+                } else {
+                    give_up();
+                }
+            }
+            for (int it = 0; ok && blk < nblk; blk += gridDim.x, ++it) {
+                const int b = it & 1, next = blk + gridDim.x;
+                const bool has_next = next < nblk;
+                if (!mbar_wait(&bar_s[b], (it >> 1) & 1, ab)) {
                     give_up();
                     break;
                 }
-                if (next < nblk) {   // V and P are free
+                if (has_next) {   // the Q and K tiles are free: stage the next block's
+                    issue_qk(next);
+                    ++nqk;
+                }
+                // whichever comes first: this block's P (then its O = P V), or the next
+                // block's Q and K with a drained TMEM buffer (then its S)
+                bool s_done = !has_next, pv_done = false;
+                const long long t0 = clock64();
+                while (!(s_done && pv_done)) {
+                    if (!pv_done && mbar_try_wait(bar_p, it & 1)) {
+                        tc_fence_after();
+                        issue_pv(it, blk);
+                        pv_done = true;
+                    }
+                    if (!s_done && mbar_try_wait(bar_qk, (it + 1) & 1) &&
+                        (it < 1 || mbar_try_wait(&bar_oe[b ^ 1], (((it + 1) >> 1) & 1) ^ 1))) {
+                        tc_fence_after();
+                        issue_s(it + 1, next);
+                        s_done = true;
+                    }
+                    if (*ab || clock64() - t0 > kWaitCycles) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok || !mbar_wait(bar_o, it & 1, ab)) {
+                    give_up();
+                    break;
+                }
+                if (has_next) {   // V and P are free
                     issue_v(next);
                     ++nv;
                 }
@@ -223,54 +262,79 @@ __global__ void __launch_bounds__(kTaThreads, 1)
             mbar_wait(done, 0, &never);
         }
     } else {
-        // ---------------- softmax and output: thread = query row r of the block
-        const int r = 32 * warp + lane;
+        // ---------------- softmax and output: warp w serves query rows r = 32 (w % 4) +
+        // lane (its TMEM lanes) over every kTaParts-th 16-key chunk and one quarter of O
+        const int q = warp & 3, part = warp >> 2;
+        const int r = 32 * q + lane;
         const float scale = rsqrtf((float)kTaHD);
         const uint32_t pbase = (uint32_t)(r >> 3) * ((uint32_t)KR * 16) + (uint32_t)(r & 7) * 16;
+        float *red = reinterpret_cast<float *>(sm + L.red);   // [part][row]
+        // barrier of the softmax threads that also tells each of them whether any failed,
+        // so that all leave the loop together
+        auto soft_sync_any = [&](bool fail) -> bool {
+            uint32_t any;
+            asm volatile(
+                "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, %2, q;\n"
+                " selp.u32 %0, 1, 0, p;\n}\n"
+                : "=r"(any)
+                : "r"((uint32_t)fail), "n"(kTaSoft)
+                : "memory");
+            return any != 0;
+        };
+        auto soft_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kTaSoft) : "memory"); };
+        // a bounded wait whose outcome is the same for the whole warp
+        auto warp_wait = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab)) != 0;
+        };
         int it = 0;
         for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
             const int b = it & 1;
             int kbase, span;
             block_keys(blk, kbase, span);
-            const int nk16 = (span + 15) / 16 * 16;
+            const int nch = (span + 15) / 16;   // 16-key chunks
             const int t = blk * TB + r / NH;
             const bool live = t < n;
             const int pos = p0 + t;
             const int lo = max(0, pos - W + 1) - kbase, hi = pos - kbase;   // the row's window, in columns
-            if (!mbar_wait(bar_s, it & 1, ab)) {
+            const uint32_t row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256);
+            float mx = -INFINITY;
+            bool ok = warp_wait(&bar_s[b], (it >> 1) & 1);
+            if (ok) {
+                tc_fence_after();
+                for (int ch = part; ch < nch; ch += kTaParts) {
+                    float s[16];
+                    tmem_ld16(row + (uint32_t)(16 * ch), s);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (16 * ch + j >= lo && 16 * ch + j <= hi) mx = fmaxf(mx, s[j]);
+                }
+            }
+            red[part * kTaRows + r] = mx;
+            if (soft_sync_any(!ok)) {
                 give_up();
                 break;
             }
-            tc_fence_after();
-            const uint32_t row = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(b * 256);
-            float mx = -INFINITY;
-            for (int c0 = 0; c0 < nk16; c0 += 16) {
-                float s[16];
-                tmem_ld16(row + (uint32_t)c0, s);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c0 + j >= lo && c0 + j <= hi) mx = fmaxf(mx, s[j]);
-            }
+            for (int u = 0; u < kTaParts; ++u) mx = fmaxf(mx, red[u * kTaRows + r]);
+            if (threadIdx.x == 0) bulk_wait_read();   // the previous block's output has left the P region
+            soft_sync();   // red is rewritten with the sums below, the P region with P
+            // P = 2^(S scale / ln 2 - max scale / ln 2): one FMA and one exp2 per key
+            const float c2 = scale * 1.44269504088896341f, moff = mx * c2;
             float sum = 0.f;
-            for (int c0 = 0; c0 < nk16; c0 += 16) {
+            for (int ch = part; ch < nch; ch += kTaParts) {
+                const int c0 = 16 * ch;
                 float s[16];
                 tmem_ld16(row + (uint32_t)c0, s);
+                const bool inside = live && c0 >= lo && c0 + 15 <= hi;   // the whole chunk is in the window
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const bool in = inside || (live && c0 + j >= lo && c0 + j <= hi);
+                    s[j] = in ? ex2_approx(fmaf(s[j], c2, -moff)) : 0.f;
+                    sum += s[j];
+                }
                 uint32_t wh[8], wl[8];
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    float p2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = c0 + j + u;
-                        p2[u] = live && c >= lo && c <= hi ? __expf((s[j + u] - mx) * scale) : 0.f;
-                        sum += p2[u];
-                    }
-                    bf16 h0, l0, h1, l1;
-                    split_hilo(p2[0], h0, l0);
-                    split_hilo(p2[1], h1, l1);
-                    wh[j / 2] = pack_bf16x2(h0, h1);
-                    wl[j / 2] = pack_bf16x2(l0, l1);
-                }
+                for (int j = 0; j < 8; ++j) split2_hilo(s[2 * j], s[2 * j + 1], wh[j], wl[j]);
                 // keys c0 .. c0+7 and c0+8 .. c0+15: two core matrices of the row's group
                 const uint32_t off = pbase + (uint32_t)(c0 >> 3) * 128;
                 *reinterpret_cast<uint4 *>(sm + L.phi + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
@@ -278,54 +342,68 @@ __global__ void __launch_bounds__(kTaThreads, 1)
                 *reinterpret_cast<uint4 *>(sm + L.plo + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 *reinterpret_cast<uint4 *>(sm + L.plo + off + 128) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
             }
+            red[part * kTaRows + r] = sum;
             // staged V rows past the last key are multiplied by P = 0: make them zeros
-            if (!mbar_wait(bar_v, it & 1, ab)) {
+            ok = warp_wait(bar_v, it & 1);
+            if (ok) {
+                for (int i = threadIdx.x; i < (16 * nch - span) * 16; i += kTaSoft) {
+                    const int vr = span + (i >> 4), box = (i >> 3) & 1, c16 = i & 7;
+                    *reinterpret_cast<uint4 *>(sm + L.v + (uint32_t)box * kvbox + (uint32_t)vr * 128 + c16 * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();   // P and the zeroed rows, before the MMAs read them
+                tc_fence_before();          // this thread's S reads, before O overwrites the columns
+                mbar_arrive(bar_p);
+            }
+            if (soft_sync_any(!ok)) {   // (also: every part's row sum is in red)
                 give_up();
                 break;
             }
-            for (int i = r; i < (nk16 - span) * 16; i += 128) {
-                const int vr = span + (i >> 4), box = (i >> 3) & 1, ch = i & 7;
-                *reinterpret_cast<uint4 *>(sm + L.v + (uint32_t)box * kvbox + (uint32_t)vr * 128 + ch * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();   // P and the zeroed rows, before the MMAs read them
-            tc_fence_before();          // this row's S reads, before O overwrites its columns
-            mbar_arrive(bar_p);
-            if (!mbar_wait(bar_o, it & 1, ab)) {
-                give_up();
-                break;
-            }
-            tc_fence_after();
+            sum = 0.f;
+#pragma unroll
+            for (int u = 0; u < kTaParts; ++u) sum += red[u * kTaRows + r];   // parts in a fixed order
             const float inv = live ? 1.f / sum : 0.f;
-            bf16 *oh = o_hi + ((size_t)blk * kTaRows + r) * kTaHD;
-            bf16 *ol = o_lo + ((size_t)blk * kTaRows + r) * kTaHD;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kTaHD; c0 += 32) {
+            const int c0 = 32 * part;   // this warp's quarter of O
+            ok = warp_wait(bar_o, it & 1);
+            if (ok) {
+                tc_fence_after();
                 float o[32];
                 tmem_ld32(row + (uint32_t)c0, o);
-                if (!live) continue;
+                // this thread's 32 dims of O / sum as hi and lo BF16 into the P region (free
+                // once O is complete), laid out as the 128-byte-swizzled 64-dim boxes that
+                // the tensor store reads: boxes hi 0-63, hi 64-127, lo 0-63, lo 64-127
+                unsigned char *bh = sm + L.phi + (uint32_t)(part >> 1) * kTaQBox, *bl = bh + 2 * kTaQBox;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
+                for (int j = 0; j < 4; ++j) {
                     uint32_t wh[4], wl[4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        bf16 h0, l0, h1, l1;
-                        split_hilo(o[8 * v + 2 * j] * inv, h0, l0);
-                        split_hilo(o[8 * v + 2 * j + 1] * inv, h1, l1);
-                        wh[j] = pack_bf16x2(h0, h1);
-                        wl[j] = pack_bf16x2(l0, l1);
-                    }
-                    reinterpret_cast<uint4 *>(oh + c0)[v] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                    reinterpret_cast<uint4 *>(ol + c0)[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                    for (int u = 0; u < 4; ++u)
+                        split2_hilo(o[8 * j + 2 * u] * inv, o[8 * j + 2 * u + 1] * inv, wh[u], wl[u]);
+                    const uint32_t cj = (uint32_t)r * 128 + (uint32_t)((((part & 1) * 4 + j) ^ (r & 7)) * 16);
+                    *reinterpret_cast<uint4 *>(bh + cj) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                    *reinterpret_cast<uint4 *>(bl + cj) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
+                fence_proxy_async_smem();   // the staged rows, before the tensor store reads them
+                tc_fence_before();
+                mbar_arrive(&bar_oe[b]);
             }
-            tc_fence_before();
-            mbar_arrive(&bar_oe[b]);
+            if (soft_sync_any(!ok)) {
+                give_up();
+                break;
+            }
+            if (threadIdx.x == 0) {   // rows blk * 128 .. of the [token][head] output
+                tma_store_2d(&ohi, sm + L.phi, 0, blk * kTaRows);
+                tma_store_2d(&ohi, sm + L.phi + kTaQBox, 64, blk * kTaRows);
+                tma_store_2d(&olo, sm + L.phi + 2 * kTaQBox, 0, blk * kTaRows);
+                tma_store_2d(&olo, sm + L.phi + 3 * kTaQBox, 64, blk * kTaRows);
+                bulk_commit();   // read out of the P region while the next block's S and maxima run
+            }
         }
+        if (threadIdx.x == 0) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kTaCtl) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -349,23 +427,21 @@ cudaError_t attn_tc_kv_maps(const Dims &d, const void *kc, const void *vc, int n
     return e;
 }
 
-cudaError_t attn_tc_q_maps(const Dims &d, int P, const bf16 *q_hi, const bf16 *q_lo, CUtensorMap &mhi,
-                           CUtensorMap &mlo)
+cudaError_t attn_tc_row_map(const Dims &d, int P, const bf16 *base, CUtensorMap &m)
 {
-    cudaError_t e = tc::make_map_bf16(&mhi, q_hi, P * d.NH, kTaHD, kTaHD, kTaRows);
-    if (!e) e = tc::make_map_bf16(&mlo, q_lo, P * d.NH, kTaHD, kTaHD, kTaRows);
-    return e;
+    return tc::make_map_bf16(&m, base, P * d.NH, kTaHD, kTaHD, kTaRows);
 }
 
 cudaError_t attn_prefill_tc(const Dims &d, const CUtensorMap &qhi, const CUtensorMap &qlo, const TcKVMaps &kv,
-                            bf16 *o_hi, bf16 *o_lo, int p0, int n, int *status, cudaStream_t st, int nsm)
+                            const CUtensorMap &ohi, const CUtensorMap &olo, int p0, int n, int *status,
+                            cudaStream_t st, int nsm)
 {
     const int TB = kTaRows / d.NH, nblk = (n + TB - 1) / TB;
     if (nblk <= 0) return cudaSuccess;
     const int KR = ta_key_rows(d.W, d.NH);
     const int grid = nblk < nsm ? nblk : nsm;
-    k_attn_prefill_tc<<<grid, kTaThreads, attn_tc_smem(d), st>>>(qhi, qlo, kv.k, kv.v, o_hi, o_lo, p0, n, d.NH,
-                                                                 d.W, KR, status);
+    k_attn_prefill_tc<<<grid, kTaThreads, attn_tc_smem(d), st>>>(qhi, qlo, kv.k, kv.v, ohi, olo, p0, n, d.NH, d.W,
+                                                                 KR, status);
     ++launch_count();
     return cudaGetLastError();
 }

@@ -233,6 +233,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(bf16 a, bf16 b)
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
+// split_hilo of two values, each half packed as a BF16 pair (a in the low half).
+__device__ __forceinline__ void split2_hilo(float a, float b, uint32_t &hi, uint32_t &lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
 template <typename T> struct VecOf;
 template <> struct VecOf<bf16> { static constexpr int n = 8; };
 template <> struct VecOf<float> { static constexpr int n = 4; };

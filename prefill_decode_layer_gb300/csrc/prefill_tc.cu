@@ -531,7 +531,10 @@ cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m)
     if ((e = make_map_bf16(&m.hs_lo, a.hs_lo, P, d.I, d.I, tc::BT))) return e;
     if (!attn_tc_eligible(d)) return cudaSuccess;
     const bf16 *q_hi = (const bf16 *)pb.Q;   // the query buffer as hi then lo BF16 halves
-    return attn_tc_q_maps(d, P, q_hi, q_hi + (size_t)P * d.QD, m.q_hi, m.q_lo);
+    if ((e = attn_tc_row_map(d, P, q_hi, m.q_hi))) return e;
+    if ((e = attn_tc_row_map(d, P, q_hi + (size_t)P * d.QD, m.q_lo))) return e;
+    if ((e = attn_tc_row_map(d, P, a.o_hi, m.oa_hi))) return e;   // the attention output's [token][head] rows
+    return attn_tc_row_map(d, P, a.o_lo, m.oa_lo);
 }
 
 // ------------------------------------------------------------------ one chunk
@@ -586,7 +589,8 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
                                    nsm, st)))
             return e;
         if (attn_tc) {
-            if ((e = attn_prefill_tc(d, am.q_hi, am.q_lo, kvm[l], ap.o_hi, ap.o_lo, p0, n, pb.status, st, nsm)))
+            if ((e = attn_prefill_tc(d, am.q_hi, am.q_lo, kvm[l], am.oa_hi, am.oa_lo, p0, n, pb.status, st,
+                                     nsm)))
                 return e;
         } else if constexpr (std::is_same<TKV, bf16>::value) {
             if (attn_mma_eligible(d)) {

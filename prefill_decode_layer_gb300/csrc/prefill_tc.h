@@ -14,8 +14,9 @@ struct TcLayerMaps {   // boxes: 64 columns x 128 rows
 struct TcActPtrs {     // hi/lo BF16 halves of the prefill activation buffers
     bf16 *xn_hi, *xn_lo, *c_hi, *c_lo, *o_hi, *o_lo, *xg_hi, *xg_lo, *hg_hi, *hg_lo, *hs_hi, *hs_lo;
 };
-struct TcActMaps {     // boxes: 64 columns x 128 token rows (q: x 128 [token][head] rows)
-    CUtensorMap xn_hi, xn_lo, c_hi, c_lo, o_hi, o_lo, xg_hi, xg_lo, hg_hi, hg_lo, hs_hi, hs_lo, q_hi, q_lo;
+struct TcActMaps {     // boxes: 64 columns x 128 token rows (q, oa: x 128 [token][head] rows)
+    CUtensorMap xn_hi, xn_lo, c_hi, c_lo, o_hi, o_lo, xg_hi, xg_lo, hg_hi, hg_lo, hs_hi, hs_lo, q_hi, q_lo, oa_hi,
+        oa_lo;
 };
 struct TcKVMaps {      // one layer's K and V cache, boxes: 64 dims x the attention's staged key rows
     CUtensorMap k, v;
@@ -33,10 +34,11 @@ bool attn_tc_eligible(const Dims &d);
 size_t attn_tc_smem(const Dims &d);
 cudaError_t attn_tc_setup(const Dims &d, int max_smem);
 cudaError_t attn_tc_kv_maps(const Dims &d, const void *kc, const void *vc, int n_ctx, TcKVMaps &m);
-cudaError_t attn_tc_q_maps(const Dims &d, int P, const bf16 *q_hi, const bf16 *q_lo, CUtensorMap &mhi,
-                           CUtensorMap &mlo);
+// Map of a [P * NH][128] BF16 array of [token][head] rows in 128-row boxes.
+cudaError_t attn_tc_row_map(const Dims &d, int P, const bf16 *base, CUtensorMap &m);
 cudaError_t attn_prefill_tc(const Dims &d, const CUtensorMap &qhi, const CUtensorMap &qlo, const TcKVMaps &kv,
-                            bf16 *o_hi, bf16 *o_lo, int p0, int n, int *status, cudaStream_t st, int nsm);
+                            const CUtensorMap &ohi, const CUtensorMap &olo, int p0, int n, int *status,
+                            cudaStream_t st, int nsm);
 cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m);
 TcActPtrs tc_act_ptrs(const Dims &d, const PrefillBufs &pb);
 cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m);

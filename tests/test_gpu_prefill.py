@@ -22,14 +22,15 @@ SMALL_TC = synth.LAYER.with_(name="small_bf16_tc", n_layers=2, hidden=512, n_hea
                              expert_inter=128, vocab=1000, gain_sigma=0.1)
 
 
-# The tcgen05 attention (head_dim 128, 16 to 128 heads): 16 heads and a 40-key window
-# (8 tokens per 128-row block), and 64 heads with the full 128-key window.
-SMALL_TCA16 = SMALL_TC.with_(name="small_bf16_tc_attn16", n_heads=16, window=40)
+# The tcgen05 attention (head_dim 128, 64 or 128 heads): 128 heads (one token per
+# 128-row block) with a 40-key window, and 64 heads (two tokens a block) with the
+# full 128-key window.
+SMALL_TCA128 = SMALL_TC.with_(name="small_bf16_tc_attn128", n_heads=128, window=40)
 SMALL_TCA64 = SMALL_TC.with_(name="small_bf16_tc_attn64", n_heads=64, window=128)
 
 
-@pytest.fixture(scope="module", params=[SMALL, SMALL_TC, SMALL_TCA16, SMALL_TCA64],
-                ids=["simt", "tensor_core", "tensor_core_attn16", "tensor_core_attn64"])
+@pytest.fixture(scope="module", params=[SMALL, SMALL_TC, SMALL_TCA128, SMALL_TCA64],
+                ids=["simt", "tensor_core", "tensor_core_attn128", "tensor_core_attn64"])
 def small(request):
     import torch
     torch.cuda.init()
