@@ -276,12 +276,19 @@ def run_case(args):
     tw.fill_kv(shape, 0, k, v, n_pre)
     assert s.restore(synth.host_tokens(n_pre, shape.vocab, stream=11)) == 0
     toks = synth.host_tokens(args.warmup + args.steps, shape.vocab, stream=5)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            ev0.record(stream)
         assert s.decode_layers(int(toks[i])) == 0
+    ev1.record(stream)
     torch.cuda.synchronize()
     assert s.status() == 0
+    us = ev0.elapsed_time(ev1) * 1e3 / max(1, args.steps)
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup,
-                      "launches": int(s.launches)}), flush=True)
+                      "launches": int(s.launches), "us_per_step": us}), flush=True)
 
 
 # --------------------------------------------------------------------------- our arm

@@ -42,6 +42,8 @@ struct ds4g_session {
     unsigned *bar;              // grid-barrier arrival counter of the persistent kernel
     unsigned bar_count = 0;     // its value after every launch so far (host copy)
     unsigned kv_count = 0;      // K/V-row counter (bar[1]) after every launch so far
+    unsigned *qflag;            // [NH] per-head query-half flags of the persistent kernel
+    unsigned q_count = 0;       // their value after every launch so far
     int *status;                // device status word
     std::vector<void *> kv_host;
     uint64_t launches = 0;
@@ -137,6 +139,7 @@ Layout layout(const ds4g_config &c, int n_ctx)
     o += al((size_t)d.V * 4);                          // logits
     o += al(64);                                       // counters
     o += al(64);                                       // barrier + status
+    o += al((size_t)d.NH * 4);                         // per-head query-half flags
     o += al((size_t)d.L * sizeof(LayerPtrs));          // layer table
     o += al((size_t)2 * d.L * sizeof(void *));         // K/V pointer table
     o += al((size_t)(d.L + 1) * d.H * 4);              // prefill: last token entering each layer
@@ -292,6 +295,7 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     b.counters = (unsigned *)take(64);
     s->bar = (unsigned *)take(64);
     s->status = (int *)(s->bar + 4);
+    s->qflag = (unsigned *)take((size_t)d.NH * 4);
     b.status = s->status;
     s->layers_dev = (LayerPtrs *)take((size_t)d.L * sizeof(LayerPtrs));
     s->kv_dev = (void **)take((size_t)2 * d.L * sizeof(void *));
@@ -398,6 +402,9 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
         pa.bar = s->bar;
         pa.bar_base = s->bar_count;
         pa.kv_base = s->kv_count;
+        pa.qflag = s->qflag;
+        pa.q_base = s->q_count;
+        pa.split_q = 2 * d.NH + 2 <= s->m->nsm;
         pa.status = s->status;
         pa.trace = s->trace;
         pa.trace_events = s->trace_events;
@@ -406,6 +413,7 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
         // one before the lm_head; two K/V-row publications per layer
         s->bar_count += (unsigned)(6 * d.L - 1 + pa.logits) * (unsigned)s->m->nsm;
         s->kv_count += 2u * (unsigned)d.L;
+        if (pa.split_q) s->q_count += (unsigned)d.L;   // one query half per head and layer
         s->hist[s->len] = token;
         s->len += 1;
         return DS4G_OK;
@@ -539,9 +547,11 @@ int ds4g_session_status(ds4g_session *s)
     if (e) return DS4G_ECUDA;
     if (st != 0) {  // clear the flag and the barrier counter a failed wait left behind
         e = cudaMemsetAsync(s->bar, 0, 64, s->st);
+        if (!e) e = cudaMemsetAsync(s->qflag, 0, (size_t)s->m->d.NH * 4, s->st);
         if (!e) e = cudaStreamSynchronize(s->st);
         s->bar_count = 0;
         s->kv_count = 0;
+        s->q_count = 0;
         if (e) return DS4G_ECUDA;
         return st == DS4G_ENONFINITE ? DS4G_ENONFINITE : DS4G_ETIMEOUT;
     }

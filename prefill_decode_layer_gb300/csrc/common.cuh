@@ -71,6 +71,9 @@ struct PersistArgs {
     unsigned *bar;             // [0] grid-barrier arrivals, [1] K/V rows published (both only grow)
     unsigned bar_base;         // its value when this launch starts
     unsigned kv_base;          // value of the K/V-row counter (bar[1]) when this launch starts
+    unsigned *qflag;           // [NH] query halves published, per head (split queries; only grow)
+    unsigned q_base;           // value of every qflag entry when this launch starts
+    int split_q;               // each head's queries are computed by two CTAs (2 NH + 2 <= grid)
     int *status;               // DS4G_ETIMEOUT if a barrier wait gave up
     unsigned long long *trace; // optional [events][gridDim] stage start times (ns)
     int trace_events;

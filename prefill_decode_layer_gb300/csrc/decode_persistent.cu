@@ -140,16 +140,33 @@ template <typename TW> __device__ __forceinline__ Piece piece(const void *b, int
 // Stages 2-3 of a layer are one stage.  CTA h < NH computes the queries of head h
 // (its HD rows of W_qb) and attends for that head; CTA NH computes the new K row
 // (W_kb) and CTA NH+1 the new V row (W_vb), and they publish them through the kv
-// counter.  Other CTAs have no work in it.  kind: 0 head, 1 K, 2 V, -1 none.
-__device__ __forceinline__ int qkv_kind(int nh)
+// counter.  With split queries (2 NH + 2 CTAs or more), CTA h computes only the
+// first HD/2 query rows of head h and CTA NH+2+h the second half, which it writes
+// to global memory and publishes through the head's query flag; the work of a
+// head CTA before its attention halves.  Other CTAs have no work in it.
+// kind: 0 head, 1 K, 2 V, 3 second query half, -1 none.
+__device__ __forceinline__ int qkv_kind(int nh, int split)
 {
     const int c = blockIdx.x;
-    return c < nh ? 0 : (c == nh ? 1 : (c == nh + 1 ? 2 : -1));
+    if (c < nh) return 0;
+    if (c == nh) return 1;
+    if (c == nh + 1) return 2;
+    return split && c < 2 * nh + 2 ? 3 : -1;
 }
-template <typename TW> __device__ __forceinline__ Piece qkv_piece(const LayerPtrs &w, const Dims &d, int kind)
+// The head a kind-0 or kind-3 CTA serves, and the first query row it computes.
+__device__ __forceinline__ int qkv_head(int nh, int kind)
 {
-    if (kind == 0)
-        return piece<TW>(static_cast<const TW *>(w.wq_b) + (size_t)blockIdx.x * d.HD * d.RQ, d.HD, d.RQ);
+    return kind == 3 ? (int)blockIdx.x - nh - 2 : (int)blockIdx.x;
+}
+__device__ __forceinline__ int qkv_row0(const Dims &d, int kind) { return kind == 3 ? d.HD / 2 : 0; }
+template <typename TW>
+__device__ __forceinline__ Piece qkv_piece(const LayerPtrs &w, const Dims &d, int kind, int split)
+{
+    if (kind == 0 || kind == 3) {
+        const int h = qkv_head(d.NH, kind), rows = split ? d.HD / 2 : d.HD;
+        return piece<TW>(static_cast<const TW *>(w.wq_b) + ((size_t)h * d.HD + qkv_row0(d, kind)) * d.RQ, rows,
+                         d.RQ);
+    }
     return piece<TW>(kind == 1 ? w.wk_b : w.wv_b, d.HD, d.RKV);
 }
 
@@ -787,10 +804,11 @@ __device__ __forceinline__ void producer_warp(const PersistArgs &a, Shared &S, u
                 prefetch_l2(w.ffn_norm, H * 4);
             }
             const Piece P1[2] = {piece<TW>(w.wq_a, d.RQ, H), piece<TW>(w.wkv_a, d.RKV, H)};
-            const int kind = qkv_kind(d.NH);
+            const int kind = qkv_kind(d.NH, a.split_q);
             const Piece P4[1] = {piece<TW>(w.wo, H, d.QD)};
             const Piece P5[1] = {piece<TW>(w.w_router, d.E, H)};
-            ok = stream(P1) && (kind < 0 || stream_all(qkv_piece<TW>(w, d, kind))) && stream(P4) && stream(P5);
+            ok = stream(P1) && (kind < 0 || stream_all(qkv_piece<TW>(w, d, kind, a.split_q))) && stream(P4) &&
+                 stream(P5);
             for (int i = slo; ok && i < shi; ++i) ok = issue_gu(xp, -1, i);
         }
         // top-k once every CTA has written its router scores for this layer
@@ -956,14 +974,17 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
         // ---- stages 2-3: queries of one head + attention (head CTAs); K or V row (two CTAs)
         stamp(a, l * 7 + 1);
         {
-            const int kind = qkv_kind(d.NH);
+            const int kind = qkv_kind(d.NH, a.split_q);
+            const bool qk = kind == 0 || kind == 3;   // query rows
+            const int qh = qkv_head(d.NH, kind), qrow0 = qkv_row0(d, kind);
+            const float scale_q = rsqrtf((float)d.HD);
             float *qs = att;   // [HD] this head's queries after RoPE, times 1/sqrt(HD)
             if (kind >= 0) {
-                if (kind == 0) cload<TW>(a.b.c, xs, d.RQ, d.RQ);
+                if (qk) cload<TW>(a.b.c, xs, d.RQ, d.RQ);
                 else cload<TW>(a.b.c + d.RQ, xs + d.RQ, d.RKV, d.RKV);
                 csync();
-                const Piece P = qkv_piece<TW>(w, d, kind);
-                const float *x = kind == 0 ? xs : xs + d.RQ;
+                const Piece P = qkv_piece<TW>(w, d, kind, a.split_q);
+                const float *x = qk ? xs : xs + d.RQ;
                 const float2 *rope = a.rope + (size_t)a.pos * (d.HD / 2);
                 const float scale = rsqrtf((float)d.HD);
                 const int nch = chunks_of(P);
@@ -979,19 +1000,22 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                                  },
                                  [&]() {
                                      for (int q = lane; q < nr / 2; q += 32) {   // row pairs
-                                         const int row = row0 + 2 * q;          // within the head
+                                         const int row = qrow0 + row0 + 2 * q;  // within the head
                                          float e = res[2 * q], o = res[2 * q + 1];
-                                         if (kind < 2) {
+                                         if (kind != 2) {
                                              const float2 cs = rope[row / 2];
                                              const float re = e * cs.x - o * cs.y, ro = e * cs.y + o * cs.x;
                                              e = re;
                                              o = ro;
                                          }
-                                         if (kind == 0) {
-                                             qs[row] = e * scale;
-                                             qs[row + 1] = o * scale;
-                                             a.b.q[(size_t)blockIdx.x * d.HD + row] = e;   // for inspection
-                                             a.b.q[(size_t)blockIdx.x * d.HD + row + 1] = o;
+                                         if (qk) {
+                                             if (kind == 0) {
+                                                 qs[row] = e * scale;
+                                                 qs[row + 1] = o * scale;
+                                             }
+                                             // for inspection, and the second half's way to its head CTA
+                                             a.b.q[(size_t)qh * d.HD + row] = e;
+                                             a.b.q[(size_t)qh * d.HD + row + 1] = o;
                                          } else {
                                              TKV *dst = (kind == 1 ? kc : vc) + (size_t)a.pos * d.HD;
                                              dst[row] = from_f32<TKV>(e);
@@ -1002,9 +1026,12 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                         return;
                 }
                 csync();
-                if (kind > 0 && threadIdx.x == 0) {   // publish the new K or V row
-                    __threadfence();
-                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.bar + 1) : "memory");
+                // publish the new K or V row, or the query half: the release (as in grid_sync)
+                // covers the CTA's writes, ordered before it by the named barrier above; a full
+                // fence here would also wait for the producer's copies in flight
+                if (kind > 0 && threadIdx.x == 0) {
+                    unsigned *ctr = kind == 3 ? a.qflag + qh : a.bar + 1;
+                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
                 }
             }
             stamp(a, l * 7 + 2);
@@ -1023,7 +1050,8 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                 }
             }
             if (kind == 0) {
-                // waits for this position's K and V rows (two arrivals per layer)
+                // waits for this position's K and V rows (two arrivals per layer) and, with
+                // split queries, for the second half of this head's queries
                 auto kv_wait = [&]() -> bool {
                     if (threadIdx.x == 0) {
                         const unsigned want = a.kv_base + 2u * (unsigned)(l + 1);
@@ -1035,9 +1063,23 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                                 break;
                             }
                         }
+                        const unsigned qwant = a.q_base + (unsigned)(l + 1);
+                        while (a.split_q && *ab == 0 && (int)(ld_acquire_gpu(a.qflag + qh) - qwant) < 0) {
+                            if (clock64() - t0 > kWaitCycles) {
+                                atomicExch(a.status, DS4G_ETIMEOUT);
+                                S.abort_flag = 1;
+                                break;
+                            }
+                        }
                     }
                     csync();
-                    return *ab == 0;
+                    if (*ab) return false;
+                    if (a.split_q) {
+                        for (int i = threadIdx.x; i < d.HD / 2; i += kCT)
+                            qs[d.HD / 2 + i] = __ldcg(a.b.q + (size_t)qh * d.HD + d.HD / 2 + i) * scale_q;
+                        csync();
+                    }
+                    return true;
                 };
                 if (!attention_head<TKV>(a, blockIdx.x, kc + (size_t)lo_w * d.HD, vc + (size_t)lo_w * d.HD,
                                          a.pos - lo_w + 1, att, S.red, kv_wait))
