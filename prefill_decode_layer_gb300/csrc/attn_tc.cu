@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kTaThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();   // programmatic launch: the queries and K/V rows are complete past this point
+    pdl_trigger();
     const uint32_t tmem = *tslot;
     volatile int *ab = abort_flag;
     auto give_up = [&]() {
@@ -440,10 +442,8 @@ cudaError_t attn_prefill_tc(const Dims &d, const CUtensorMap &qhi, const CUtenso
     if (nblk <= 0) return cudaSuccess;
     const int KR = ta_key_rows(d.W, d.NH);
     const int grid = nblk < nsm ? nblk : nsm;
-    k_attn_prefill_tc<<<grid, kTaThreads, attn_tc_smem(d), st>>>(qhi, qlo, kv.k, kv.v, ohi, olo, p0, n, d.NH, d.W,
-                                                                 KR, status);
-    ++launch_count();
-    return cudaGetLastError();
+    return launch_pdl(k_attn_prefill_tc, dim3(grid), dim3(kTaThreads), attn_tc_smem(d), st, qhi, qlo, kv.k, kv.v, ohi,
+                      olo, p0, n, (int)d.NH, (int)d.W, KR, status);
 }
 
 }  // namespace ds4g

@@ -26,6 +26,8 @@ namespace ds4g {
 
 __global__ void k_embed_rows(const uint16_t *table, const int *tok, float *X, int H)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     const int t = blockIdx.x;
     const __half *row = reinterpret_cast<const __half *>(table) + (size_t)tok[t] * H;
     for (int i = threadIdx.x; i < H; i += blockDim.x) X[(size_t)t * H + i] = __half2float(row[i]);
@@ -55,6 +57,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *X, const floa
 // over the selected scores.  One warp per token.
 __global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E, int K, int *status)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= n) return;
     float sel[8];
@@ -77,6 +81,8 @@ __global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E
 // the ids.  Pass 1: per-segment histograms (shared-memory atomics).
 __global__ void __launch_bounds__(256) k_group_hist(const int *ids, int nent, int E, int *segcnt)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     extern __shared__ int hist[];
     const int seg = blockIdx.x, i0 = seg * kSortSeg, i1 = min(nent, i0 + kSortSeg);
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -124,6 +130,8 @@ __device__ int block_exclusive_scan(int v, int *tmp, int &total)
 __global__ void __launch_bounds__(1024) k_group_offsets(int *segcnt, int nseg, int E, int bm, int *cnt, int *off,
                                                         int *tiles)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     __shared__ int tmp[32];
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
@@ -174,6 +182,8 @@ __global__ void __launch_bounds__(1024) k_group_offsets(int *segcnt, int nseg, i
 __global__ void __launch_bounds__(32) k_group_place(const int *ids, int nent, int E, const int *segcnt,
                                                     const int *off, int *rows)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     extern __shared__ int base[];
     const int seg = blockIdx.x, lane = threadIdx.x;
     const int i0 = seg * kSortSeg, i1 = min(nent, i0 + kSortSeg);
@@ -206,14 +216,14 @@ cudaError_t group_by_expert(const PrefillBufs &pb, int nent, int E, int bm, cuda
         return cudaMemsetAsync(pb.off, 0, (size_t)(E + 1) * sizeof(int), st);
     }
     const size_t sh = (size_t)E * sizeof(int);
-    k_group_hist<<<nseg, 256, sh, st>>>(pb.ids, nent, E, pb.segcnt);
-    ++launch_count();
+    cudaError_t e = launch_pdl(k_group_hist, dim3(nseg), dim3(256), sh, st, (const int *)pb.ids, nent, E, pb.segcnt);
     const int thr = E >= 1024 ? 1024 : ((E + 31) / 32) * 32;
-    k_group_offsets<<<1, thr, 0, st>>>(pb.segcnt, nseg, E, bm, pb.cnt, pb.off, pb.tiles);
-    ++launch_count();
-    k_group_place<<<nseg, 32, sh, st>>>(pb.ids, nent, E, pb.segcnt, pb.off, pb.rows);
-    ++launch_count();
-    return cudaGetLastError();
+    if (!e)
+        e = launch_pdl(k_group_offsets, dim3(1), dim3(thr), 0, st, pb.segcnt, nseg, E, bm, pb.cnt, pb.off, pb.tiles);
+    if (!e)
+        e = launch_pdl(k_group_place, dim3(nseg), dim3(32), sh, st, (const int *)pb.ids, nent, E,
+                       (const int *)pb.segcnt, (const int *)pb.off, pb.rows);
+    return e;
 }
 
 // Windowed causal multi-query attention for a chunk: CTA (token t, group of heads).

@@ -26,6 +26,8 @@ namespace ds4g {
 __global__ void __launch_bounds__(1024) k_rmsnorm_hilo(const float *X, const float *g, bf16 *hi, bf16 *lo,
                                                        int H, float eps)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     __shared__ float red[32];
     const int t = blockIdx.x, nv = H / 4;
     const float4 *x = reinterpret_cast<const float4 *>(X + (size_t)t * H);
@@ -59,6 +61,8 @@ static int rmsnorm_threads(int H) { return H / 4 < 1024 ? ((H / 4 + 31) / 32) * 
 __global__ void __launch_bounds__(256) k_gather_rows(const bf16 *hi, const bf16 *lo, const int *rows, int K,
                                                      int nent, int H, bf16 *ghi, bf16 *glo)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     const int r = blockIdx.x;
     if (r >= nent) return;
     const size_t src = (size_t)(rows[r] / K) * H, dst = (size_t)r * H;
@@ -130,6 +134,8 @@ __global__ void __launch_bounds__(256) k_attn_prefill_mma(const float *Q, bf16 *
                                                           const bf16 *kc, const bf16 *vc, int p0, int n,
                                                           Dims d)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char sm_attn[];
     const int W = d.W, NH = d.NH, QD = d.QD;
     const int t0 = blockIdx.x * kAttnTB;
@@ -385,7 +391,8 @@ struct EpiAddX {   // residual: X[m][n..n+3] += v
     __device__ Aux load4(int m, int n, int) const { return *reinterpret_cast<const float4 *>(X + (size_t)m * H + n); }
     __device__ void store4(int m, int n, const float (&v)[4], const Aux &x, int) const
     {
-        *reinterpret_cast<float4 *>(X + (size_t)m * H + n) = make_float4(x.x + v[0], x.y + v[1], x.z + v[2], x.w + v[3]);
+        *reinterpret_cast<float4 *>(X + (size_t)m * H + n) =
+            make_float4(x.x + v[0], x.y + v[1], x.z + v[2], x.w + v[3]);
     }
 };
 
@@ -440,6 +447,8 @@ struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16, 16-by
 // outputs, after the shared expert's down projection was added by its GEMM.
 __global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, const float *wts, int H, int K)
 {
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
     const int t = blockIdx.x;
     float w[8];
 #pragma unroll
@@ -551,9 +560,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
     const TcActPtrs ap = tc_act_ptrs(d, pb);
     const int ny = (n + tc::BT - 1) / tc::BT;
     const int max_tiles = nent / tc::BT + d.E + 1;
-    k_embed_rows<<<n, 256, 0, st>>>(tok_embd, pb.tok, pb.X, H);
-    ++launch_count();
-    if ((e = cudaGetLastError())) return e;
+    if ((e = launch_pdl(k_embed_rows, dim3(n), dim3(256), 0, st, tok_embd, (const int *)pb.tok, pb.X, H))) return e;
     for (int l = 0; l <= d.L; ++l) {
         if (pb.rec_row >= 0 && pb.layer_x &&
             (e = cudaMemcpyAsync(pb.layer_x + (size_t)l * H, pb.X + (size_t)pb.rec_row * H, (size_t)H * 4,
@@ -567,8 +574,9 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         a.status = pb.status;
         a.m_tok = n;
         // ---- attention half
-        k_rmsnorm_hilo<<<n, rmsnorm_threads(H), 0, st>>>(pb.X, w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
-        ++launch_count();
+        if ((e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
+                            (const float *)w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
+            return e;
         a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ, a.x_col0 = 0;
         if ((e = tc::launch<false>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a, EpiHiLo{ap.c_hi, ap.c_lo, d.RQ + d.RKV},
                                    ny, nsm, st)))
@@ -608,16 +616,19 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         if ((e = tc::launch<false>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
         // ---- MoE half
-        k_rmsnorm_hilo<<<n, rmsnorm_threads(H), 0, st>>>(pb.X, w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps);
-        ++launch_count();
+        if ((e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
+                            (const float *)w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
+            return e;
         a.n_out = d.E, a.k = H;
         if ((e = tc::launch<false>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, ny, nsm, st)))
             return e;
-        k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K, pb.status);
-        ++launch_count();
+        if ((e = launch_pdl(k_router_topk, dim3((n * 32 + 255) / 256), dim3(256), 0, st, (const float *)pb.S, pb.ids,
+                            pb.wts, n, d.E, K, pb.status)))
+            return e;
         if ((e = group_by_expert(pb, nent, d.E, tc::BT, st))) return e;
-        k_gather_rows<<<nent, 256, 0, st>>>(ap.xn_hi, ap.xn_lo, pb.rows, K, nent, H, ap.xg_hi, ap.xg_lo);
-        ++launch_count();
+        if ((e = launch_pdl(k_gather_rows, dim3(nent), dim3(256), 0, st, (const bf16 *)ap.xn_hi, (const bf16 *)ap.xn_lo,
+                            (const int *)pb.rows, K, nent, H, ap.xg_hi, ap.xg_lo)))
+            return e;
         if ((e = cudaGetLastError())) return e;
         // routed gate/up + SwiGLU (grouped), then the shared expert's
         tc::Args g{};
@@ -639,8 +650,9 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         a.n_out = H, a.k = I;
         if ((e = tc::launch<false>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
-        k_moe_combine<<<n, 256, 0, st>>>(pb.X, pb.YS, pb.wts, H, K);
-        ++launch_count();
+        if ((e = launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, st, pb.X, (const float *)pb.YS,
+                            (const float *)pb.wts, H, K)))
+            return e;
     }
     return cudaGetLastError();
 }

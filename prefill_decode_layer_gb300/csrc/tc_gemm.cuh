@@ -165,6 +165,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // with a programmatic launch the set-up above overlaps the previous kernel's tail;
+    // its outputs (this GEMM's inputs) are complete past this point
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = *tslot;
     volatile int *ab = abort_flag;
     auto give_up = [&]() {
@@ -376,9 +380,8 @@ static cudaError_t launch_wn(const CUtensorMap &w0, const CUtensorMap &w1, const
         attr_set = true;
     }
     const int grid = (int)(work < nsm ? work : nsm);
-    k_tc_gemm<Epi, GU, WN><<<grid, THREADS, Geo<GU, WN>::SMEM, st>>>(w0, w1, xhi, xlo, a, epi);
-    ++launch_count();
-    return cudaGetLastError();
+    return launch_pdl(k_tc_gemm<Epi, GU, WN>, dim3(grid), dim3(THREADS), Geo<GU, WN>::SMEM, st, w0, w1, xhi, xlo, a,
+                      epi);
 }
 
 // ntile_bound: token tiles at most (dense: exact; grouped: the tile list's bound).
