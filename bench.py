@@ -364,7 +364,19 @@ def main():
     torch.cuda.synchronize()
 
     def timed_steps(first, n, flush_l2):
-        # per-step CUDA events on the session's (current) stream; returns total ms
+        # CUDA events on the session's (current) stream; returns total ms.  Steps run back
+        # to back between one pair of events; with an L2 flush before every step, each
+        # step has its own pair so that the flushes stay outside the timed time.
+        if not flush_l2:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(n):
+                rc = sess.decode_layers(int(toks[first + i]))
+                if rc != 0:
+                    raise RuntimeError(f"decode failed: {rc}")
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n)]
         for i in range(n):
@@ -425,7 +437,7 @@ def main():
                 "frac": round(achieved / hbm_peak, 4),
                 "peak_source": f"{peak_src} hbm_gbs (copy, read+write; burst)",
                 "traffic": ncu_traffic("k_decode_persistent"), "algorithmic_bytes": step_bytes,
-                "timing": "CUDA events around each launch, steps back to back"}
+                "timing": "CUDA events around the timed steps (back to back), average per launch"}
     staged = {"note": "one kernel per stage (decode_kernel=1), per-kernel CUDA events, "
                       "L2 flushed between steps", "per_kernel": per_kernel}
 
