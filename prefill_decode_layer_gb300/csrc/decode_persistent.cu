@@ -843,7 +843,10 @@ __device__ __forceinline__ void producer_warp(const PersistArgs &a, Shared &S, u
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 if (k < K) {
-                    S.ids[k] = ids[k];
+                    // an id always indexes a real expert: copy addresses are built from it
+                    const bool valid = (unsigned)ids[k] < (unsigned)d.E;
+                    if (!valid) atomicCAS(a.status, 0, DS4G_ENONFINITE);
+                    S.ids[k] = valid ? ids[k] : 0;
                     S.w[k] = wv[k] / sum;
                     if (blockIdx.x == 0) {
                         a.b.ids[l * K + k] = ids[k];
