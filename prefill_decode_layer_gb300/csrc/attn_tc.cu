@@ -11,13 +11,14 @@
 // windows, staged once.  Per block:
 //   S = (Qhi + Qlo) K^T      M 128 rows x N keys (<= KR) x K 128 dims, hi and lo
 //                            query tiles into one FP32 accumulator in TMEM;
-//   softmax                  one thread per row reads its S row from TMEM, masks it
-//                            to the token's window, and writes P = exp(scale (S -
-//                            max)) as BF16 hi/lo rows into shared memory (the row
-//                            sum stays FP32 in a register);
+//   softmax                  the warps of a row read its S from TMEM, mask it to
+//                            the token's window, and write P = exp(scale (S - max))
+//                            as BF16 hi/lo rows into shared memory (the row sum
+//                            stays FP32);
 //   O = (Phi + Plo) V        M 128 x N 128 dims x K keys, V read MN-major (its rows
 //                            are keys) straight from the TMA tile;
-//   out                      O / sum as BF16 hi/lo rows (the W_o GEMM's input).
+//   out                      O / sum as BF16 hi/lo rows (the W_o GEMM's input),
+//                            staged in shared memory and written by TMA stores.
 // Keys are staged from an absolute position that is a multiple of 16 and every
 // reduction runs over absolute 16-key steps (keys outside a row's window add exact
 // zeros), so a token's result does not depend on how the prompt was cut into
