@@ -155,6 +155,20 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- helpers
 
+def replica_rate(local_ms: float, units: int, dist=None, device: str = "cuda"):
+    """Whole-job rate of N independent replicas (no data-path collective): every rank
+    processed `units` in its own `local_ms`; the slowest rank bounds the job, so the
+    value is N * units over the maximum time.  Returns (max ms, units per second)."""
+    world, total = 1, float(local_ms)
+    if dist is not None:
+        import torch
+        t = torch.tensor([total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+        world = dist.get_world_size()
+    return total, world * units / (total / 1000.0)
+
+
 def nproc():
     try:
         return len(os.sched_getaffinity(0))
@@ -401,11 +415,7 @@ def main():
     barrier()
     clk = clocks.stop()
     gpu_launches = sess.launches - launches0
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * args.steps / (total_ms / 1000.0)
+    total_ms, value = replica_rate(total_ms, args.steps, dist)
     ms_per_step = total_ms / args.steps
     # Secondary: the same with a 512 MB L2 flush before every step (cold code and data).
     fl_ms = timed_steps(args.warmup + args.steps, n_flushed, True) / n_flushed
