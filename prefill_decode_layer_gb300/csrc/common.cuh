@@ -147,6 +147,19 @@ __device__ __forceinline__ bool topk_better(float va, int ia, float vb, int ib)
 {
     return va > vb || (va == vb && ia < ib);
 }
+// One comparator of the sorting network: the better of entries I and J ends at I.
+// (Template indices keep both arrays in registers; indices read from a table
+// put them in local memory.)
+template <int I, int J> __device__ __forceinline__ void topk_cswap(float (&v)[8], int (&id)[8])
+{
+    const bool sw = topk_better(v[J], id[J], v[I], id[I]);
+    const float vi = v[I], vj = v[J];
+    const int ii = id[I], ij = id[J];
+    v[I] = sw ? vj : vi;
+    v[J] = sw ? vi : vj;
+    id[I] = sw ? ij : ii;
+    id[J] = sw ? ii : ij;
+}
 __device__ __forceinline__ bool warp_topk(const float *s, int E, int K, float *sel, int *ids, int lane)
 {
     bool finite = true;
@@ -160,17 +173,13 @@ __device__ __forceinline__ bool warp_topk(const float *s, int E, int K, float *s
             v[u] = x != x ? -INFINITY : x;
             id[u] = e < E ? e : 0x7fffffff;   // padding: loses every tie to a real expert
         }
-        constexpr int net[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
-                                    {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
-                                    {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
-#pragma unroll
-        for (int c = 0; c < 19; ++c) {
-            const int i = net[c][0], j = net[c][1];
-            if (topk_better(v[j], id[j], v[i], id[i])) {
-                const float tv = v[i]; v[i] = v[j]; v[j] = tv;
-                const int ti = id[i]; id[i] = id[j]; id[j] = ti;
-            }
-        }
+        topk_cswap<0, 2>(v, id); topk_cswap<1, 3>(v, id); topk_cswap<4, 6>(v, id);
+        topk_cswap<5, 7>(v, id); topk_cswap<0, 4>(v, id); topk_cswap<1, 5>(v, id);
+        topk_cswap<2, 6>(v, id); topk_cswap<3, 7>(v, id); topk_cswap<0, 1>(v, id);
+        topk_cswap<2, 3>(v, id); topk_cswap<4, 5>(v, id); topk_cswap<6, 7>(v, id);
+        topk_cswap<2, 4>(v, id); topk_cswap<3, 5>(v, id); topk_cswap<1, 4>(v, id);
+        topk_cswap<3, 6>(v, id); topk_cswap<1, 2>(v, id); topk_cswap<3, 4>(v, id);
+        topk_cswap<5, 6>(v, id);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {   // K <= 8
             if (k >= K) break;
@@ -216,6 +225,71 @@ __device__ __forceinline__ bool warp_topk(const float *s, int E, int K, float *s
         ids[k] = bi;
         if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         finite = finite && isfinite(bv);
+    }
+    return finite;
+}
+
+// Order-preserving 32-bit key of a score: for non-NaN floats a, b (with -0 taken
+// as +0), a > b exactly when key(a) > key(b), and a == b when the keys are equal.
+__device__ __forceinline__ unsigned topk_key(float v)
+{
+    const unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float topk_unkey(unsigned k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+template <int I, int J> __device__ __forceinline__ void topk_cswap_key(unsigned (&k)[8], int (&id)[8])
+{
+    const bool sw = k[J] > k[I] || (k[J] == k[I] && id[J] < id[I]);
+    const unsigned ki = k[I], kj = k[J];
+    const int ii = id[I], ij = id[J];
+    k[I] = sw ? kj : ki;
+    k[J] = sw ? ki : kj;
+    id[I] = sw ? ij : ii;
+    id[J] = sw ? ii : ij;
+}
+// The same selection as warp_topk for E <= 256, from registers: lane l passes the
+// scores of experts l, l+32, ... in x[0..8).  Each of the K rounds is two warp
+// reductions (redux.sync): the largest head key, then the lowest id among the
+// lanes holding it; the warp-wide shuffle butterfly of warp_topk takes five
+// dependent exchange steps per round instead.
+__device__ __forceinline__ bool warp_topk_r256(const float (&x)[8], int E, int K, float *sel, int *ids,
+                                               int lane)
+{
+    unsigned k8[8];
+    int id[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int e = lane + 32 * u;
+        const float v = e < E ? x[u] : -INFINITY;
+        k8[u] = topk_key(v != v ? -INFINITY : v);
+        id[u] = e < E ? e : 0x7fffffff;   // padding: loses every tie to a real expert
+    }
+    topk_cswap_key<0, 2>(k8, id); topk_cswap_key<1, 3>(k8, id); topk_cswap_key<4, 6>(k8, id);
+    topk_cswap_key<5, 7>(k8, id); topk_cswap_key<0, 4>(k8, id); topk_cswap_key<1, 5>(k8, id);
+    topk_cswap_key<2, 6>(k8, id); topk_cswap_key<3, 7>(k8, id); topk_cswap_key<0, 1>(k8, id);
+    topk_cswap_key<2, 3>(k8, id); topk_cswap_key<4, 5>(k8, id); topk_cswap_key<6, 7>(k8, id);
+    topk_cswap_key<2, 4>(k8, id); topk_cswap_key<3, 5>(k8, id); topk_cswap_key<1, 4>(k8, id);
+    topk_cswap_key<3, 6>(k8, id); topk_cswap_key<1, 2>(k8, id); topk_cswap_key<3, 4>(k8, id);
+    topk_cswap_key<5, 6>(k8, id);
+    bool finite = true;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {   // K <= 8
+        if (k >= K) break;
+        const unsigned m = __reduce_max_sync(0xffffffffu, k8[0]);
+        const unsigned bi = __reduce_min_sync(0xffffffffu, k8[0] == m ? (unsigned)id[0] : 0x7fffffffu);
+        const float bv = topk_unkey(m);
+        sel[k] = bv;
+        ids[k] = (int)bi;
+        finite = finite && isfinite(bv);
+        if (k8[0] == m && (unsigned)id[0] == bi) {   // this lane's head was taken
+#pragma unroll
+            for (int u = 0; u < 7; ++u) { k8[u] = k8[u + 1]; id[u] = id[u + 1]; }
+            k8[7] = topk_key(-INFINITY);
+            id[7] = 0x7fffffff;
+        }
     }
     return finite;
 }

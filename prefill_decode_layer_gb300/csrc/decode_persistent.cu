@@ -814,45 +814,67 @@ __device__ __forceinline__ void producer_warp(const PersistArgs &a, Shared &S, u
         // top-k once every CTA has written its router scores for this layer
         bool go = __shfl_sync(0xffffffffu, ok, 0) && mbar_wait(&S.scores_ready, (unsigned)l & 1u, ab);
         if (!__all_sync(0xffffffffu, go)) { ok = false; break; }
-        for (int e0 = 0; e0 < d.E; e0 += 256) {   // eight loads in flight per lane
+        float sel[8] = {};
+        int ids[8] = {};
+        bool finite;
+        if (d.E <= 256) {   // lane l: experts l, l + 32, ... straight from the loads
             float v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int e = e0 + lane + 32 * u;
+                const int e = lane + 32 * u;
                 v[u] = e < d.E ? __ldcg(a.b.scores + e) : 0.f;
             }
+            finite = warp_topk_r256(v, d.E, K, sel, ids, lane);
+        } else {
+            for (int e0 = 0; e0 < d.E; e0 += 256) {   // eight loads in flight per lane
+                float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = e0 + lane + 32 * u;
-                if (e < d.E) sc[e] = v[u];
+                for (int u = 0; u < 8; ++u) {
+                    const int e = e0 + lane + 32 * u;
+                    v[u] = e < d.E ? __ldcg(a.b.scores + e) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = e0 + lane + 32 * u;
+                    if (e < d.E) sc[e] = v[u];
+                }
             }
+            __syncwarp();
+            finite = warp_topk(sc, d.E, K, sel, ids, lane);
         }
-        __syncwarp();
-        float sel[8];
-        int ids[8];
-        const bool finite = warp_topk(sc, d.E, K, sel, ids, lane);
+        // Gate weights, softmax over the selected scores: lane k < K takes the k-th
+        // selected expert; every lane sums the K terms in selection order.
+        {
+            float mys = sel[0];
+            int myid = ids[0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k)
+                if (lane == k) {
+                    mys = sel[k];
+                    myid = ids[k];
+                }
+            const float wv = expf(mys - sel[0]);
+            float sum = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, wv, k);
+                if (k < K) sum += wk;
+            }
+            if (lane < K) {
+                // an id always indexes a real expert: copy addresses are built from it
+                const bool valid = (unsigned)myid < (unsigned)d.E;
+                if (!valid) atomicCAS(a.status, 0, DS4G_ENONFINITE);
+                S.ids[lane] = valid ? myid : 0;
+                S.w[lane] = wv / sum;
+                if (blockIdx.x == 0) {
+                    a.b.ids[l * K + lane] = myid;
+                    a.b.wts[l * K + lane] = wv / sum;
+                }
+            }
+            __syncwarp();
+        }
         if (lane == 0) {
             if (!finite) atomicCAS(a.status, 0, DS4G_ENONFINITE);
-            float sum = 0.f, wv[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < K) {
-                    wv[k] = expf(sel[k] - sel[0]);
-                    sum += wv[k];
-                }
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < K) {
-                    // an id always indexes a real expert: copy addresses are built from it
-                    const bool valid = (unsigned)ids[k] < (unsigned)d.E;
-                    if (!valid) atomicCAS(a.status, 0, DS4G_ENONFINITE);
-                    S.ids[k] = valid ? ids[k] : 0;
-                    S.w[k] = wv[k] / sum;
-                    if (blockIdx.x == 0) {
-                        a.b.ids[l * K + k] = ids[k];
-                        a.b.wts[l * K + k] = wv[k] / sum;
-                    }
-                }
             S.w[K] = 1.f;
             mbar_arrive(&S.ids_ready);   // consumers start stage 6; the combine reads S.w
             int lo, hi;
