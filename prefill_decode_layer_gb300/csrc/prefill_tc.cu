@@ -57,22 +57,6 @@ __global__ void __launch_bounds__(1024) k_rmsnorm_hilo(const float *X, const flo
 }
 static int rmsnorm_threads(int H) { return H / 4 < 1024 ? ((H / 4 + 31) / 32) * 32 : 1024; }
 
-// Grouped copy of the MoE input: row r <- token rows[r] / K (16-byte chunks).
-__global__ void __launch_bounds__(256) k_gather_rows(const bf16 *hi, const bf16 *lo, const int *rows, int K,
-                                                     int nent, int H, bf16 *ghi, bf16 *glo)
-{
-    pdl_wait();      // inputs of the previous kernel (programmatic launch)
-    pdl_trigger();
-    const int r = blockIdx.x;
-    if (r >= nent) return;
-    const size_t src = (size_t)(rows[r] / K) * H, dst = (size_t)r * H;
-    const int nv = H / 8;
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-        reinterpret_cast<uint4 *>(ghi + dst)[v] = reinterpret_cast<const uint4 *>(hi + src)[v];
-        reinterpret_cast<uint4 *>(glo + dst)[v] = reinterpret_cast<const uint4 *>(lo + src)[v];
-    }
-}
-
 // ------------------------------------------------------------------ attention on the tensor cores
 //
 // Windowed causal MQA for a chunk with warp-level BF16 MMAs (m16n8k16, FP32
@@ -511,8 +495,6 @@ TcActPtrs tc_act_ptrs(const Dims &d, const PrefillBufs &pb)
     a.c_lo = a.c_hi + P * RC;
     a.o_hi = (bf16 *)pb.O;
     a.o_lo = a.o_hi + P * d.QD;
-    a.xg_hi = (bf16 *)pb.YS;   // dead once the routed gate/up GEMM has run
-    a.xg_lo = a.xg_hi + PK * d.H;
     a.hg_hi = (bf16 *)pb.HG;
     a.hg_lo = a.hg_hi + PK * d.I;
     a.hs_hi = (bf16 *)pb.HS;
@@ -532,8 +514,6 @@ cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m)
     if ((e = make_map_bf16(&m.c_lo, a.c_lo, P, RC, RC, tc::BT))) return e;
     if ((e = make_map_bf16(&m.o_hi, a.o_hi, P, d.QD, d.QD, tc::BT))) return e;
     if ((e = make_map_bf16(&m.o_lo, a.o_lo, P, d.QD, d.QD, tc::BT))) return e;
-    if ((e = make_map_bf16(&m.xg_hi, a.xg_hi, PK, d.H, d.H, tc::BT))) return e;
-    if ((e = make_map_bf16(&m.xg_lo, a.xg_lo, PK, d.H, d.H, tc::BT))) return e;
     if ((e = make_map_bf16(&m.hg_hi, a.hg_hi, PK, d.I, d.I, tc::BT))) return e;
     if ((e = make_map_bf16(&m.hg_lo, a.hg_lo, PK, d.I, d.I, tc::BT))) return e;
     if ((e = make_map_bf16(&m.hs_hi, a.hs_hi, P, d.I, d.I, tc::BT))) return e;
@@ -626,17 +606,16 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
                             pb.wts, n, d.E, K, pb.status)))
             return e;
         if ((e = group_by_expert(pb, nent, d.E, tc::BT, st))) return e;
-        if ((e = launch_pdl(k_gather_rows, dim3(nent), dim3(256), 0, st, (const bf16 *)ap.xn_hi, (const bf16 *)ap.xn_lo,
-                            (const int *)pb.rows, K, nent, H, ap.xg_hi, ap.xg_lo)))
-            return e;
-        if ((e = cudaGetLastError())) return e;
-        // routed gate/up + SwiGLU (grouped), then the shared expert's
+        // routed gate/up + SwiGLU (grouped; the GEMM gathers each group's token rows of
+        // the normalised input itself), then the shared expert's
         tc::Args g{};
         g.status = pb.status;
         g.n_out = I, g.k = H, g.tiles = pb.tiles, g.off = pb.off;
-        if ((e = tc::launch<true>(m.wg, m.wu, am.xg_hi, am.xg_lo, g, EpiSwiGLU{ap.hg_hi, ap.hg_lo, I}, max_tiles,
+        g.grow = pb.rows, g.gdiv = K, g.gx_hi = ap.xn_hi, g.gx_lo = ap.xn_lo, g.gld = H;
+        if ((e = tc::launch<true>(m.wg, m.wu, am.xn_hi, am.xn_lo, g, EpiSwiGLU{ap.hg_hi, ap.hg_lo, I}, max_tiles,
                                   nsm, st)))
             return e;
+        g.grow = nullptr;
         a.n_out = I, a.k = H;
         if ((e = tc::launch<true>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, ap.hs_lo, I}, ny, nsm,
                                   st)))

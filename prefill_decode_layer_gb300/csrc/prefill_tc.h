@@ -12,10 +12,10 @@ struct TcLayerMaps {   // boxes: 64 columns x 128 rows
     CUtensorMap wqa, wkva, wqb, wkb, wvb, wo, wr, wsg, wsu, wsd, wg, wu, wd;
 };
 struct TcActPtrs {     // hi/lo BF16 halves of the prefill activation buffers
-    bf16 *xn_hi, *xn_lo, *c_hi, *c_lo, *o_hi, *o_lo, *xg_hi, *xg_lo, *hg_hi, *hg_lo, *hs_hi, *hs_lo;
+    bf16 *xn_hi, *xn_lo, *c_hi, *c_lo, *o_hi, *o_lo, *hg_hi, *hg_lo, *hs_hi, *hs_lo;
 };
 struct TcActMaps {     // boxes: 64 columns x 128 token rows (q, oa: x 128 [token][head] rows)
-    CUtensorMap xn_hi, xn_lo, c_hi, c_lo, o_hi, o_lo, xg_hi, xg_lo, hg_hi, hg_lo, hs_hi, hs_lo, q_hi, q_lo, oa_hi,
+    CUtensorMap xn_hi, xn_lo, c_hi, c_lo, o_hi, o_lo, hg_hi, hg_lo, hs_hi, hs_lo, q_hi, q_lo, oa_hi,
         oa_lo;
 };
 struct TcKVMaps {      // one layer's K and V cache, boxes: 64 dims x the attention's staged key rows

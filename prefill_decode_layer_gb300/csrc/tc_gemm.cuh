@@ -54,6 +54,8 @@ static constexpr int BT = 128;      // tokens per tile (MMA M)
 static constexpr int BK = 64;       // K per stage: one 128-byte swizzle row of BF16
 static constexpr int BOXW = 128;    // weight rows per TMA box
 static constexpr int THREADS = 320;   // producer warp, MMA warp, 8 epilogue warps
+static constexpr int GWARPS = 2;      // token-row gather warps (grouped GEMMs that gather)
+static constexpr int THREADS_GA = THREADS + 32 * GWARPS;
 static constexpr uint32_t TILE_X = BT * BK * 2;              // 16 KB
 static constexpr uint32_t BOX_BYTES = BOXW * BK * 2;         // 16 KB
 static constexpr int CH = 32;                                // features per epilogue chunk
@@ -86,7 +88,19 @@ struct Args {
     const int *tiles; // grouped: [0] = count, then (expert, first row) pairs
     const int *off;   // grouped: expert row offsets [E + 1]
     int *status;      // DS4G_ETIMEOUT on a wait that gave up
+    // gathering launches: grouped row r reads activation row grow[r] / gdiv of the
+    // row-major BF16 arrays gx_hi, gx_lo (row stride gld elements)
+    const int *grow;
+    int gdiv;
+    const bf16 *gx_hi, *gx_lo;
+    int gld;
 };
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 struct NoAux {};
 
@@ -108,8 +122,10 @@ __device__ __forceinline__ float4 staged(const float *wstg, int t, int g)
 // the epilogue calls Epi::store_row(m, i0, h[32], e) with h = silu(gate) * up of
 // features i0 .. i0 + 31 of token m.  Otherwise Epi provides  Aux load4(m, n, e)
 // and  store4(m, n, v[4], aux, e).
-template <class Epi, bool GU, int WN>
-__global__ void __launch_bounds__(THREADS, 1)
+// GA (grouped only): the token tiles are gathered row by row from a.gx_hi / a.gx_lo
+// by GWARPS extra warps with 16-byte cp.async copies (the maps xhi, xlo are unused).
+template <class Epi, bool GU, int WN, bool GA = false>
+__global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
               const __grid_constant__ CUtensorMap xhi, const __grid_constant__ CUtensorMap xlo,
               const Args a, const Epi epi)
@@ -150,7 +166,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], GA ? 1 + GWARPS : 1);   // TMA, and each gather warp
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -216,12 +232,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     unsigned char *st = sm + s * STAGE_BYTES;
-                    mbar_expect_tx(&full[s], STAGE_BYTES);
+                    mbar_expect_tx(&full[s], GA ? G::TILE_W : STAGE_BYTES);
                     const int kx = i * BK;
 #pragma unroll
                     for (int h = 0; h < WN / BOXW; ++h) tma_load_2d(st + h * BOX_BYTES, bm[h], kx, brow[h], &full[s]);
-                    tma_load_2d(st + G::TILE_W, &xhi, a.x_col0 + kx, r0, &full[s]);
-                    tma_load_2d(st + G::TILE_W + TILE_X, &xlo, a.x_col0 + kx, r0, &full[s]);
+                    if constexpr (!GA) {
+                        tma_load_2d(st + G::TILE_W, &xhi, a.x_col0 + kx, r0, &full[s]);
+                        tma_load_2d(st + G::TILE_W + TILE_X, &xlo, a.x_col0 + kx, r0, &full[s]);
+                    }
                 }
             }
             // no copy may still be in flight when the CTA exits
@@ -271,6 +289,64 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_commit(done);
             volatile int never = 0;
             mbar_wait(done, 0, &never);
+        }
+    } else if (GA && warp >= THREADS / 32) {
+        if constexpr (GA) {
+            // ---------------- token-row gather (warps 10 ..): gather warp gw fills tile rows
+            // [64 gw, 64 gw + 64), hi and lo, in the stage's 128-byte-swizzled token tiles
+            // (16-byte chunk c of row t at chunk c ^ (t & 7) of its 128-byte row, as TMA lays
+            // it).  Lane l copies chunk l % 8 of rows 4 q + l / 8, so that each copy
+            // instruction reads four whole 128-byte row segments.  A warp arrives on a
+            // stage's full barrier once its copies of that stage have landed (cp.async
+            // groups), right after issuing the next stage: two stages are in flight, and
+            // the arrival never waits for the tensor core to free a later stage.  Rows past
+            // the group's end are not copied: their products only reach accumulator rows
+            // the epilogue skips.
+            const int gw = warp - THREADS / 32, c = lane & 7;
+            unsigned it = 0, arrived = 0;
+            auto arrive_upto = [&](unsigned n) {
+                fence_proxy_async_smem();   // the copies are read by the tensor core next
+                __syncwarp();
+                if (lane == 0)
+                    for (unsigned q = arrived; q < n; ++q) mbar_arrive(&full[q % STAGES]);
+                arrived = n;
+            };
+            bool ok = true;
+            for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
+                int mb, e, r0, rend;
+                tile_of(tau, mb, e, r0, rend);
+                int src[16];   // source row of this lane's tile rows in gx (-1: not copied)
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int r = r0 + 64 * gw + 4 * q + (lane >> 3);
+                    src[q] = r < rend ? a.grow[r] / a.gdiv : -1;
+                }
+                const int col = a.x_col0 + 8 * c;
+                for (int i = 0; i < nk; ++i, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, ab)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    unsigned char *xt = sm + s * STAGE_BYTES + G::TILE_W;
+                    const int kx = i * BK;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        if (src[q] < 0) continue;
+                        const int row = 64 * gw + 4 * q + (lane >> 3);
+                        const int off = row * 128 + ((c ^ (row & 7)) << 4);
+                        const size_t so = (size_t)src[q] * a.gld + col + kx;
+                        cp_async16(xt + off, a.gx_hi + so);
+                        cp_async16(xt + TILE_X + off, a.gx_lo + so);
+                    }
+                    cp_async_commit();
+                    cp_async_wait_group<1>();   // the previous stage's copies have landed
+                    arrive_upto(it);
+                }
+            }
+            cp_async_wait_group<0>();   // nothing in flight at exit; the last stages land
+            arrive_upto(it);
         }
     } else {
         // ---------------- epilogue (warps 2-9): warp w reads TMEM lane quarter w % 4
@@ -367,21 +443,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 // `rows` read as zeros.
 cudaError_t make_map_bf16(CUtensorMap *m, const void *base, int rows, int cols, int ld, int box_rows);
 
-template <bool GU, int WN, class Epi>
+template <bool GU, int WN, class Epi, bool GA = false>
 static cudaError_t launch_wn(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
                              const CUtensorMap &xlo, const Args &a, const Epi &epi, long long work, int nsm,
                              cudaStream_t st)
 {
     static bool attr_set = false;   // per instantiation; set before the first launch
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU, WN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Geo<GU, WN>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU, WN, GA>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Geo<GU, WN>::SMEM);
         if (e) return e;
         attr_set = true;
     }
     const int grid = (int)(work < nsm ? work : nsm);
-    return launch_pdl(k_tc_gemm<Epi, GU, WN>, dim3(grid), dim3(THREADS), Geo<GU, WN>::SMEM, st, w0, w1, xhi, xlo, a,
-                      epi);
+    return launch_pdl(k_tc_gemm<Epi, GU, WN, GA>, dim3(grid), dim3(GA ? THREADS_GA : THREADS), Geo<GU, WN>::SMEM,
+                      st, w0, w1, xhi, xlo, a, epi);
 }
 
 // ntile_bound: token tiles at most (dense: exact; grouped: the tile list's bound).
@@ -394,7 +470,9 @@ static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CU
 {
     if (ntile_bound <= 0 || a.n_out <= 0) return cudaSuccess;
     if constexpr (GU) {
-        return launch_wn<true, 256>(w0, w1, xhi, xlo, a, epi, (long long)(a.n_out / BOXW) * ntile_bound, nsm, st);
+        const long long work = (long long)(a.n_out / BOXW) * ntile_bound;
+        if (a.grow) return launch_wn<true, 256, Epi, true>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
+        return launch_wn<true, 256>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
     } else {
         const long long w256 = (long long)((a.n_out + 255) / 256) * ntile_bound;
         if (w256 >= 2ll * nsm) return launch_wn<false, 256>(w0, w1, xhi, xlo, a, epi, w256, nsm, st);
