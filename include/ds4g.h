@@ -167,6 +167,27 @@ int ds4g_session_common_prefix(const ds4g_session *s, const int32_t *tokens, int
  * no-op.  The logits are not recomputed. */
 int ds4g_session_truncate(ds4g_session *s, int common_prefix);
 
+/* [P1] section 3 ds4_session_sync / [P3] 阶段三: bring the session to the prompt
+ * tokens[0..n) (host) in one call.  The cached K/V of the prompt's common prefix
+ * with the history is kept, the rest is dropped, and the suffix is prefilled,
+ * so that the session then holds exactly the prompt and the logits of its last
+ * token.  The logits of a token are not kept once later tokens were processed,
+ * so a prompt that the history already holds (whole, or as a prefix) runs its
+ * last token again.  n == 0 empties the session.  *n_prefilled (may be NULL)
+ * receives the number of tokens run through the layers.  Checked before the
+ * session changes: DS4G_ECONTEXT if n >= n_ctx, DS4G_ETOKEN if a token is out of
+ * range; then the errors of ds4g_prefill. */
+int ds4g_session_sync(ds4g_session *s, const int32_t *tokens, int n, int *n_prefilled);
+
+/* [P1] section 6 ds4_session_rewrite_from_common: rewrite the live checkpoint to
+ * the prompt tokens[0..n) from a common prefix the caller found with
+ * ds4g_session_common_prefix: positions [0, common) are kept and tokens[common..n)
+ * are prefilled (when n > common; else the session is cut to n).  A prompt equal
+ * to the history (common == n == len) changes nothing.  DS4G_EINVAL unless
+ * 0 <= common <= ds4g_session_common_prefix(s, tokens, n); ECONTEXT and ETOKEN as
+ * for ds4g_session_sync, checked before the session changes. */
+int ds4g_session_rewrite_from_common(ds4g_session *s, const int32_t *tokens, int n, int common);
+
 int ds4g_session_len(const ds4g_session *s);
 
 /* Device pointer to the f32 [V] logits of the last processed token. */

@@ -479,6 +479,40 @@ int ds4g_session_truncate(ds4g_session *s, int common_prefix)
     return DS4G_OK;
 }
 
+// Checks of a prompt that come before a sync or a rewrite changes the session.
+static int prompt_ok(const ds4g_session *s, const int32_t *tokens, int n)
+{
+    if (!s || n < 0 || (n > 0 && !tokens)) return DS4G_EINVAL;
+    if (n >= s->n_ctx) return DS4G_ECONTEXT;
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= s->m->d.V) return DS4G_ETOKEN;
+    return DS4G_OK;
+}
+
+int ds4g_session_sync(ds4g_session *s, const int32_t *tokens, int n, int *n_prefilled)
+{
+    if (n_prefilled) *n_prefilled = 0;
+    const int rc = prompt_ok(s, tokens, n);
+    if (rc) return rc;
+    int cp = ds4g_session_common_prefix(s, tokens, n);
+    if (cp == n && n > 0) cp = n - 1;   // its logits are gone: run the last token again
+    s->len = cp;
+    if (n == cp) return DS4G_OK;
+    const int e = ds4g_prefill(s, tokens + cp, n - cp);
+    if (e == DS4G_OK && n_prefilled) *n_prefilled = n - cp;
+    return e;
+}
+
+int ds4g_session_rewrite_from_common(ds4g_session *s, const int32_t *tokens, int n, int common)
+{
+    const int rc = prompt_ok(s, tokens, n);
+    if (rc) return rc;
+    if (common < 0 || common > ds4g_session_common_prefix(s, tokens, n)) return DS4G_EINVAL;
+    if (common == n && n == s->len) return DS4G_OK;   // the checkpoint already holds the prompt
+    s->len = common;
+    return n > common ? ds4g_prefill(s, tokens + common, n - common) : DS4G_OK;
+}
+
 int ds4g_session_len(const ds4g_session *s) { return s ? s->len : DS4G_EINVAL; }
 
 const float *ds4g_session_logits(const ds4g_session *s) { return s ? s->b.logits : nullptr; }

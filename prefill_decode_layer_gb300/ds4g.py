@@ -73,6 +73,8 @@ def lib():
             "ds4g_session_hidden": ([vp], vp),
             "ds4g_session_common_prefix": ([vp, vp, i32], i32),
             "ds4g_session_truncate": ([vp, i32], i32),
+            "ds4g_session_sync": ([vp, vp, i32, vp], i32),
+            "ds4g_session_rewrite_from_common": ([vp, vp, i32, i32], i32),
             "ds4g_session_len": ([vp], i32),
             "ds4g_session_logits": ([vp], vp),
             "ds4g_session_kv": ([vp, i32, vp, vp], i32),
@@ -198,6 +200,17 @@ class Session:
 
     def truncate(self, cp: int) -> int:
         return lib().ds4g_session_truncate(self.ptr, int(cp))
+
+    def sync(self, tokens):
+        """Bring the session to the prompt `tokens`: (status, tokens prefilled)."""
+        t = (C.c_int32 * max(1, len(tokens)))(*[int(x) for x in tokens])
+        n = C.c_int(0)
+        rc = lib().ds4g_session_sync(self.ptr, t, len(tokens), C.byref(n))
+        return rc, n.value
+
+    def rewrite_from_common(self, tokens, common: int) -> int:
+        t = (C.c_int32 * max(1, len(tokens)))(*[int(x) for x in tokens])
+        return lib().ds4g_session_rewrite_from_common(self.ptr, t, len(tokens), int(common))
 
     def common_prefix(self, tokens) -> int:
         t = (C.c_int32 * len(tokens))(*[int(x) for x in tokens])

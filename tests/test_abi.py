@@ -57,4 +57,6 @@ def test_library_loads_and_validates_without_gpu(lib_path):
     # a null session is rejected before any device work
     assert L.ds4g_decode_step(None, 1) == pdl.ds4g.EINVAL
     assert L.ds4g_session_truncate(None, 0) == pdl.ds4g.EINVAL
+    assert L.ds4g_session_sync(None, None, 0, None) == pdl.ds4g.EINVAL
+    assert L.ds4g_session_rewrite_from_common(None, None, 0, 0) == pdl.ds4g.EINVAL
     assert L.ds4g_sample_workspace_bytes(129280) > 0

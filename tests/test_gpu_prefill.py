@@ -118,6 +118,65 @@ def test_truncate_then_suffix_equals_scratch_bitwise(small):
         assert live.decode(a) == 0 and scratch.decode(b) == 0
 
 
+def test_sync_and_rewrite_equal_scratch_bitwise(small):
+    """ds4g_session_sync and ds4g_session_rewrite_from_common leave the session
+    exactly as a scratch prefill of the prompt: K/V of every position and the
+    logits, bit for bit, in each case the calls distinguish."""
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    gm, _, SMALL = small
+    hist = synth.host_tokens(90, SMALL.vocab, stream=27)
+    fresh = synth.host_tokens(12, SMALL.vocab, stream=28)
+    fresh[0] = (hist[60] + 1) % SMALL.vocab
+
+    def same_as_scratch(sess, prompt):
+        scratch = pdl.Session(gm, 128)
+        assert scratch.prefill(prompt) == 0
+        torch.cuda.synchronize()
+        assert sess.len == len(prompt)
+        assert torch.equal(sess.logits(), scratch.logits())
+        for l in range(SMALL.n_layers):
+            assert torch.equal(sess.kv(l)[0][:len(prompt)], scratch.kv(l)[0][:len(prompt)])
+            assert torch.equal(sess.kv(l)[1][:len(prompt)], scratch.kv(l)[1][:len(prompt)])
+
+    def live():
+        s = pdl.Session(gm, 128)
+        assert s.prefill(hist[:88]) == 0
+        assert s.decode(int(hist[88])) == 0 and s.decode(int(hist[89])) == 0
+        return s
+
+    # a prompt that leaves the history after 60 tokens: the suffix only
+    s = live()
+    prompt = np.concatenate([hist[:60], fresh])
+    assert s.sync(prompt) == (0, 12)
+    same_as_scratch(s, prompt)
+    # a prompt the history holds as a prefix, then the same prompt again: the last
+    # token runs again, since its logits were not kept
+    s = live()
+    assert s.sync(hist[:50]) == (0, 1)
+    same_as_scratch(s, hist[:50])
+    assert s.sync(hist[:50]) == (0, 1)
+    same_as_scratch(s, hist[:50])
+    # empty prompt; errors leave the session as it was
+    assert s.sync([]) == (0, 0) and s.len == 0
+    s = live()
+    bad = np.concatenate([hist[:30], [SMALL.vocab]])
+    assert s.sync(bad)[0] == pdl.ds4g.ETOKEN and s.len == 90
+    assert s.sync(synth.host_tokens(128, SMALL.vocab, stream=29))[0] == pdl.ds4g.ECONTEXT and s.len == 90
+
+    # rewrite from the caller's common prefix, or from any shorter one
+    canonical = np.concatenate([hist[:60], fresh[:10]])
+    for common in (60, 41):
+        s = live()
+        assert s.common_prefix(canonical) == 60
+        assert s.rewrite_from_common(canonical, common) == 0
+        same_as_scratch(s, canonical)
+    s = live()
+    assert s.rewrite_from_common(canonical, 61) == pdl.ds4g.EINVAL and s.len == 90
+    assert s.rewrite_from_common(hist, 90) == 0 and s.len == 90     # already the prompt
+    assert s.rewrite_from_common(hist[:70], 70) == 0 and s.len == 70  # cut, nothing to run
+
+
 def test_session_errors(small):
     import prefill_decode_layer_gb300 as pdl
     gm, _, SMALL = small
