@@ -206,6 +206,27 @@ int ds4g_session_kv(ds4g_session *s, int layer, void **k, void **v);
  * n >= n_ctx. */
 int ds4g_session_restore(ds4g_session *s, const int32_t *tokens, int n);
 
+/* [P1] section 3 (steps 3-4: the disk KV cache, whose payload is restored before
+ * only the suffix is prefilled): a checkpoint of a session's cached state, the
+ * token history and the K/V rows of positions [0, len) of every layer, in a
+ * caller-owned host buffer.  Layout (little-endian): a 64-byte header (magic
+ * "DS4GKV01", format version, K/V element size, n_layers, head_dim, token count,
+ * a digest of the configuration), the int32 tokens padded to 16 bytes, then per
+ * layer the K rows and the V rows, [len][head_dim] each, as cached (K after RoPE).
+ * The logits are not part of it: after a load, ds4g_session_sync with the prompt
+ * runs the suffix (at least the last token) again. */
+size_t ds4g_checkpoint_bytes(const ds4g_config *cfg, int n_tokens);
+/* Write the checkpoint of s into buf (host memory of `bytes` bytes; pinned
+ * memory copies faster).  Synchronises the session stream.  DS4G_ESIZE if bytes <
+ * ds4g_checkpoint_bytes(cfg, len). */
+int ds4g_session_save(ds4g_session *s, void *buf, size_t bytes);
+/* Replace the state of s by a checkpoint written by ds4g_session_save for a model
+ * of the same configuration: DS4G_EINVAL on a header or configuration mismatch,
+ * DS4G_ESIZE if bytes is shorter than the checkpoint, DS4G_ECONTEXT if its length
+ * is >= n_ctx, DS4G_ETOKEN if a token is out of range; the session is unchanged on
+ * any of these.  Synchronises the session stream. */
+int ds4g_session_load(ds4g_session *s, const void *buf, size_t bytes);
+
 /* Router decision of the last decoded token: ids (int32) and weights (f32) of
  * `layer`, top_k each, copied to host arrays (synchronises the stream). */
 int ds4g_session_router(ds4g_session *s, int layer, int32_t *ids, float *weights);

@@ -538,6 +538,112 @@ int ds4g_session_restore(ds4g_session *s, const int32_t *tokens, int n)
     return DS4G_OK;
 }
 
+// ------------------------------------------------------------------ checkpoints
+namespace {
+struct CkptHeader {            // 64 bytes
+    char magic[8];             // "DS4GKV01"
+    uint32_t version, kv_size;
+    int32_t n_layers, head_dim, n_tokens, reserved;
+    uint64_t cfg_digest;
+    uint8_t pad[24];
+};
+static_assert(sizeof(CkptHeader) == 64, "checkpoint header");
+constexpr char kCkptMagic[8] = {'D', 'S', '4', 'G', 'K', 'V', '0', '1'};
+
+// FNV-1a over the configuration fields that fix the cached state's meaning.
+uint64_t cfg_digest(const ds4g_config &c)
+{
+    const int64_t f[] = {c.n_layers, c.hidden, c.n_heads, c.head_dim, c.q_rank, c.kv_rank, c.window,
+                         c.n_experts, c.top_k, c.expert_inter, c.vocab, c.weight_dtype, c.kv_dtype};
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&](const void *p, size_t n) {
+        const unsigned char *b = static_cast<const unsigned char *>(p);
+        for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
+    };
+    mix(f, sizeof(f));
+    mix(&c.rope_base, sizeof(c.rope_base));
+    mix(&c.rms_eps, sizeof(c.rms_eps));
+    return h;
+}
+size_t ckpt_tokens_bytes(int n) { return ((size_t)n * 4 + 15) & ~(size_t)15; }
+size_t ckpt_rows_bytes(const ds4g_config &c, int n)
+{
+    return (size_t)n * c.head_dim * (c.kv_dtype == DS4G_BF16 ? 2 : 4);
+}
+}  // namespace
+
+size_t ds4g_checkpoint_bytes(const ds4g_config *cfg, int n_tokens)
+{
+    if (!cfg_ok(cfg) || n_tokens < 0) return 0;
+    return sizeof(CkptHeader) + ckpt_tokens_bytes(n_tokens) +
+           (size_t)cfg->n_layers * 2 * ckpt_rows_bytes(*cfg, n_tokens);
+}
+
+int ds4g_session_save(ds4g_session *s, void *buf, size_t bytes)
+{
+    if (!s || !buf) return DS4G_EINVAL;
+    const ds4g_config &c = s->m->cfg;
+    const int n = s->len;
+    if (bytes < ds4g_checkpoint_bytes(&c, n)) return DS4G_ESIZE;
+    CkptHeader h;
+    memset(&h, 0, sizeof(h));
+    memcpy(h.magic, kCkptMagic, 8);
+    h.version = 1;
+    h.kv_size = c.kv_dtype == DS4G_BF16 ? 2 : 4;
+    h.n_layers = c.n_layers;
+    h.head_dim = c.head_dim;
+    h.n_tokens = n;
+    h.cfg_digest = cfg_digest(c);
+    char *p = static_cast<char *>(buf);
+    memcpy(p, &h, sizeof(h));
+    p += sizeof(h);
+    if (n) memcpy(p, s->hist.data(), (size_t)n * 4);
+    p += ckpt_tokens_bytes(n);
+    const size_t rows = ckpt_rows_bytes(c, n);
+    cudaError_t e = cudaSuccess;
+    for (int l = 0; !e && l < c.n_layers && rows; ++l) {
+        e = cudaMemcpyAsync(p, s->kc[l], rows, cudaMemcpyDeviceToHost, s->st);
+        p += rows;
+        if (!e) e = cudaMemcpyAsync(p, s->vc[l], rows, cudaMemcpyDeviceToHost, s->st);
+        p += rows;
+    }
+    if (!e) e = cudaStreamSynchronize(s->st);
+    return cuda_status(e);
+}
+
+int ds4g_session_load(ds4g_session *s, const void *buf, size_t bytes)
+{
+    if (!s || !buf) return DS4G_EINVAL;
+    const ds4g_config &c = s->m->cfg;
+    if (bytes < sizeof(CkptHeader)) return DS4G_ESIZE;
+    CkptHeader h;
+    memcpy(&h, buf, sizeof(h));
+    if (memcmp(h.magic, kCkptMagic, 8) || h.version != 1 || h.kv_size != (c.kv_dtype == DS4G_BF16 ? 2u : 4u) ||
+        h.n_layers != c.n_layers || h.head_dim != c.head_dim || h.n_tokens < 0 || h.cfg_digest != cfg_digest(c))
+        return DS4G_EINVAL;
+    const int n = h.n_tokens;
+    if (bytes < ds4g_checkpoint_bytes(&c, n)) return DS4G_ESIZE;
+    if (n >= s->n_ctx) return DS4G_ECONTEXT;
+    const char *p = static_cast<const char *>(buf) + sizeof(h);
+    const int32_t *tok = reinterpret_cast<const int32_t *>(p);
+    for (int i = 0; i < n; ++i)
+        if (tok[i] < 0 || tok[i] >= s->m->d.V) return DS4G_ETOKEN;
+    p += ckpt_tokens_bytes(n);
+    const size_t rows = ckpt_rows_bytes(c, n);
+    cudaError_t e = cudaSuccess;
+    for (int l = 0; !e && l < c.n_layers && rows; ++l) {
+        e = cudaMemcpyAsync(s->kc[l], p, rows, cudaMemcpyHostToDevice, s->st);
+        p += rows;
+        if (!e) e = cudaMemcpyAsync(s->vc[l], p, rows, cudaMemcpyHostToDevice, s->st);
+        p += rows;
+    }
+    if (!e) e = cudaStreamSynchronize(s->st);
+    if (e) return cuda_status(e);
+    if (n) memcpy(s->hist.data(), tok, (size_t)n * 4);
+    s->len = n;
+    return DS4G_OK;
+}
+
 int ds4g_session_router(ds4g_session *s, int layer, int32_t *ids, float *weights)
 {
     if (!s || layer < 0 || layer >= s->m->d.L || !ids || !weights) return DS4G_EINVAL;

@@ -74,6 +74,9 @@ def lib():
             "ds4g_session_common_prefix": ([vp, vp, i32], i32),
             "ds4g_session_truncate": ([vp, i32], i32),
             "ds4g_session_sync": ([vp, vp, i32, vp], i32),
+            "ds4g_checkpoint_bytes": ([vp, i32], sz),
+            "ds4g_session_save": ([vp, vp, sz], i32),
+            "ds4g_session_load": ([vp, vp, sz], i32),
             "ds4g_session_rewrite_from_common": ([vp, vp, i32, i32], i32),
             "ds4g_session_len": ([vp], i32),
             "ds4g_session_logits": ([vp], vp),
@@ -207,6 +210,18 @@ class Session:
         n = C.c_int(0)
         rc = lib().ds4g_session_sync(self.ptr, t, len(tokens), C.byref(n))
         return rc, n.value
+
+    def checkpoint_bytes(self) -> int:
+        return int(lib().ds4g_checkpoint_bytes(C.byref(self.model.cfg), self.len))
+
+    def save(self, buf: bytearray) -> int:
+        """Write the session's checkpoint into the host buffer `buf`."""
+        b = (C.c_char * len(buf)).from_buffer(buf)
+        return lib().ds4g_session_save(self.ptr, b, len(buf))
+
+    def load(self, buf) -> int:
+        b = (C.c_char * len(buf)).from_buffer_copy(bytes(buf))
+        return lib().ds4g_session_load(self.ptr, b, len(buf))
 
     def rewrite_from_common(self, tokens, common: int) -> int:
         t = (C.c_int32 * max(1, len(tokens)))(*[int(x) for x in tokens])

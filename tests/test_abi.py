@@ -58,5 +58,14 @@ def test_library_loads_and_validates_without_gpu(lib_path):
     assert L.ds4g_decode_step(None, 1) == pdl.ds4g.EINVAL
     assert L.ds4g_session_truncate(None, 0) == pdl.ds4g.EINVAL
     assert L.ds4g_session_sync(None, None, 0, None) == pdl.ds4g.EINVAL
+    assert L.ds4g_session_save(None, None, 0) == pdl.ds4g.EINVAL
+    assert L.ds4g_session_load(None, None, 0) == pdl.ds4g.EINVAL
+    # checkpoint size: 64-byte header, tokens padded to 16 bytes, K and V rows per layer
+    sh = synth.LAYER.with_(n_layers=3)
+    c3 = pdl.config_struct(sh)
+    for n in (0, 1, 5, 4096):
+        want = 64 + (4 * n + 15) // 16 * 16 + 3 * 2 * n * sh.head_dim * 2
+        assert L.ds4g_checkpoint_bytes(C.byref(c3), n) == want
+    assert L.ds4g_checkpoint_bytes(C.byref(c3), -1) == 0
     assert L.ds4g_session_rewrite_from_common(None, None, 0, 0) == pdl.ds4g.EINVAL
     assert L.ds4g_sample_workspace_bytes(129280) > 0

@@ -177,6 +177,49 @@ def test_sync_and_rewrite_equal_scratch_bitwise(small):
     assert s.rewrite_from_common(hist[:70], 70) == 0 and s.len == 70  # cut, nothing to run
 
 
+def test_checkpoint_save_load_then_suffix_equals_scratch(small):
+    """A checkpoint restores the K/V and the history bit for bit; the suffix
+    prefilled after it gives the scratch prefill's K/V and logits.  Damaged or
+    short buffers and a context that is too small leave the session as it was."""
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    gm, _, SMALL = small
+    hist = synth.host_tokens(72, SMALL.vocab, stream=30)
+    suffix = synth.host_tokens(8, SMALL.vocab, stream=31)
+    a = pdl.Session(gm, 128)
+    assert a.prefill(hist) == 0   # (decode steps would write K/V rows a prefill does not reproduce bitwise)
+    buf = bytearray(a.checkpoint_bytes())
+    assert a.save(bytearray(len(buf) - 1)) == pdl.ds4g.ESIZE
+    assert a.save(buf) == 0
+    b = pdl.Session(gm, 128)
+    assert b.load(buf) == 0 and b.len == 72
+    assert b.common_prefix(hist) == 72
+    torch.cuda.synchronize()
+    for l in range(SMALL.n_layers):
+        assert torch.equal(a.kv(l)[0][:72], b.kv(l)[0][:72])
+        assert torch.equal(a.kv(l)[1][:72], b.kv(l)[1][:72])
+    prompt = np.concatenate([hist, suffix])
+    assert b.sync(prompt) == (0, 8)
+    scratch = pdl.Session(gm, 128)
+    assert scratch.prefill(prompt) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(b.logits(), scratch.logits())
+    for l in range(SMALL.n_layers):
+        assert torch.equal(b.kv(l)[0][:80], scratch.kv(l)[0][:80])
+        assert torch.equal(b.kv(l)[1][:80], scratch.kv(l)[1][:80])
+    c = pdl.Session(gm, 128)
+    assert c.prefill(suffix) == 0
+    assert c.load(buf[:len(buf) - 16]) == pdl.ds4g.ESIZE and c.len == 8
+    bad = bytearray(buf)
+    bad[0] ^= 1                       # magic
+    assert c.load(bad) == pdl.ds4g.EINVAL and c.len == 8
+    bad = bytearray(buf)
+    bad[32] ^= 1                      # configuration digest
+    assert c.load(bad) == pdl.ds4g.EINVAL and c.len == 8
+    small_ctx = pdl.Session(gm, 72)
+    assert small_ctx.load(buf) == pdl.ds4g.ECONTEXT and small_ctx.len == 0
+
+
 def test_session_errors(small):
     import prefill_decode_layer_gb300 as pdl
     gm, _, SMALL = small
