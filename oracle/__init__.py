@@ -62,7 +62,7 @@ class SampleInfo(C.Structure):
                 ("cut_sum_margin", C.c_double), ("cut_gap_margin", C.c_double),
                 ("cdf_margin", C.c_double), ("cut_index", C.c_int), ("cut_next_index", C.c_int),
                 ("cut_p", C.c_double),
-                ("p_rms", C.c_double)]
+                ("p_rms", C.c_double), ("minp_margin", C.c_double)]
 
 
 _lib = None
@@ -91,6 +91,7 @@ def lib():
             "orc_lm_head": ([vp, vp, vp, vp], None),
             "orc_argmax": ([vp, i32], C.c_int32),
             "orc_sample": ([vp, i32, d, d, d, vp], C.c_int32),
+            "orc_sample_min_p": ([vp, i32, d, d, d, d, vp], C.c_int32),
             "orc_xorshift64s": ([vp], C.c_uint64),
             "orc_uniform": ([vp], d),
             "orc_session_new": ([vp, i32], vp),
@@ -233,10 +234,14 @@ def layer_step(cfg: Config, layer: Layer, kv: KV, pos: int, x: np.ndarray, trace
                          C.byref(trace) if trace is not None else None)
 
 
-def sample(logits: np.ndarray, temperature: float, top_p: float, u: float):
+def sample(logits: np.ndarray, temperature: float, top_p: float, u: float, min_p: float = 0.0):
     lg = np.ascontiguousarray(logits, dtype=np.float32)
     info = SampleInfo()
-    tok = lib().orc_sample(lg.ctypes.data, len(lg), temperature, top_p, u, C.byref(info))
+    if min_p > 0.0:
+        tok = lib().orc_sample_min_p(lg.ctypes.data, len(lg), temperature, top_p, min_p, u,
+                                     C.byref(info))
+    else:
+        tok = lib().orc_sample(lg.ctypes.data, len(lg), temperature, top_p, u, C.byref(info))
     return tok, info
 
 

@@ -318,9 +318,16 @@ static int cmp_desc(const void *a, const void *b)
 int32_t orc_sample(const float *logits, int n, double temperature, double top_p, double u,
                    orc_sample_info *info)
 {
+    return orc_sample_min_p(logits, n, temperature, top_p, 0.0, u, info);
+}
+
+int32_t orc_sample_min_p(const float *logits, int n, double temperature, double top_p, double min_p,
+                         double u, orc_sample_info *info)
+{
     orc_sample_info tmp;
     if (!info) info = &tmp;
     memset(info, 0, sizeof(*info));
+    info->minp_margin = 1.0;
     if (temperature <= 0.0) {
         info->n_kept = 1;
         info->cut_sum_margin = info->cut_gap_margin = info->cdf_margin = 1.0;
@@ -382,6 +389,19 @@ int32_t orc_sample(const float *logits, int n, double temperature, double top_p,
             }
         }
     }
+    /* 3. min-p: of the top-p set, keep the tokens whose probability is at least
+       min_p times the largest (p is relative to the largest, which is 1) */
+    if (min_p > 0.0)
+        for (int i = 0; i < n; i++)
+            if (kept[i]) {
+                const double mg = fabs(p[i] - min_p) / min_p;
+                if (mg < info->minp_margin) info->minp_margin = mg;
+                if (p[i] < min_p) kept[i] = 0;
+            }
+    if (min_p > 0.0) {
+        n_kept = 0;
+        for (int i = 0; i < n; i++) n_kept += kept[i];
+    }
     double sum = 0.0, sq = 0.0;
     for (int i = 0; i < n; i++)
         if (kept[i]) {
@@ -391,7 +411,7 @@ int32_t orc_sample(const float *logits, int n, double temperature, double top_p,
     info->p_rms = sqrt(sq) / sum;
     info->cut_p = info->cut_index >= 0 ? p[info->cut_index] / sum : 0.0;
 
-    /* 3. inverse CDF in vocabulary order over the kept tokens */
+    /* 4. inverse CDF in vocabulary order over the kept tokens */
     double rnd = u * sum;
     int32_t id = -1, last = -1;
     for (int i = 0; i < n; i++) {

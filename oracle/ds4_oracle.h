@@ -123,6 +123,8 @@ typedef struct {
     double p_rms;           /* sqrt(sum of kept p^2) / sum_kept: scale of how far a
                                cumulative sum moves when every p carries a small
                                independent relative error */
+    double minp_margin;     /* min-p: smallest |p - min_p| / min_p over the top-p set
+                               (1 when min-p is off) */
 } orc_sample_info;
 
 /* ---- scalar formats ---- */
@@ -151,6 +153,11 @@ void orc_lm_head(const orc_config *c, const void *lm, const double *x, double *l
 int32_t orc_argmax(const float *logits, int n);
 int32_t orc_sample(const float *logits, int n, double temperature, double top_p, double u,
                    orc_sample_info *info);
+/* The same with a min-p filter (reading of the pages' sample_top_p_min_p, which
+ * names the two filters only): a token of the top-p set is kept if its probability
+ * is at least min_p times the largest; min_p <= 0 is off. */
+int32_t orc_sample_min_p(const float *logits, int n, double temperature, double top_p, double min_p,
+                         double u, orc_sample_info *info);
 uint64_t orc_xorshift64s(uint64_t *state);
 double orc_uniform(uint64_t *state);
 

@@ -432,6 +432,53 @@ def test_sampler_top_p_kept_set_brute_force():
             assert info.n_kept == len(kept)
 
 
+def test_sampler_min_p_hand_derived_cases():
+    # Relative probabilities 1, 1/2, 1/4, 1/8 and ~8e-4 at T = 1 (logits ln 8, ln 4,
+    # ln 2, 0, -5).  Reading of the pages' sample_top_p_min_p (the two filters are
+    # named only): a token of the top-p set stays if p >= min_p * max p.
+    lg = np.array([np.log(8.0), np.log(4.0), np.log(2.0), 0.0, -5.0], dtype=np.float32)
+    cases = [
+        # min_p, top_p, u, expected: kept set and CDF worked out by hand
+        (0.3, 1.0, 0.5, 0),    # kept {0, 1}, sum 1.5: u*sum = 0.75 lies in token 0's [0, 1)
+        (0.3, 1.0, 0.9, 1),    # 1.35 lies in token 1's [1, 1.5)
+        (0.2, 1.0, 0.95, 2),   # kept {0, 1, 2}, sum 1.75: 1.6625 lies in token 2's [1.5, 1.75)
+        (0.1, 0.6, 0.9, 1),    # top-p target 0.6 * 1.8758 = 1.1255 keeps {0, 1}: 1.35 -> 1
+        (0.1, 1.0, 0.99, 3),   # kept {0, 1, 2, 3}, sum 1.875: 1.856 lies in token 3's [1.75, 1.875)
+        (1.0, 1.0, 0.999, 0),  # only the largest survives min_p = 1
+        (0.0005, 1.0, 0.9999, 4),  # min_p below 8.4e-4 keeps token 4: 1.8757 in [1.875, 1.8758)
+        (0.001, 1.0, 0.9999, 3),   # above it drops token 4: sum 1.875, 1.8748 in [1.75, 1.875)
+    ]
+    for mp, tp, u, expect in cases:
+        tok, info = oracle.sample(lg, 1.0, tp, u, min_p=mp)
+        assert tok == expect, (mp, tp, u, tok)
+
+
+def test_sampler_min_p_kept_set_brute_force():
+    rng = np.random.default_rng(15)
+    for _ in range(40):
+        n = int(rng.integers(2, 9))
+        lg = (rng.standard_normal(n) * 2).astype(np.float32)
+        T, tp = float(rng.uniform(0.3, 2.0)), float(rng.choice([1.0, rng.uniform(0.05, 0.999)]))
+        mp = float(rng.uniform(0.01, 0.9))
+        pr = np.exp(lg.astype(np.float64) / T - (lg.astype(np.float64) / T).max())
+        order = sorted(range(n), key=lambda i: (-pr[i], i))
+        cum, nucleus = 0.0, []
+        for i in order:
+            cum += pr[i]
+            nucleus.append(i)
+            if tp < 1.0 and cum >= tp * pr.sum():
+                break
+        kept = sorted(i for i in nucleus if pr[i] >= mp * pr.max())
+        S = pr[kept].sum()
+        edges = np.cumsum(pr[kept]) / S
+        for u in rng.uniform(0, 1, 20):
+            expect = kept[int(np.searchsorted(edges, u, side="left"))]
+            tok, info = oracle.sample(lg, T, tp, float(u), min_p=mp)
+            if info.cdf_margin > 1e-12 and info.minp_margin > 1e-12:
+                assert tok == expect
+                assert info.n_kept == len(kept)
+
+
 def test_sampler_frequencies_chi_square():
     rng = np.random.default_rng(14)
     lg = rng.standard_normal(8).astype(np.float32)
