@@ -314,6 +314,18 @@ int32_t ds4g_sample(const float *logits, int n_vocab, float temperature, float t
 int32_t ds4g_sample_u(const float *logits, int n_vocab, float temperature, float top_p,
                       uint32_t u24, void *workspace, size_t workspace_bytes, void *cuda_stream);
 
+/* [P3] 阶段四 sample_top_p_min_p (named there with top-p, without a definition):
+ * ds4g_sample with a min-p filter as well.  Reading: of the top-p set, a token is
+ * kept only if its probability is at least min_p times the largest probability;
+ * min_p = 0 is ds4g_sample, min_p = 1 keeps the most probable token (and its exact
+ * ties).  0 <= min_p <= 1, else DS4G_EINVAL.  Everything else as ds4g_sample. */
+int32_t ds4g_sample_min_p(const float *logits, int n_vocab, float temperature, float top_p, float min_p,
+                          uint64_t *rng_state, void *workspace, size_t workspace_bytes,
+                          void *cuda_stream);
+/* ds4g_sample_min_p with the uniform draw given by the caller, as ds4g_sample_u. */
+int32_t ds4g_sample_u_min_p(const float *logits, int n_vocab, float temperature, float top_p, float min_p,
+                            uint32_t u24, void *workspace, size_t workspace_bytes, void *cuda_stream);
+
 /* Largest vocabulary ds4g_sample_static accepts. */
 #define DS4G_SAMPLE_STATIC_MAX_VOCAB 262144
 

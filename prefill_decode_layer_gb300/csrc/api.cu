@@ -743,13 +743,13 @@ size_t ds4g_sample_workspace_bytes(int n_vocab)
     return n_vocab > 0 ? sample_workspace_bytes(n_vocab) : 0;
 }
 
-static int32_t sample_common(const float *logits, int n_vocab, float temperature, float top_p,
+static int32_t sample_common(const float *logits, int n_vocab, float temperature, float top_p, float min_p,
                              unsigned u24, void *workspace, size_t workspace_bytes, void *stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int *res = nullptr;
     int32_t tok = -1;
-    cudaError_t e = sample_launch(logits, n_vocab, temperature, top_p, u24, workspace, st, &res);
+    cudaError_t e = sample_launch(logits, n_vocab, temperature, top_p, min_p, u24, workspace, st, &res);
     if (!e) e = cudaMemcpyAsync(&tok, res, 4, cudaMemcpyDeviceToHost, st);
     if (!e) e = cudaStreamSynchronize(st);
     if (e) return DS4G_ECUDA;
@@ -775,7 +775,7 @@ int32_t ds4g_sample(const float *logits, int n_vocab, float temperature, float t
         if (!rng_state || *rng_state == 0) return DS4G_EINVAL;
         u24 = (unsigned)(xorshift64s(rng_state) >> 40);
     }
-    return sample_common(logits, n_vocab, temperature, top_p, u24, workspace, workspace_bytes,
+    return sample_common(logits, n_vocab, temperature, top_p, 0.f, u24, workspace, workspace_bytes,
                          stream);
 }
 
@@ -785,8 +785,31 @@ int32_t ds4g_sample_u(const float *logits, int n_vocab, float temperature, float
     const int rc = sample_args_ok(logits, n_vocab, temperature, top_p, workspace, workspace_bytes);
     if (rc) return rc;
     if (u24 >= (1u << 24)) return DS4G_EINVAL;
-    return sample_common(logits, n_vocab, temperature, top_p, u24, workspace, workspace_bytes,
+    return sample_common(logits, n_vocab, temperature, top_p, 0.f, u24, workspace, workspace_bytes,
                          stream);
+}
+
+int32_t ds4g_sample_min_p(const float *logits, int n_vocab, float temperature, float top_p, float min_p,
+                          uint64_t *rng_state, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const int rc = sample_args_ok(logits, n_vocab, temperature, top_p, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (!(min_p >= 0.f && min_p <= 1.f)) return DS4G_EINVAL;
+    unsigned u24 = 0;
+    if (temperature > 0.f) {
+        if (!rng_state || *rng_state == 0) return DS4G_EINVAL;
+        u24 = (unsigned)(xorshift64s(rng_state) >> 40);
+    }
+    return sample_common(logits, n_vocab, temperature, top_p, min_p, u24, workspace, workspace_bytes, stream);
+}
+
+int32_t ds4g_sample_u_min_p(const float *logits, int n_vocab, float temperature, float top_p, float min_p,
+                            uint32_t u24, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const int rc = sample_args_ok(logits, n_vocab, temperature, top_p, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (!(min_p >= 0.f && min_p <= 1.f) || u24 >= (1u << 24)) return DS4G_EINVAL;
+    return sample_common(logits, n_vocab, temperature, top_p, min_p, u24, workspace, workspace_bytes, stream);
 }
 
 static_assert(DS4G_SAMPLE_STATIC_MAX_VOCAB == kSampleStaticMaxVocab, "header and library agree");
@@ -801,7 +824,7 @@ int32_t ds4g_sample_static(const float *logits, int n_vocab, float temperature, 
     if (sample_static_scratch(&scratch)) return DS4G_ECUDA;
     unsigned u24 = 0;
     if (temperature > 0.f) u24 = (unsigned)(xorshift64s(rng_state) >> 40);
-    return sample_common(logits, n_vocab, temperature, top_p, u24, scratch, kSampleStaticBytes, stream);
+    return sample_common(logits, n_vocab, temperature, top_p, 0.f, u24, scratch, kSampleStaticBytes, stream);
 }
 
 const char *ds4g_strerror(int code)

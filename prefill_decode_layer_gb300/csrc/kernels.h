@@ -23,7 +23,7 @@ constexpr int kSampleStaticMaxVocab = 262144;
 constexpr size_t kSampleStaticBytes = 16384;
 constexpr int kMaxDevices = 64;
 cudaError_t sample_static_scratch(void **p);
-cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p,
+cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p, float min_p,
                           unsigned u24, void *ws, cudaStream_t st, int **result_dev);
 
 // prefill.cu

@@ -14,9 +14,12 @@
 //            Ties at tau are kept in index order, as many as the target needs.
 //   pass 5   per-chunk sums of kept q; the last CTA finds the chunk and then the
 //            first token, in vocabulary order, whose running kept sum reaches
-//            R = max(1, ceil(u * kept_total)) (u = k / 2^24 exactly).
+//            R = max(1, ceil(u * kept_total)) (u = k / 2^24 exactly).  With min-p,
+//            a token of the top-p set is kept only if p >= min_p (p is relative to
+//            the largest, which is exactly 1): the bit patterns compare the same way.
 // T <= 0.   argmax: max of (ordered logit bits, inverted index) as one u64.
 #include "common.cuh"
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kSThreads) k_s_hist(const float *logits, int n
 
 // Final pass: per-chunk kept sums, then the inverse-CDF search by the last CTA.
 __global__ void __launch_bounds__(kSThreads) k_s_draw(const float *logits, int n, float temp,
-                                                      int keep_all, unsigned u24, SampleWS *ws,
+                                                      int keep_all, unsigned mbits, unsigned u24, SampleWS *ws,
                                                       unsigned long long *chunk_above,
                                                       unsigned *chunk_ties)
 {
@@ -169,6 +172,7 @@ __global__ void __launch_bounds__(kSThreads) k_s_draw(const float *logits, int n
     for (int i = base + threadIdx.x; i < min(base + kChunk, n); i += blockDim.x) {
         const float p = prob(logits[i], temp, zm);
         const unsigned bits = __float_as_uint(p);
+        if (bits < mbits) continue;   // below min-p
         if (keep_all || bits > tau) sum += fixed_q(p);
         else if (bits == tau) ties += 1u;
     }
@@ -242,8 +246,10 @@ __global__ void __launch_bounds__(kSThreads) k_s_draw(const float *logits, int n
         if (i < c1) {
             const float p = prob(logits[i], temp, zm);
             const unsigned bits = __float_as_uint(p);
-            if (keep_all || bits > tau) qv[j] = fixed_q(p);
-            else if (bits == tau) { tie[j] = 1; tcount++; }
+            if (bits >= mbits) {
+                if (keep_all || bits > tau) qv[j] = fixed_q(p);
+                else if (bits == tau) { tie[j] = 1; tcount++; }
+            }
         }
         psum += qv[j];
     }
@@ -300,12 +306,22 @@ __global__ void __launch_bounds__(kSThreads) k_s_draw(const float *logits, int n
         if (r == 0x7fffffff) {  // rounding guard: the last kept token of the chunk
             for (int i = c1 - 1; i >= c0; --i) {
                 const float p = prob(logits[i], temp, zm);
-                if (fixed_q(p) && (keep_all || __float_as_uint(p) >= tau)) { r = i; break; }
+                if (fixed_q(p) && __float_as_uint(p) >= mbits && (keep_all || __float_as_uint(p) >= tau)) {
+                    r = i;
+                    break;
+                }
             }
         }
         ws->result = r;
         ws->tickets[5] = 0u;
     }
+}
+
+static unsigned host_float_bits(float f)
+{
+    unsigned u;
+    memcpy(&u, &f, 4);
+    return u;
 }
 
 size_t sample_workspace_bytes(int n)
@@ -315,7 +331,7 @@ size_t sample_workspace_bytes(int n)
 }
 
 // Issues the sampler kernels; the token id is left at *result_dev.
-cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p,
+cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p, float min_p,
                           unsigned u24, void *ws_mem, cudaStream_t st, int **result_dev)
 {
     SampleWS *ws = static_cast<SampleWS *>(ws_mem);
@@ -338,7 +354,9 @@ cudaError_t sample_launch(const float *logits, int n, float temperature, float t
             if ((e = cudaGetLastError())) return e;
         }
     }
-    k_s_draw<<<nch, kSThreads, 0, st>>>(logits, n, temperature, keep_all, u24, ws, chunk_above,
+    // min-p as a bound on the bit pattern of p (p >= 0); 0 keeps everything
+    const unsigned mbits = min_p > 0.f ? host_float_bits(min_p < 1.f ? min_p : 1.f) : 0u;
+    k_s_draw<<<nch, kSThreads, 0, st>>>(logits, n, temperature, keep_all, mbits, u24, ws, chunk_above,
                                          chunk_ties);
     ++launch_count();
     return cudaGetLastError();

@@ -92,6 +92,9 @@ def lib():
             "ds4g_session_timing": ([vp, vp, vp, i32], i32),
             "ds4g_sample": ([vp, i32, C.c_float, C.c_float, vp, vp, sz, vp], C.c_int32),
             "ds4g_sample_u": ([vp, i32, C.c_float, C.c_float, C.c_uint32, vp, sz, vp], C.c_int32),
+            "ds4g_sample_min_p": ([vp, i32, C.c_float, C.c_float, C.c_float, vp, vp, sz, vp], C.c_int32),
+            "ds4g_sample_u_min_p": ([vp, i32, C.c_float, C.c_float, C.c_float, C.c_uint32, vp, sz, vp],
+                                    C.c_int32),
             "ds4g_strerror": ([i32], C.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -299,12 +302,17 @@ def sample_workspace_bytes(n_vocab: int) -> int:
 
 
 def sample(logits: torch.Tensor, temperature: float, top_p: float, rng_state: int | None,
-           workspace: torch.Tensor, stream=None):
-    """Returns (token, new_rng_state)."""
+           workspace: torch.Tensor, stream=None, min_p: float = 0.0):
+    """Returns (token, new_rng_state); min_p > 0 calls ds4g_sample_min_p."""
     st = C.c_uint64(rng_state or 0)
-    tok = lib().ds4g_sample(logits.data_ptr(), logits.numel(), float(temperature), float(top_p),
-                            C.byref(st), workspace.data_ptr(), workspace.numel(),
-                            _stream_ptr(stream))
+    if min_p > 0.0:
+        tok = lib().ds4g_sample_min_p(logits.data_ptr(), logits.numel(), float(temperature),
+                                      float(top_p), float(min_p), C.byref(st), workspace.data_ptr(),
+                                      workspace.numel(), _stream_ptr(stream))
+    else:
+        tok = lib().ds4g_sample(logits.data_ptr(), logits.numel(), float(temperature), float(top_p),
+                                C.byref(st), workspace.data_ptr(), workspace.numel(),
+                                _stream_ptr(stream))
     return tok, st.value
 
 
@@ -318,8 +326,12 @@ def sample_static(logits: torch.Tensor, temperature: float, top_p: float,
 
 
 def sample_u(logits: torch.Tensor, temperature: float, top_p: float, u24: int,
-             workspace: torch.Tensor, stream=None) -> int:
+             workspace: torch.Tensor, stream=None, min_p: float = 0.0) -> int:
     """Sample with a caller-given uniform draw u = u24 / 2^24."""
+    if min_p > 0.0:
+        return lib().ds4g_sample_u_min_p(logits.data_ptr(), logits.numel(), float(temperature),
+                                         float(top_p), float(min_p), int(u24), workspace.data_ptr(),
+                                         workspace.numel(), _stream_ptr(stream))
     return lib().ds4g_sample_u(logits.data_ptr(), logits.numel(), float(temperature),
                                float(top_p), int(u24), workspace.data_ptr(), workspace.numel(),
                                _stream_ptr(stream))

@@ -35,6 +35,15 @@ def undecidable(info, token: int) -> bool:
     return info.cdf_margin < band
 
 
+def undecidable_min_p(info, token: int) -> bool:
+    """As undecidable(), and a token of the top-p set whose p lies within f32 noise
+    (4e-6 relative) of the min-p bound may be kept on one side and not the other:
+    that moves the kept total by up to that token's p (at most min_p * max p)."""
+    if info.minp_margin < 4e-6:
+        return True
+    return undecidable(info, token)
+
+
 def workspace(n):
     import torch
     import prefill_decode_layer_gb300 as pdl
@@ -94,3 +103,43 @@ def test_draws_match_oracle(sigma, T, top_p, stream):
             assert tok == otok, f"draw {i}: {tok} vs {otok} (u={u})"
         state = new_state
     assert ambiguous <= (3 * n) // 10, ambiguous   # the rest (>= 70%) matched exactly
+
+
+def test_min_p_hand_derived_cases_on_device():
+    """The hand-derived min-p cases of the oracle pins, on the device."""
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    lg = np.array([np.log(8.0), np.log(4.0), np.log(2.0), 0.0, -5.0], dtype=np.float32)
+    t = torch.from_numpy(lg).cuda()
+    ws = workspace(len(lg))
+    for mp, tp, u, expect in [(0.3, 1.0, 0.5, 0), (0.3, 1.0, 0.9, 1), (0.2, 1.0, 0.95, 2),
+                              (0.1, 0.6, 0.9, 1), (0.1, 1.0, 0.99, 3), (1.0, 1.0, 0.999, 0),
+                              (0.0005, 1.0, 0.9999, 4), (0.001, 1.0, 0.9999, 3)]:
+        u24 = int(round(u * (1 << 24)))
+        assert pdl.sample_u(t, 1.0, tp, u24, ws, min_p=mp) == expect, (mp, tp, u)
+    assert pdl.sample_u(t, 1.0, 1.0, 5, ws, min_p=1.5) == pdl.ds4g.EINVAL
+
+
+@pytest.mark.parametrize("sigma,T,top_p,min_p", [(2.0, 0.7, 0.95, 0.05), (1.0, 1.0, 1.0, 0.2),
+                                                 (3.0, 0.5, 0.9, 0.01), (0.3, 1.3, 1.0, 0.9)])
+def test_min_p_draws_match_oracle(sigma, T, top_p, min_p):
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    from synth import torch_weights as tw
+    V = 129280
+    ws = workspace(V)
+    dev = tw.dev_logits(V, sigma, stream_id=12)
+    host = synth.host_logits(V, sigma, stream=12)
+    state = 0x9E3779B97F4A7C15
+    n, ambiguous = 200, 0
+    for i in range(n):
+        tok, new_state = pdl.sample(dev, T, top_p, state, ws, min_p=min_p)
+        u, ostate = oracle.uniform(state)
+        assert new_state == ostate
+        otok, info = oracle.sample(host, T, top_p, u, min_p=min_p)
+        if undecidable_min_p(info, otok):
+            ambiguous += 1
+        else:
+            assert tok == otok, f"draw {i}: {tok} vs {otok} (u={u})"
+        state = new_state
+    assert ambiguous <= (3 * n) // 10, ambiguous
