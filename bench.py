@@ -289,7 +289,7 @@ def run_case(args):
     emb, lm, layers = tw.dev_model(shape)
     m = pdl.Model(shape, emb, lm, layers)
     n_pre = 4096
-    s = pdl.Session(m, n_pre + args.warmup + args.steps + 8)
+    s = pdl.Session(m, n_pre + args.warmup + args.steps + 16)
     k, v = s.kv(0)
     tw.fill_kv(shape, 0, k, v, n_pre)
     assert s.restore(synth.host_tokens(n_pre, shape.vocab, stream=11)) == 0
@@ -305,8 +305,44 @@ def run_case(args):
     torch.cuda.synchronize()
     assert s.status() == 0
     us = ev0.elapsed_time(ev1) * 1e3 / max(1, args.steps)
-    print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup,
-                      "launches": int(s.launches), "us_per_step": us}), flush=True)
+    out = {"case": args.case, "steps": args.steps, "warmup": args.warmup,
+           "launches": int(s.launches), "us_per_step": us}
+    if args.timeline:
+        out["timeline_us"] = decode_timeline(torch, s, shape, synth.host_tokens(6, shape.vocab, stream=6))
+    print(json.dumps(out), flush=True)
+
+
+# Stage starts of the persistent decode kernel (globaltimer stamps of every CTA,
+# the session's trace buffer): per event, the earliest, median and latest CTA, in
+# us after the first CTA started, averaged over a few steps run back to back.
+# Events per layer l: 7 l + 0 stage 1, + 1 stages 2-3, + 2 stages 2-3 after the
+# query/K/V items, + 3 stage 4, + 4 stage 5, + 5 stage 6, + 6 stage 7; then the
+# lm_head and the end.
+TIMELINE_NAMES = ["stage 1 (norm, W_qa/W_kva)", "stages 2-3 (queries, K/V, attention)",
+                  "stages 2-3 after the query/K/V rows", "stage 4 (W_o)", "stage 5 (norm, router)",
+                  "stage 6 (gate/up, after the top-k)", "stage 7 (down, combine)"]
+
+
+def decode_timeline(torch, sess, shape, toks):
+    ev = 7 * shape.n_layers + 2
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros(ev * nsm, dtype=torch.int64, device="cuda")
+    acc = np.zeros((ev, 3))
+    for t in toks:
+        buf.zero_()
+        sess.set_trace(buf)
+        assert sess.decode_layers(int(t)) == 0
+        sess.set_trace(None)
+        torch.cuda.synchronize()
+        st = buf.cpu().numpy().reshape(ev, nsm).astype(np.float64)
+        t0 = st[0].min()
+        for e in range(ev):
+            row = (st[e] - t0) / 1e3
+            acc[e] += [row.min(), np.median(row), row.max()]
+    acc /= len(toks)
+    names = [f"layer {l}: {n}" for l in range(shape.n_layers) for n in TIMELINE_NAMES]
+    names += ["lm_head", "end"]
+    return {n: [round(v, 2) for v in acc[e]] for e, n in enumerate(names)}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -320,6 +356,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the prefill / stack / resync measurements")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--timeline", action="store_true",
+                    help="with --case decode-*: also print the kernel's stage start times")
     ap.add_argument("--case", default=None, choices=list(CASES),
                     help="run only warmup + steps of one workload (the profiling commands "
                          "recorded in profiles/ use this) and print a one-line summary")
