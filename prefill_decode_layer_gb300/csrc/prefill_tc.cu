@@ -429,7 +429,10 @@ struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16, 16-by
 
 // x[t] += sum over slots s (in order) of w[t][s] * YS[t*K + s]: the selected experts'
 // outputs, after the shared expert's down projection was added by its GEMM.
-__global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, const float *wts, int H, int K)
+// With gnext (H <= 8192): also the next layer's attention RMSNorm of the new row,
+// as BF16 hi/lo into hi, lo (what k_rmsnorm_hilo would write next).
+__global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, const float *wts, int H, int K,
+                                                     const float *gnext, float eps, bf16 *nhi, bf16 *nlo)
 {
     pdl_wait();      // inputs of the previous kernel (programmatic launch)
     pdl_trigger();
@@ -437,6 +440,7 @@ __global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, 
     float w[8];
 #pragma unroll
     for (int s = 0; s < 8; ++s) w[s] = s < K ? wts[(size_t)t * K + s] : 0.f;
+    float4 xr[8];   // the new row, for the fused RMSNorm
     for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
         float4 y[8];
 #pragma unroll
@@ -453,7 +457,33 @@ __global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, 
             }
         float4 *x = reinterpret_cast<float4 *>(X + (size_t)t * H + i);
         const float4 xv = *x;
-        *x = make_float4(xv.x + r.x, xv.y + r.y, xv.z + r.z, xv.w + r.w);
+        const float4 xn = make_float4(xv.x + r.x, xv.y + r.y, xv.z + r.z, xv.w + r.w);
+        *x = xn;
+        const int u = i / (blockDim.x * 4);
+        if (u < 8) xr[u] = xn;
+    }
+    if (!gnext) return;
+    __shared__ float red[32];
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = threadIdx.x * 4 + u * blockDim.x * 4;
+        if (i < H) ss = fmaf(xr[u].x, xr[u].x, fmaf(xr[u].y, xr[u].y, fmaf(xr[u].z, xr[u].z, fmaf(xr[u].w, xr[u].w, ss))));
+    }
+    ss = block_sum(ss, red);
+    const float inv = rsqrtf(ss / (float)H + eps);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = threadIdx.x * 4 + u * blockDim.x * 4;
+        if (i >= H) continue;
+        const float4 gv = *reinterpret_cast<const float4 *>(gnext + i);
+        __align__(8) bf16 h[4], l[4];
+        split_hilo(xr[u].x * inv * gv.x, h[0], l[0]);
+        split_hilo(xr[u].y * inv * gv.y, h[1], l[1]);
+        split_hilo(xr[u].z * inv * gv.z, h[2], l[2]);
+        split_hilo(xr[u].w * inv * gv.w, h[3], l[3]);
+        *reinterpret_cast<uint2 *>(nhi + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(h);
+        *reinterpret_cast<uint2 *>(nlo + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(l);
     }
 }
 
@@ -541,6 +571,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
     const int ny = (n + tc::BT - 1) / tc::BT;
     const int max_tiles = nent / tc::BT + d.E + 1;
     if ((e = launch_pdl(k_embed_rows, dim3(n), dim3(256), 0, st, tok_embd, (const int *)pb.tok, pb.X, H))) return e;
+    bool normed = false;   // xn holds the next layer's attention RMSNorm already
     for (int l = 0; l <= d.L; ++l) {
         if (pb.rec_row >= 0 && pb.layer_x &&
             (e = cudaMemcpyAsync(pb.layer_x + (size_t)l * H, pb.X + (size_t)pb.rec_row * H, (size_t)H * 4,
@@ -553,8 +584,9 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         tc::Args a{};
         a.status = pb.status;
         a.m_tok = n;
-        // ---- attention half
-        if ((e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
+        // ---- attention half (its RMSNorm came with the previous layer's combine)
+        if (!normed &&
+            (e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
                             (const float *)w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
             return e;
         a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ, a.x_col0 = 0;
@@ -629,9 +661,11 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         a.n_out = H, a.k = I;
         if ((e = tc::launch<false>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
+        const float *gn = l + 1 < d.L && H <= 8 * 1024 ? layers[l + 1].attn_norm : nullptr;
         if ((e = launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, st, pb.X, (const float *)pb.YS,
-                            (const float *)pb.wts, H, K)))
+                            (const float *)pb.wts, H, K, gn, d.eps, ap.xn_hi, ap.xn_lo)))
             return e;
+        normed = gn != nullptr;
     }
     return cudaGetLastError();
 }
