@@ -70,6 +70,25 @@ def test_bf16_widening_and_rounding_match_torch():
     assert np.array_equal(got, ref)
 
 
+def test_embed_gathers_the_token_row():
+    """orc_embed (ds4 page "端到端推理流程", 4.1 embed_token_f16) against numpy
+    indexing of a [V][H] float16 table whose rows are all different; the first,
+    last and interior tokens are checked, and hidden != vocab, so a wrong stride,
+    a transposed table or an off-by-one row fails."""
+    V, H = 11, 16
+    rng = np.random.default_rng(21)
+    vals = rng.standard_normal((V, H)) * 4.0
+    vals[:, 0] = np.arange(V)                     # row t starts with t: rows are distinct
+    table = np.ascontiguousarray(vals.astype(np.float16))
+    cfg = oracle.config_from(tiny_cfg(hidden=H, vocab=V))
+    for tok in (0, 1, 5, V - 2, V - 1):
+        x = np.full(H, np.nan)
+        L.orc_embed(C.byref(cfg), p(table.view(np.uint16)), tok, p(x))
+        assert np.array_equal(x, table[tok].astype(np.float64))
+        if tok > 0:
+            assert not np.array_equal(x, table[tok - 1].astype(np.float64))
+
+
 # ----------------------------------------------------------------------------- rmsnorm
 
 def rmsnorm(x, g, eps):
@@ -492,21 +511,41 @@ def test_sampler_frequencies_chi_square():
     assert pval > 1e-4
 
 
-def test_xorshift_golden_states_and_uniformity():
-    vals = {}
-    states = []
+def read_xorshift_golden():
+    start, steps = None, []
     for line in open(os.path.join(GOLD, "xorshift64s.txt")):
         line = line.split("#")[0].strip()
-        if line:
-            k, v = line.split()
-            if k == "start":
-                vals["start"] = int(v)
-            else:
-                states.append(int(v))
-    s = C.c_uint64(vals["start"])
-    for expect in states:
-        L.orc_xorshift64s(C.byref(s))
-        assert s.value == expect
+        if not line:
+            continue
+        k, v = line.split()
+        if k == "start":
+            start = int(v)
+        elif k == "state":
+            steps.append({"state": int(v)})
+        else:
+            steps[-1][k] = int(v, 0)
+    return start, steps
+
+
+def test_xorshift_golden_states_draws_and_uniforms():
+    """State sequence, scrambled draws and uniforms against the hand-derived fixture
+    (Vigna 2016; the workloads' seeded xorshift generator).  A wrong shift fails the
+    states, a wrong multiplier the draws, a wrong bit selection the uniforms."""
+    start, steps = read_xorshift_golden()
+    assert len(steps) == 2 and all(len(st) == 3 for st in steps)
+    s = C.c_uint64(start)
+    for st in steps:
+        draw = L.orc_xorshift64s(C.byref(s))
+        assert s.value == st["state"]
+        assert draw == st["output"]
+    s = C.c_uint64(start)
+    for st in steps:
+        u = L.orc_uniform(C.byref(s))
+        assert s.value == st["state"]
+        assert u == st["unum"] / 16777216.0
+
+
+def test_xorshift_uniformity():
     state = 12345
     us = []
     for _ in range(20000):
@@ -515,6 +554,8 @@ def test_xorshift_golden_states_and_uniformity():
     us = np.array(us)
     assert us.min() >= 0.0 and us.max() < 1.0
     assert scipy.stats.kstest(us, "uniform").pvalue > 1e-4
+    # 24-bit resolution: every draw is a whole multiple of 2^-24
+    assert np.all(us * 16777216.0 == np.floor(us * 16777216.0))
 
 
 # ----------------------------------------------------------------------------- session
@@ -548,6 +589,30 @@ def test_layer_major_prefill_equals_sequential_decode():
         ka, va = oracle.kv_views(a, layer, 32)
         kb, vb = oracle.kv_views(b, layer, 32)
         assert np.array_equal(ka[:11], kb[:11]) and np.array_equal(va[:11], vb[:11])
+
+
+@pytest.mark.parametrize("wdtype", ["f32", "bf16"])
+def test_prefill_logits_are_lm_head_of_the_last_token(wdtype):
+    """orc_prefill's logits (page "端到端推理流程", 4.3: the last layer's output goes
+    to lm_head) equal W_lm @ hidden[n-1] computed by numpy from the prefill's own
+    final hidden states: the last token, not the first, and no final norm.  The
+    same holds for one decode step after the prefill."""
+    shape = small_shape().with_(weight_dtype=wdtype)
+    om = tiny_model(shape)
+    lm = synth.host_lm_head(shape)
+    W = lm.astype(np.float64) if wdtype == "f32" else \
+        torch.from_numpy(lm.astype(np.int16)).view(torch.bfloat16).double().numpy()
+    toks = synth.host_tokens(7, shape.vocab, stream=5)
+    s = oracle.OracleSession(om, 16)
+    rc, logits, hidden = s.prefill(toks, want_hidden=True)
+    assert rc == 0 and hidden.shape == (7, shape.hidden)
+    ref = W @ hidden[-1]
+    assert np.allclose(logits, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert not np.allclose(logits, W @ hidden[0], rtol=1e-3)
+    rc, logits2, h2 = s.decode(int(toks[0]), want_hidden=True)
+    assert rc == 0
+    ref2 = W @ h2
+    assert np.allclose(logits2, ref2, rtol=1e-12, atol=1e-12 * np.abs(ref2).max())
 
 
 def test_truncate_then_suffix_equals_scratch_prefill():
