@@ -88,6 +88,7 @@ def lib():
             "orc_router": ([vp, vp, vp, vp, vp, vp], None),
             "orc_swiglu_expert": ([vp, vp, vp, vp, vp, vp, vp], None),
             "orc_layer_step": ([vp, vp, vp, i32, vp, vp], None),
+            "orc_layer_step_ids": ([vp, vp, vp, i32, vp, vp, vp], None),
             "orc_lm_head": ([vp, vp, vp, vp], None),
             "orc_argmax": ([vp, i32], C.c_int32),
             "orc_sample": ([vp, i32, d, d, d, vp], C.c_int32),
@@ -232,6 +233,15 @@ def layer_step(cfg: Config, layer: Layer, kv: KV, pos: int, x: np.ndarray, trace
     assert x.dtype == np.float64 and x.flags["C_CONTIGUOUS"]
     lib().orc_layer_step(C.byref(cfg), C.byref(layer), C.byref(kv), pos, x.ctypes.data,
                          C.byref(trace) if trace is not None else None)
+
+
+def layer_step_ids(cfg: Config, layer: Layer, kv: KV, pos: int, x: np.ndarray, ids, trace=None):
+    """layer_step with the router's choice given (K expert ids in combine order)."""
+    assert x.dtype == np.float64 and x.flags["C_CONTIGUOUS"]
+    a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    assert a.shape == (cfg.top_k,)
+    lib().orc_layer_step_ids(C.byref(cfg), C.byref(layer), C.byref(kv), pos, x.ctypes.data,
+                             C.byref(trace) if trace is not None else None, a.ctypes.data)
 
 
 def sample(logits: np.ndarray, temperature: float, top_p: float, u: float, min_p: float = 0.0):

@@ -222,6 +222,15 @@ void orc_swiglu_expert(const orc_config *c, const void *wg, const void *wu, cons
 void orc_layer_step(const orc_config *c, const orc_layer *L, orc_kv *kv, int pos, double *x,
                     orc_trace *t)
 {
+    orc_layer_step_ids(c, L, kv, pos, x, t, NULL);
+}
+
+/* The same layer step with the router's choice given (ids_in: K distinct experts
+ * in combine order) instead of the top-k of the scores; their weights are the
+ * softmax over their own scores, as orc_router computes them.  NULL: the top-k. */
+void orc_layer_step_ids(const orc_config *c, const orc_layer *L, orc_kv *kv, int pos, double *x,
+                        orc_trace *t, const int32_t *ids_in)
+{
     int H = c->hidden, NH = c->n_heads, HD = c->head_dim, RQ = c->q_rank, RKV = c->kv_rank;
     int E = c->n_experts, K = c->top_k, I = c->expert_inter, dt = c->weight_dtype;
     size_t QD = (size_t)NH * HD;
@@ -258,6 +267,15 @@ void orc_layer_step(const orc_config *c, const orc_layer *L, orc_kv *kv, int pos
     /* MoE half: norm, router, top-k, weighted routed experts + shared, residual */
     orc_rmsnorm(H, x, L->ffn_norm, c->rms_eps, xn2);
     orc_router(c, L, xn2, scores, ids, w);
+    if (ids_in) {
+        double sum = 0.0;
+        for (int s = 0; s < K; s++) {
+            ids[s] = ids_in[s];
+            w[s] = exp((double)scores[ids[s]] - (double)scores[ids[0]]);
+            sum += w[s];
+        }
+        for (int s = 0; s < K; s++) w[s] /= sum;
+    }
     for (int s = 0; s < K; s++) {
         size_t e = (size_t)ids[s];
         orc_swiglu_expert(c, woff(dt, L->w_gate, e * I * H), woff(dt, L->w_up, e * I * H),

@@ -147,6 +147,12 @@ void orc_swiglu_expert(const orc_config *c, const void *wg, const void *wu, cons
                        const double *xn, double *h, double *y);
 void orc_layer_step(const orc_config *c, const orc_layer *L, orc_kv *kv, int pos, double *x,
                     orc_trace *t);
+/* orc_layer_step with the router's choice given: ids (K distinct experts, combine
+ * order) replace the top-k; the weights are the softmax over their scores.  For
+ * checking a result whose k-th and (k+1)-th scores lie within rounding of each
+ * other, where either choice is the method's result.  ids == NULL: orc_layer_step. */
+void orc_layer_step_ids(const orc_config *c, const orc_layer *L, orc_kv *kv, int pos, double *x,
+                        orc_trace *t, const int32_t *ids);
 void orc_lm_head(const orc_config *c, const void *lm, const double *x, double *logits);
 
 /* ---- sampler ---- */

@@ -353,6 +353,58 @@ def test_layer_step_wiring_against_library_routines():
     assert np.allclose(x1, t["x_mid"] + moe, rtol=1e-12)
 
 
+def test_layer_step_with_given_router_choice():
+    """orc_layer_step_ids: with the oracle's own top-k (or NULL) it is orc_layer_step
+    bit for bit; with another choice of experts (the k-th swapped for the (k+1)-th,
+    combined in the given order) the MoE output is the library computation of
+    sum_s softmax(scores[ids])_s * expert_s(xn2) + shared(xn2)."""
+    rng = np.random.default_rng(19)
+    shape = tiny_cfg(window=3)
+    w = random_layer(shape, rng)
+    H, HD, Kk = shape.hidden, shape.head_dim, shape.top_k
+    n_ctx, pos = 8, 5
+    K0 = rng.standard_normal((n_ctx, HD)).astype(np.float32)
+    V0 = rng.standard_normal((n_ctx, HD)).astype(np.float32)
+    x0 = rng.standard_normal(H)
+    x_ref, t_ref = run_layer(shape, w, x0, pos, K0.copy(), V0.copy())
+    cfg = oracle.config_from(shape)
+    lay = oracle.layer_struct(w)
+
+    def run_ids(ids):
+        K, V = K0.copy(), V0.copy()
+        kv = oracle.KV(K.ctypes.data, V.ctypes.data)
+        tr, bufs = oracle.make_trace(cfg)
+        x = x0.copy()
+        if ids is None:
+            L.orc_layer_step_ids(C.byref(cfg), C.byref(lay), C.byref(kv), pos, p(x), C.byref(tr),
+                                 None)
+        else:
+            oracle.layer_step_ids(cfg, lay, kv, pos, x, ids, tr)
+        return x, bufs
+
+    for ids in (None, t_ref["ids"].copy()):
+        x, t = run_ids(ids)
+        assert np.array_equal(x, x_ref) and np.array_equal(t["weights"], t_ref["weights"])
+    order = np.argsort(-t_ref["scores"], kind="stable")
+    alt = np.concatenate([order[:Kk - 1], order[Kk:Kk + 1]])[::-1].astype(np.int32)
+    x, t = run_ids(alt)
+    assert np.array_equal(t["ids"], alt)
+    W = {k: v.astype(np.float64) for k, v in w.items()}
+    wt = scipy.special.softmax(t_ref["scores"][alt].astype(np.float64))
+    assert np.allclose(t["weights"], wt, rtol=1e-12)
+
+    def expert(wg, wu, wd):
+        g, u = wg @ t["xn2"], wu @ t["xn2"]
+        return wd @ (torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u)
+
+    moe = sum(wt[s] * expert(W["w_gate"][e], W["w_up"][e], W["w_down"][e])
+              for s, e in enumerate(alt))
+    moe = moe + expert(W["ws_gate"], W["ws_up"], W["ws_down"])
+    assert np.allclose(t["moe"], moe, rtol=1e-12)
+    assert np.allclose(x, t_ref["x_mid"] + moe, rtol=1e-12)
+    assert not np.allclose(x, x_ref, rtol=1e-6)
+
+
 def test_layer_step_with_zero_outputs_is_identity():
     rng = np.random.default_rng(10)
     shape = tiny_cfg()
