@@ -224,7 +224,9 @@ int ds4g_session_save(ds4g_session *s, void *buf, size_t bytes);
  * of the same configuration: DS4G_EINVAL on a header or configuration mismatch,
  * DS4G_ESIZE if bytes is shorter than the checkpoint, DS4G_ECONTEXT if its length
  * is >= n_ctx, DS4G_ETOKEN if a token is out of range; the session is unchanged on
- * any of these.  Synchronises the session stream. */
+ * any of these.  If a copy to the device fails (DS4G_ECUDA), some layers' K/V rows
+ * may already be overwritten, so the session is emptied (len 0).  Synchronises the
+ * session stream. */
 int ds4g_session_load(ds4g_session *s, const void *buf, size_t bytes);
 
 /* Router decision of the last decoded token: ids (int32) and weights (f32) of
@@ -250,6 +252,19 @@ enum {
                                      entering each layer, then its final hidden state */
 };
 const void *ds4g_session_debug(const ds4g_session *s, int which);
+
+/* Record the residual stream at chosen positions, for teacher-forced checks of a
+ * layer against a reference ([P3] 阶段四 4.2: each layer maps the residual x of a
+ * position to the next layer's x).  positions: host array of n absolute session
+ * positions (copied; 0 <= position < n_ctx; n <= 64).  buf: device memory owned by
+ * the caller, n * (n_layers + 1) * hidden floats, which must outlive the setting.
+ * Whenever a later ds4g_prefill, ds4g_decode_step or ds4g_decode_layers computes
+ * positions[i], row i * (n_layers + 1) + l of buf receives the residual entering
+ * layer l (row l = 0: the widened embedding), and row l = n_layers the final
+ * hidden state.  n = 0 turns recording off.  DS4G_EINVAL on a bad argument; the
+ * setting is then unchanged.  Recording adds device-to-device copies to a prefill
+ * and one store per element to a decode step. */
+int ds4g_session_set_probe(ds4g_session *s, const int32_t *positions, int n, float *buf);
 
 /* Synchronise the session stream and report the first device-side error since the
  * last call: DS4G_ETIMEOUT (a bounded wait gave up) or DS4G_ENONFINITE (a router
@@ -337,11 +352,13 @@ int32_t ds4g_sample_u_min_p(const float *logits, int n_vocab, float temperature,
  * Its scratch is a fixed 16 KB array in the library's device image, which exists
  * once the module is loaded; the call allocates nothing.  n_vocab above
  * DS4G_SAMPLE_STATIC_MAX_VOCAB returns DS4G_ESIZE; other arguments and the result
- * are as for ds4g_sample.  The first call on each device resolves the scratch
- * address (runtime set-up), so make it before any stream capture.  There is one
- * scratch per device: calls that overlap in time on one device (two host threads,
- * or two streams whose calls are not ordered) race on it and give undefined
- * results.  Synchronises `cuda_stream`. */
+ * are as for ds4g_sample.  Every call looks up the scratch's address on the
+ * current device (cudaGetSymbolAddress, which allocates nothing), so a device reset
+ * between calls is safe.  There is one scratch per device: calls that overlap in
+ * time on one device (two host threads, or two streams whose calls are not
+ * ordered) race on it and give undefined results.  The scratch keeps the last
+ * call's contents; each call clears the part that must start at zero.
+ * Synchronises `cuda_stream`. */
 int32_t ds4g_sample_static(const float *logits, int n_vocab, float temperature, float top_p,
                            uint64_t *rng_state, void *cuda_stream);
 

@@ -49,6 +49,9 @@ struct ds4g_session {
     uint64_t launches = 0;
     unsigned long long *trace = nullptr;
     int trace_events = 0;
+    float *last_x = nullptr;          // [L+1][H] layer inputs of the last prefilled token
+    std::vector<int32_t> probe_pos;   // positions whose layer inputs are recorded
+    float *probe_buf = nullptr;       // caller's [n][L+1][H] record buffer
     bool timing = false;
     cudaEvent_t ev[DS4G_K_COUNT][2];
     double t_ms[DS4G_K_COUNT] = {};
@@ -293,6 +296,7 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     b.h = (float *)take((size_t)(d.K + 1) * d.I * 4);
     b.logits = (float *)take((size_t)d.V * 4);
     b.counters = (unsigned *)take(64);
+    b.layer_x = nullptr;
     s->bar = (unsigned *)take(64);
     s->status = (int *)(s->bar + 4);
     s->qflag = (unsigned *)take((size_t)d.NH * 4);
@@ -304,7 +308,8 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     s->kv_host.insert(s->kv_host.end(), s->vc.begin(), s->vc.end());
     prefill_carve(d, prefill_P(m->cfg), base + L.pre, s->pb);
     s->pb.status = s->status;
-    s->pb.layer_x = layer_x;
+    s->pb.n_rec = 0;
+    s->last_x = layer_x;
     if (m->tc && tc_act_maps(d, s->pb, s->tcact)) {
         delete s;
         return DS4G_ECUDA;
@@ -356,7 +361,21 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
     const int P = s->pb.P;
     for (int c = 0; c < n; c += P) {
         const int nc = n - c < P ? n - c : P;
-        s->pb.rec_row = c + nc == n ? nc - 1 : -1;   // record the last token's layer inputs
+        // record the last token's layer inputs, and those of probed positions in this chunk
+        s->pb.n_rec = 0;
+        if (c + nc == n) {
+            s->pb.rec_row[0] = nc - 1;
+            s->pb.rec_dst[0] = s->last_x;
+            s->pb.n_rec = 1;
+        }
+        if (s->probe_buf)
+            for (size_t i = 0; i < s->probe_pos.size(); ++i) {
+                const int r = s->probe_pos[i] - (s->len + c);
+                if (r < 0 || r >= nc) continue;
+                s->pb.rec_row[s->pb.n_rec] = r;
+                s->pb.rec_dst[s->pb.n_rec] = s->probe_buf + i * (size_t)(d.L + 1) * d.H;
+                ++s->pb.n_rec;
+            }
         cudaError_t e = cudaMemcpyAsync(s->pb.tok, tokens + c, (size_t)nc * 4,
                                         cudaMemcpyHostToDevice, s->st);
         if (!e)
@@ -385,6 +404,10 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
     if (token < 0 || token >= d.V) return DS4G_ETOKEN;
     if (s->len + 1 >= s->n_ctx) return DS4G_ECONTEXT;
     LaunchScope scope(s);
+    float *rec = nullptr;   // layer inputs of this position, when it is probed
+    if (s->probe_buf)
+        for (size_t i = 0; i < s->probe_pos.size(); ++i)
+            if (s->probe_pos[i] == s->len) rec = s->probe_buf + i * (size_t)(d.L + 1) * d.H;
     if (s->m->persistent && !s->timing) {
         PersistArgs pa;
         memset(&pa, 0, sizeof(pa));
@@ -394,6 +417,7 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
         pa.vc = s->kv_dev + d.L;
         pa.rope = s->rope;
         pa.b = s->b;
+        pa.b.layer_x = rec;
         pa.tok_embd = s->m->tok_embd;
         pa.lm_head = s->m->lm_head;
         pa.pos = s->len;
@@ -420,6 +444,7 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
     }
     StepArgs a = step_base(s);
     a.pos = s->len;
+    a.b.layer_x = rec;   // row 0 (the embedding) is written by the first kernel
     cudaEvent_t(*ev)[2] = s->timing ? s->ev : nullptr;
     for (int l = 0; l < d.L; ++l) {
         a.w = s->m->layers[l];
@@ -428,6 +453,9 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
         a.layer = l;
         a.token = l == 0 ? token : -1;
         if (decode_layer(a, s->st, s->m->nsm, ev)) return DS4G_ECUDA;
+        if (rec && cudaMemcpyAsync(rec + (size_t)(l + 1) * d.H, s->b.x, (size_t)d.H * 4,
+                                   cudaMemcpyDeviceToDevice, s->st))
+            return DS4G_ECUDA;
         if (ev) {  // read this layer's kernel times before the events are reused
             if (cudaStreamSynchronize(s->st)) return DS4G_ECUDA;
             for (int k = 0; k <= DS4G_K_EXPERT_DOWN; ++k) {
@@ -638,7 +666,12 @@ int ds4g_session_load(ds4g_session *s, const void *buf, size_t bytes)
         p += rows;
     }
     if (!e) e = cudaStreamSynchronize(s->st);
-    if (e) return cuda_status(e);
+    if (e) {
+        // Some layers' K/V rows may already be overwritten: the cache no longer
+        // matches the history, so the session is emptied.
+        s->len = 0;
+        return cuda_status(e);
+    }
     if (n) memcpy(s->hist.data(), tok, (size_t)n * 4);
     s->len = n;
     return DS4G_OK;
@@ -671,7 +704,7 @@ const void *ds4g_session_debug(const ds4g_session *s, int which)
     case DS4G_DBG_HIDDEN: return s->b.x;
     case DS4G_DBG_PREFILL_X: return s->pb.X;
     case DS4G_DBG_STATUS: return s->status;
-    case DS4G_DBG_PREFILL_LAYER_X: return s->pb.layer_x;
+    case DS4G_DBG_PREFILL_LAYER_X: return s->last_x;
     default: return nullptr;
     }
 }
@@ -713,6 +746,16 @@ int ds4g_session_set_timing(ds4g_session *s, int on)
         }
         s->timing = false;
     }
+    return DS4G_OK;
+}
+
+int ds4g_session_set_probe(ds4g_session *s, const int32_t *positions, int n, float *buf)
+{
+    if (!s || n < 0 || n > kMaxProbe || (n > 0 && (!positions || !buf))) return DS4G_EINVAL;
+    for (int i = 0; i < n; ++i)
+        if (positions[i] < 0 || positions[i] >= s->n_ctx) return DS4G_EINVAL;
+    s->probe_pos.assign(positions, positions + n);
+    s->probe_buf = n > 0 ? buf : nullptr;
     return DS4G_OK;
 }
 

@@ -43,6 +43,8 @@ struct DecodeBufs {
     float *hidden;   // [H]   final hidden state
     unsigned *counters;  // [8] grid-completion tickets (reset by their last user)
     int *status;         // session status word (DS4G_* error raised on the device)
+    float *layer_x;      // optional [L+1][H]: the residual entering each layer (row 0 the
+                         // embedding), then the final hidden state; null: not recorded
 };
 
 // Arguments of every decode kernel: one layer at one position.

@@ -41,8 +41,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_qkv_a(StepArgs a)
         ss = load_f16_sumsq(a.tok_embd + (size_t)a.token * H, xs, H);
         __syncthreads();
         if (blockIdx.x == 0)
-            for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4)
+            for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
                 *reinterpret_cast<float4 *>(a.b.x + i) = *reinterpret_cast<float4 *>(xs + i);
+                if (a.b.layer_x)   // recorded input of layer 0
+                    *reinterpret_cast<float4 *>(a.b.layer_x + i) = *reinterpret_cast<float4 *>(xs + i);
+            }
     } else {
         ss = load_f32_sumsq(a.b.x, xs, H);
     }

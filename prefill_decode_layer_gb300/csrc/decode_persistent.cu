@@ -983,8 +983,10 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                 prefetch_l2(kc + (size_t)lo_w * d.HD, (uint32_t)bytes);
                 prefetch_l2(vc + (size_t)lo_w * d.HD, (uint32_t)bytes);
             }
-            float ss = l == 0 ? cload_f16_g<TW>(a.tok_embd + (size_t)a.token * H, w.attn_norm, xs, H,
-                                                blockIdx.x == 0 ? a.b.x : nullptr)
+            // the plain embedding row: the residual (CTA 0) and, when recorded, the
+            // input of layer 0 (the last CTA)
+            float *plain = blockIdx.x == 0 ? a.b.x : blockIdx.x == gridDim.x - 1 ? a.b.layer_x : nullptr;
+            float ss = l == 0 ? cload_f16_g<TW>(a.tok_embd + (size_t)a.token * H, w.attn_norm, xs, H, plain)
                               : cload_g<TW>(a.b.x, w.attn_norm, xs, H);
             const float inv = rsqrtf(csum(ss, S.red) / (float)H + d.eps);
             const Piece P[2] = {piece<TW>(w.wq_a, d.RQ, H), piece<TW>(w.wkv_a, d.RKV, H)};
@@ -1243,7 +1245,9 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                     const int slot = t == 0 ? K : t - 1;
                     tot = fmaf(S.w[slot], ybuf[((size_t)(b - lo) * (K + 1) + t) * RB + r], tot);
                 }
-                a.b.x[row] = __ldcg(a.b.xm + row) + tot;
+                const float xo = __ldcg(a.b.xm + row) + tot;
+                a.b.x[row] = xo;
+                if (a.b.layer_x) a.b.layer_x[(size_t)(l + 1) * H + row] = xo;
             }
         }
         if (l + 1 < d.L || a.logits)

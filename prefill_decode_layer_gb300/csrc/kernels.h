@@ -21,12 +21,15 @@ size_t sample_workspace_bytes(int n);
 // Fixed sampler scratch (ds4g_sample_static): vocabularies up to kSampleStaticMaxVocab.
 constexpr int kSampleStaticMaxVocab = 262144;
 constexpr size_t kSampleStaticBytes = 16384;
-constexpr int kMaxDevices = 64;
 cudaError_t sample_static_scratch(void **p);
 cudaError_t sample_launch(const float *logits, int n, float temperature, float top_p, float min_p,
                           unsigned u24, void *ws, cudaStream_t st, int **result_dev);
 
 // prefill.cu
+// Positions whose per-layer residual a session records (ds4g_session_set_probe),
+// plus the last prefilled token (DS4G_DBG_PREFILL_LAYER_X).
+constexpr int kMaxProbe = 64;
+constexpr int kMaxRec = kMaxProbe + 1;
 struct PrefillBufs {
     int P;            // chunk capacity (tokens)
     int *tok;         // [P]
@@ -48,8 +51,11 @@ struct PrefillBufs {
     void *HS;         // [P][I] shared SwiGLU hidden
     float *YS;        // [P*K][H] routed expert outputs, token-slot order
     int *status;      // session status word (set after carving)
-    float *layer_x;   // [L+1][H]: residual of chunk row rec_row entering each layer, then final
-    int rec_row;      // chunk row to record (-1: none)
+    // Recorded rows: the residual of chunk row rec_row[i] entering each layer l, then
+    // the final hidden state, is copied to rec_dst[i] + l * H ([L+1][H] each).
+    int n_rec;
+    int rec_row[kMaxRec];
+    float *rec_dst[kMaxRec];
 };
 // Entries per segment of the counting sort that groups (token, slot) entries by expert.
 static constexpr int kSortSeg = 512;

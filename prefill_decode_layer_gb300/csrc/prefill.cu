@@ -403,10 +403,10 @@ static cudaError_t chunk_t(const Dims &d, const LayerPtrs *layers, void *const *
     ++launch_count();
     if ((e = cudaGetLastError())) return e;
     for (int l = 0; l <= d.L; ++l) {
-        if (pb.rec_row >= 0 && pb.layer_x &&
-            (e = cudaMemcpyAsync(pb.layer_x + (size_t)l * H, pb.X + (size_t)pb.rec_row * H, (size_t)H * 4,
-                                 cudaMemcpyDeviceToDevice, st)))
-            return e;
+        for (int i = 0; i < pb.n_rec; ++i)
+            if ((e = cudaMemcpyAsync(pb.rec_dst[i] + (size_t)l * H, pb.X + (size_t)pb.rec_row[i] * H,
+                                     (size_t)H * 4, cudaMemcpyDeviceToDevice, st)))
+                return e;
         if (l == d.L) break;
         const LayerPtrs &w = layers[l];
         TKV *kc = (TKV *)kcs[l], *vc = (TKV *)vcs[l];

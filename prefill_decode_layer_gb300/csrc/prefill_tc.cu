@@ -573,10 +573,10 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
     if ((e = launch_pdl(k_embed_rows, dim3(n), dim3(256), 0, st, tok_embd, (const int *)pb.tok, pb.X, H))) return e;
     bool normed = false;   // xn holds the next layer's attention RMSNorm already
     for (int l = 0; l <= d.L; ++l) {
-        if (pb.rec_row >= 0 && pb.layer_x &&
-            (e = cudaMemcpyAsync(pb.layer_x + (size_t)l * H, pb.X + (size_t)pb.rec_row * H, (size_t)H * 4,
-                                 cudaMemcpyDeviceToDevice, st)))
-            return e;
+        for (int i = 0; i < pb.n_rec; ++i)
+            if ((e = cudaMemcpyAsync(pb.rec_dst[i] + (size_t)l * H, pb.X + (size_t)pb.rec_row[i] * H,
+                                     (size_t)H * 4, cudaMemcpyDeviceToDevice, st)))
+                return e;
         if (l == d.L) break;
         const LayerPtrs &w = layers[l];
         const TcLayerMaps &m = lm[l];

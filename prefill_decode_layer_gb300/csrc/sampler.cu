@@ -20,7 +20,6 @@
 // T <= 0.   argmax: max of (ordered logit bits, inverted index) as one u64.
 #include "common.cuh"
 #include <cstring>
-#include <mutex>
 
 #include "kernels.h"
 
@@ -368,23 +367,16 @@ static __device__ __align__(256) unsigned char g_sample_scratch[kSampleStaticByt
 static_assert(kSampleStaticBytes >= sizeof(SampleWS) + ((kSampleStaticMaxVocab + kChunk - 1) / kChunk) * 12 + 256,
               "static sampler scratch too small for its maximum vocabulary");
 
-// Device address of the fixed scratch on the current device.  The first call per
-// device resolves the symbol (runtime set-up); later calls reuse the cached value.
+// Device address of the fixed scratch on the current device, looked up on every
+// call.  The lookup allocates nothing and is cheap once the module is loaded; a
+// cached address would go stale if the caller reset the device or destroyed its
+// primary context, after which the module (and the array) can be loaded elsewhere.
 cudaError_t sample_static_scratch(void **p)
 {
-    static std::mutex mu;
-    static void *addr[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *a = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_sample_scratch);
     if (e) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> g(mu);
-    if (!addr[dev]) {
-        void *a = nullptr;
-        if ((e = cudaGetSymbolAddress(&a, g_sample_scratch))) return e;
-        addr[dev] = a;
-    }
-    *p = addr[dev];
+    *p = a;
     return cudaSuccess;
 }
 

@@ -88,6 +88,7 @@ def lib():
             "ds4g_session_launches": ([vp], C.c_uint64),
             "ds4g_session_status": ([vp], i32),
             "ds4g_session_set_trace": ([vp, vp, sz], i32),
+            "ds4g_session_set_probe": ([vp, vp, i32, vp], i32),
             "ds4g_session_set_timing": ([vp, i32], i32),
             "ds4g_session_timing": ([vp, vp, vp, i32], i32),
             "ds4g_sample": ([vp, i32, C.c_float, C.c_float, vp, vp, sz, vp], C.c_int32),
@@ -270,6 +271,20 @@ class Session:
         _check(lib().ds4g_session_set_trace(self.ptr, buf.data_ptr() if buf is not None else None,
                                             buf.numel() * buf.element_size() if buf is not None
                                             else 0), "ds4g_session_set_trace")
+
+    def set_probe(self, positions) -> torch.Tensor | None:
+        """Record the residual entering every layer (then the final hidden state) at
+        the given session positions during later prefills and decode steps.  Returns
+        the device buffer [n][L+1][H] (f32) the rows go to; an empty list stops it."""
+        pos = (C.c_int32 * len(positions))(*[int(p) for p in positions])
+        s = self.model.shape
+        buf = torch.full((len(positions), s.n_layers + 1, s.hidden), float("nan"),
+                         dtype=torch.float32, device="cuda") if len(positions) else None
+        _check(lib().ds4g_session_set_probe(self.ptr, pos, len(positions),
+                                            buf.data_ptr() if buf is not None else None),
+               "ds4g_session_set_probe")
+        self._probe = buf   # kept alive while the setting holds
+        return buf
 
     def status(self) -> int:
         return lib().ds4g_session_status(self.ptr)

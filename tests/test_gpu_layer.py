@@ -45,7 +45,7 @@ def test_seeded_kv_matches_host_generator(layer_setup):
 def test_decode_steps_match_oracle(layer_setup):
     import torch
     shape, gm, sess, om, kv = layer_setup
-    toks = synth.host_tokens(3, shape.vocab, stream=5)
+    toks = synth.host_tokens(8, shape.vocab, stream=5)
     H, QD, K, I = shape.hidden, shape.n_heads * shape.head_dim, shape.top_k, shape.expert_inter
     ties = 0
     for s, t in enumerate(toks):
@@ -72,5 +72,6 @@ def test_decode_steps_match_oracle(layer_setup):
             assert rel_err(to_np(sess.hidden()), x) <= TOL_BF16
         else:
             ties += 1
-    assert ties <= 1
+    print(f"{len(toks)} decode steps, {ties} with the router in the tie band")
+    assert ties <= 2
     assert sess.status() == 0

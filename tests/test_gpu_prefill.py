@@ -1,14 +1,13 @@
 """Layer-major prefill on the GPU: parity with the oracle on a small BF16 model over
 several ragged chunks, chunk-size invariance, truncate + suffix == scratch prefill
-(bit for bit), decode after prefill, error codes; and the first positions of the
-full-width 8-layer, 4096-token prefill against the oracle."""
+(bit for bit), decode after prefill, error codes.  The full-width 8-layer,
+4096-token prefill is checked in test_gpu_stack.py."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from helpers import (TOL_BF16, LazyOracleModel, OracleKV, gpu_model, kv_to_f64, oracle_embed,
-                     oracle_layer, rel_err, to_np)
+from helpers import TOL_BF16, LazyOracleModel, gpu_model, kv_to_f64, rel_err, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -250,41 +249,3 @@ def test_tensor_core_and_simt_prefill_agree():
     for l in range(SMALL_TC.n_layers):
         assert rel_err(to_np(a.kv(l)[0][:150]), to_np(b.kv(l)[0][:150])) <= TOL_BF16
         assert rel_err(to_np(a.kv(l)[1][:150]), to_np(b.kv(l)[1][:150])) <= TOL_BF16
-
-
-def test_full_width_8_layer_prefill_first_positions():
-    """4096-token layer-major prefill of the 8-layer full-width model; the oracle
-    recomputes the first positions through all 8 layers (hidden states and KV)."""
-    import torch
-    import prefill_decode_layer_gb300 as pdl
-    shape = synth.STACK
-    gm = gpu_model(shape)
-    toks = synth.host_tokens(4096, shape.vocab, stream=31)
-    sess = pdl.Session(gm, 4200)
-    assert sess.prefill(toks) == 0
-    torch.cuda.synchronize()
-    npos = 3
-    om = LazyOracleModel(shape, keep_layers=True)
-    kv = OracleKV(shape, npos + 1)
-    X = [oracle_embed(om, t) for t in toks[:npos]]
-    # A router decision within the tie band makes everything downstream of it
-    # (that position and, through attention, later ones) undecidable.
-    valid = npos
-    checked = 0
-    for l in range(shape.n_layers):
-        trs = [oracle_layer(om, kv, l, p, X[p], trace=True) for p in range(npos)]
-        om._layers.clear()
-        gk, gv = kv_np(sess, l, npos)
-        if valid > 0:
-            assert rel_err(gk[:valid], kv_to_f64(shape, kv.k[l][:valid])) <= TOL_BF16, f"layer {l}"
-            assert rel_err(gv[:valid], kv_to_f64(shape, kv.v[l][:valid])) <= TOL_BF16, f"layer {l}"
-            checked += 1
-        for p in range(valid):
-            srt = np.sort(trs[p]["scores"].astype(np.float64))[::-1]
-            if srt[shape.top_k - 1] - srt[shape.top_k] <= 1e-3 * np.max(np.abs(srt)):
-                valid = p
-                break
-    assert checked >= 4
-    if valid > 0:
-        px = to_np(sess.debug("prefill_x", valid * shape.hidden)).reshape(valid, shape.hidden)
-        assert rel_err(px, np.stack(X[:valid])) <= TOL_BF16

@@ -13,8 +13,9 @@ pytestmark = pytest.mark.gpu
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def undecidable(info, token: int) -> bool:
-    """Draws whose token the device may legitimately choose differently.
+def undecided_band(info, token: int) -> float:
+    """Width (in units of the kept total) of the band around u * total in which the
+    device may legitimately choose a different token; 0 when the draw is decided.
 
     The device computes each p in f32 (z = l / T, exp(z - max z)): a relative error
     of at most ~2e-6 per token, independent across tokens, so a cumulative sum
@@ -32,16 +33,28 @@ def undecidable(info, token: int) -> bool:
         first = min(i for i in (info.cut_index, info.cut_next_index) if i >= 0)
         if token >= first:
             band += info.cut_p
-    return info.cdf_margin < band
+    return band if info.cdf_margin < band else 0.0
 
 
-def undecidable_min_p(info, token: int) -> bool:
-    """As undecidable(), and a token of the top-p set whose p lies within f32 noise
-    (4e-6 relative) of the min-p bound may be kept on one side and not the other:
-    that moves the kept total by up to that token's p (at most min_p * max p)."""
+def undecided_band_min_p(info, token: int, min_p: float) -> float:
+    """As undecided_band(); besides, a token of the top-p set whose p lies within f32
+    noise (4e-6 relative) of the min-p bound may be kept on one side and not the
+    other, which moves the kept total and the CDF by up to that token's p (at most
+    min_p times the largest p, so at most min_p of the kept total)."""
     if info.minp_margin < 4e-6:
+        return 8e-6 * info.p_rms + 2.0 * min_p
+    return undecided_band(info, token)
+
+
+def within_band(host, T, top_p, u, band, tok, info, min_p=0.0) -> bool:
+    """The device's token of an undecided draw lies among the tokens the oracle
+    draws for uniforms in [u - band, u + band] (the walk is monotone in u for a
+    fixed kept set), or is the crossing token or the one after it in top-p order."""
+    if tok in (info.cut_index, info.cut_next_index):
         return True
-    return undecidable(info, token)
+    lo = oracle.sample(host, T, top_p, max(0.0, u - band), min_p=min_p)[0]
+    hi = oracle.sample(host, T, top_p, min(1.0 - 2.0 ** -53, u + band), min_p=min_p)[0]
+    return lo <= tok <= hi
 
 
 def workspace(n):
@@ -77,11 +90,16 @@ def test_greedy_matches_argmax_and_ties_go_low():
 
 
 # stream 9 at (2.0, 0.7, 0.95) puts the top-p target within f32 noise of a cut boundary
-# (an undecidable kept set); the other instances have clear cuts.
-@pytest.mark.parametrize("sigma,T,top_p,stream", [(2.0, 0.7, 0.95, 10), (2.0, 0.7, 0.95, 9),
-                                                  (1.0, 1.0, 1.0, 10), (3.0, 0.5, 0.5, 10),
-                                                  (0.3, 1.3, 0.9, 10)])
-def test_draws_match_oracle(sigma, T, top_p, stream):
+# (an undecidable kept set): 66 of its 300 draws are undecided.  The other instances
+# have clear cuts; their undecided draws are those whose u * total falls within the
+# f32 noise of a CDF boundary: 0 of 300, except 5 of 300 for top-p = 1 over the flat
+# sigma = 1 logits (129280 tokens of p ~ 8e-6 each, so the boundaries are dense).
+# The limits are those counts plus one or two draws.
+@pytest.mark.parametrize("sigma,T,top_p,stream,max_undecided",
+                         [(2.0, 0.7, 0.95, 10, 2), (2.0, 0.7, 0.95, 9, 90),
+                          (1.0, 1.0, 1.0, 10, 7), (3.0, 0.5, 0.5, 10, 2),
+                          (0.3, 1.3, 0.9, 10, 2)])
+def test_draws_match_oracle(sigma, T, top_p, stream, max_undecided):
     import torch
     import prefill_decode_layer_gb300 as pdl
     from synth import torch_weights as tw
@@ -91,18 +109,23 @@ def test_draws_match_oracle(sigma, T, top_p, stream):
     host = synth.host_logits(V, sigma, stream=stream)
     assert np.array_equal(dev.cpu().numpy(), host)
     state = 0x9E3779B97F4A7C15
-    n, ambiguous = 300, 0
+    n, undecided, differ = 300, 0, 0
     for i in range(n):
         tok, new_state = pdl.sample(dev, T, top_p, state, ws)
         u, ostate = oracle.uniform(state)
         assert new_state == ostate
         otok, info = oracle.sample(host, T, top_p, u)
-        if undecidable(info, otok):
-            ambiguous += 1
+        band = undecided_band(info, otok)
+        if band > 0.0:
+            undecided += 1
+            differ += tok != otok
+            assert within_band(host, T, top_p, u, band, tok, info), f"draw {i}: {tok} vs {otok}"
         else:
             assert tok == otok, f"draw {i}: {tok} vs {otok} (u={u})"
         state = new_state
-    assert ambiguous <= (3 * n) // 10, ambiguous   # the rest (>= 70%) matched exactly
+    print(f"sigma={sigma} T={T} top_p={top_p} stream={stream}: {undecided} of {n} draws "
+          f"undecided, {differ} of them differ")
+    assert undecided <= max_undecided, undecided
 
 
 def test_min_p_hand_derived_cases_on_device():
@@ -120,9 +143,12 @@ def test_min_p_hand_derived_cases_on_device():
     assert pdl.sample_u(t, 1.0, 1.0, 5, ws, min_p=1.5) == pdl.ds4g.EINVAL
 
 
-@pytest.mark.parametrize("sigma,T,top_p,min_p", [(2.0, 0.7, 0.95, 0.05), (1.0, 1.0, 1.0, 0.2),
-                                                 (3.0, 0.5, 0.9, 0.01), (0.3, 1.3, 1.0, 0.9)])
-def test_min_p_draws_match_oracle(sigma, T, top_p, min_p):
+# Undecided counts of these instances (oracle only): 9 of 200 for the first (tokens
+# of the top-p set within f32 noise of the min-p bound), 0 for the others.
+@pytest.mark.parametrize("sigma,T,top_p,min_p,max_undecided",
+                         [(2.0, 0.7, 0.95, 0.05, 10), (1.0, 1.0, 1.0, 0.2, 2),
+                          (3.0, 0.5, 0.9, 0.01, 2), (0.3, 1.3, 1.0, 0.9, 2)])
+def test_min_p_draws_match_oracle(sigma, T, top_p, min_p, max_undecided):
     import torch
     import prefill_decode_layer_gb300 as pdl
     from synth import torch_weights as tw
@@ -131,15 +157,21 @@ def test_min_p_draws_match_oracle(sigma, T, top_p, min_p):
     dev = tw.dev_logits(V, sigma, stream_id=12)
     host = synth.host_logits(V, sigma, stream=12)
     state = 0x9E3779B97F4A7C15
-    n, ambiguous = 200, 0
+    n, undecided, differ = 200, 0, 0
     for i in range(n):
         tok, new_state = pdl.sample(dev, T, top_p, state, ws, min_p=min_p)
         u, ostate = oracle.uniform(state)
         assert new_state == ostate
         otok, info = oracle.sample(host, T, top_p, u, min_p=min_p)
-        if undecidable_min_p(info, otok):
-            ambiguous += 1
+        band = undecided_band_min_p(info, otok, min_p)
+        if band > 0.0:
+            undecided += 1
+            differ += tok != otok
+            assert within_band(host, T, top_p, u, band, tok, info, min_p), \
+                f"draw {i}: {tok} vs {otok}"
         else:
             assert tok == otok, f"draw {i}: {tok} vs {otok} (u={u})"
         state = new_state
-    assert ambiguous <= (3 * n) // 10, ambiguous
+    print(f"sigma={sigma} T={T} top_p={top_p} min_p={min_p}: {undecided} of {n} draws "
+          f"undecided, {differ} of them differ")
+    assert undecided <= max_undecided, undecided

@@ -53,3 +53,27 @@ def test_static_sampler_rejects_vocab_above_limit():
     assert L.ds4g_sample_static(C.c_void_p(logits.data_ptr()), MAX_VOCAB + 1, 0.7, 0.9,
                                 C.byref(st), stream) == DS4G_ESIZE
     assert st.value == 1   # rejected before the draw
+
+
+def test_static_sampler_allocates_no_device_memory():
+    """After one warm-up call per sampler path (which loads the library's kernels
+    and its fixed scratch, lazily, on first use), further calls at the largest
+    vocabulary leave the device's free memory unchanged."""
+    import torch
+    from prefill_decode_layer_gb300 import ds4g
+    L = ds4g.lib()
+    logits = _logits(MAX_VOCAB, seed=7)
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = C.c_uint64(0x9E3779B97F4A7C15)
+    cases = [(0.0, 1.0), (1.0, 1.0), (0.7, 0.95)]
+    for temperature, top_p in cases:   # warm-up: every kernel of the path is loaded
+        assert L.ds4g_sample_static(C.c_void_p(logits.data_ptr()), MAX_VOCAB, temperature, top_p,
+                                    C.byref(st), stream) >= 0
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        for temperature, top_p in cases:
+            assert L.ds4g_sample_static(C.c_void_p(logits.data_ptr()), MAX_VOCAB, temperature,
+                                        top_p, C.byref(st), stream) >= 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
