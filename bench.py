@@ -186,23 +186,29 @@ def cpu_model():
     return "unknown"
 
 
-def oracle_decode_rate(m: synth.ModelShape, n_pre: int, seconds: float, seed: int = 0):
-    """Oracle decode steps/s on the single-layer workload (one thread), bounded by time."""
+def oracle_decode_rate(m: synth.ModelShape, n_pre: int, seconds: float, seed: int = 0,
+                       steps: int = 256, warmup: int = 0):
+    """Oracle decode steps/s on the single-layer workload (one thread): `warmup`
+    untimed steps, then up to `steps` timed steps, stopping early once `seconds` have
+    passed.  Returns (rate, timed steps, seconds)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
     from helpers import LazyOracleModel, OracleKV, oracle_embed, oracle_layer
     om = LazyOracleModel(m.with_(n_layers=1), seed)
     om.layer(0)                                   # generate weights outside the timing
-    kv = OracleKV(m.with_(n_layers=1), n_pre + 256)
+    total = warmup + steps
+    kv = OracleKV(m.with_(n_layers=1), n_pre + total + 1)
     hk, hv = synth.host_kv(m, 0, n_pre, seed)
     kv.k[0][:n_pre] = hk
     kv.v[0][:n_pre] = hv
-    toks = synth.host_tokens(256, m.vocab, seed, stream=5)
+    toks = synth.host_tokens(total, m.vocab, seed, stream=5)
+    for i in range(warmup):
+        oracle_layer(om, kv, 0, n_pre + i, oracle_embed(om, toks[i]))
     t0 = time.perf_counter()
     n = 0
-    while n < 256:
-        x = oracle_embed(om, toks[n])
-        oracle_layer(om, kv, 0, n_pre + n, x)
+    while n < steps:
+        x = oracle_embed(om, toks[warmup + n])
+        oracle_layer(om, kv, 0, n_pre + warmup + n, x)
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
@@ -214,22 +220,27 @@ def oracle_decode_rate(m: synth.ModelShape, n_pre: int, seconds: float, seed: in
 # --------------------------------------------------------------------------- reference arm
 
 def run_reference(args) -> dict:
-    secs = float(os.environ.get("DS4G_REF_SECONDS", "40"))
+    """The oracle (single-threaded C, double precision) on the headline workload:
+    `warmup` untimed decode steps, then `steps` timed ones, the timed part cut short
+    after DS4G_REF_SECONDS (default 120 s); `steps` reports the steps it timed."""
+    secs = float(os.environ.get("DS4G_REF_SECONDS", "120"))
     m = synth.LAYER
-    # every step is one oracle decode step of the same workload; the run is bounded in time
-    budget_steps = args.warmup + args.steps
-    rate, n, dt = oracle_decode_rate(m, 4096, secs)
+    warm = min(args.warmup, 3)   # oracle warm-up: weights are generated outside the timing
+    rate, n, dt = oracle_decode_rate(m, 4096, secs, steps=args.steps, warmup=warm)
     value = rate
+    bounded = n < args.steps
     return {
         "metric": "decode tok/s (batch 1)", "value": value, "unit": "tok/s", "n_gpus": 0,
-        "steps": n, "warmup": 0, "ms_per_step": 1000.0 / value, "higher_is_better": True,
+        "steps": n, "warmup": warm, "ms_per_step": 1000.0 / value, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
         "config": workload_config(m),
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} of the requested {budget_steps} oracle decode steps "
+                         "sample": f"{n} timed oracle decode steps after {warm} untimed ones "
                                    f"(positions 4096.., {dt:.1f} s, single thread, "
-                                   f"{cpu_model()}, {nproc()} cores present)"},
+                                   f"{cpu_model()}, {nproc()} cores present)"
+                                   + (f"; time-bounded at {secs:.0f} s, {args.steps} requested"
+                                      if bounded else "")},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -356,6 +367,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the prefill / stack / resync measurements")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--min-seconds", type=float, default=1.25,
+                    help="the headline's K timed steps are repeated until the timed region "
+                         "lasts about this long")
     ap.add_argument("--timeline", action="store_true",
                     help="with --case decode-*: also print the kernel's stage start times")
     ap.add_argument("--case", default=None, choices=list(CASES),
@@ -405,15 +419,14 @@ def main():
     m1 = pdl.Model(layer, emb, lm, layers[:1])
     n_pre = 4096
     n_flushed = min(args.steps, 200)
-    n_ctx = n_pre + args.warmup + args.steps + n_flushed + 48 + 32 + 16
+    # positions: warm-up and each repeat of the timed steps restart at n_pre; then the
+    # flushed steps, the per-kernel timing pass (48) and the end-to-end steps (64)
+    n_ctx = n_pre + max(args.warmup, args.steps) + n_flushed + 48 + 64 + 16
     sess = pdl.Session(m1, n_ctx)
     k, v = sess.kv(0)
     tw.fill_kv(layer, 0, k, v, n_pre)
     assert sess.restore(synth.host_tokens(n_pre, layer.vocab, stream=11)) == 0
     toks = synth.host_tokens(args.warmup + args.steps + n_flushed + 64, layer.vocab, stream=5)
-    for i in range(args.warmup):
-        assert sess.decode_layers(int(toks[i])) == 0
-    torch.cuda.synchronize()
 
     def timed_steps(first, n, flush_l2):
         # CUDA events on the session's (current) stream; returns total ms.  Steps run back
@@ -443,18 +456,47 @@ def main():
         return sum(a.elapsed_time(b) for a, b in ev)
 
     # Headline: steps back to back.  Every step streams ~275 MB of weights, more than
-    # the 129 MB L2, so no weight is still cached when the next step reads it.
+    # the 129 MB L2, so no weight is still cached when the next step reads it.  The K
+    # steps are repeated R times, the session truncated back to its 4096 pre-filled
+    # positions between repeats (host bookkeeping only: nothing is launched, so the
+    # stream stays back to back), so that the timed region lasts at least about a
+    # second whatever K is and the clock samples cover it.
+    est = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    est[0].record(stream)
+    for i in range(args.warmup):
+        assert sess.decode_layers(int(toks[i])) == 0
+    est[1].record(stream)
+    torch.cuda.synchronize()
+    assert sess.truncate(n_pre) == 0
+    est_ms = est[0].elapsed_time(est[1]) / args.warmup
+    repeats = max(1, int(np.ceil(args.min_seconds * 1000.0 / (args.steps * est_ms))))
+
+    def timed_batches(n, reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for r in range(reps):
+            if r:
+                assert sess.truncate(n_pre) == 0
+            for i in range(n):
+                rc = sess.decode_layers(int(toks[args.warmup + i]))
+                if rc != 0:
+                    raise RuntimeError(f"decode failed: {rc}")
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
     torch.cuda.synchronize()
     launches0 = sess.launches
-    total_ms = timed_steps(args.warmup, args.steps, False)
+    total_ms = timed_batches(args.steps, repeats)
     barrier()
     clk = clocks.stop()
     gpu_launches = sess.launches - launches0
-    total_ms, value = replica_rate(total_ms, args.steps, dist)
-    ms_per_step = total_ms / args.steps
+    assert sess.status() == 0
+    total_ms, value = replica_rate(total_ms, args.steps * repeats, dist)
+    ms_per_step = total_ms / (args.steps * repeats)
     # Secondary: the same with a 512 MB L2 flush before every step (cold code and data).
     fl_ms = timed_steps(args.warmup + args.steps, n_flushed, True) / n_flushed
     flushed = {"ms_per_step": round(fl_ms, 5), "value": round(world * 1000.0 / fl_ms, 1),
@@ -485,33 +527,54 @@ def main():
                 "frac": round(achieved / hbm_peak, 4),
                 "peak_source": f"{peak_src} hbm_gbs (copy, read+write; burst)",
                 "traffic": ncu_traffic("k_decode_persistent"), "algorithmic_bytes": step_bytes,
-                "timing": "CUDA events around the timed steps (back to back), average per launch"}
+                "timing": "CUDA events around the timed region (R repeats of K back-to-back "
+                          "steps), average per launch"}
     staged = {"note": "one kernel per stage (decode_kernel=1), per-kernel CUDA events, "
                       "L2 flushed between steps", "per_kernel": per_kernel}
 
     # ---------------- end to end through the C ABI with host buffers
+    # Per step: the token comes from pinned host memory, the decode call is made, the
+    # 16 KB hidden state is copied to pinned host memory, and the stream is
+    # synchronised.  The host time splits into the call (argument marshalling and
+    # the launch), the copy's enqueue, and the wait for the device (kernel plus the
+    # copy and the synchronisation round trip).
     hidden_host = torch.empty(layer.hidden, dtype=torch.float32, pin_memory=True)
     tok_host = torch.tensor(toks[:64].astype(np.int32), dtype=torch.int32).pin_memory()
     x_dev = sess.hidden()
-    e2e_ms = []
-    for i in range(32):
+    e2e_ms, call_us, copy_us, wait_us = [], [], [], []
+    for i in range(64):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         rc = sess.decode_layers(int(tok_host[i].item()))
+        t1 = time.perf_counter()
         hidden_host.copy_(x_dev, non_blocking=True)
+        t2 = time.perf_counter()
         stream.synchronize()
-        e2e_ms.append((time.perf_counter() - t0) * 1000)
+        t3 = time.perf_counter()
         assert rc == 0
+        if i >= 8:
+            e2e_ms.append((t3 - t0) * 1000)
+            call_us.append((t1 - t0) * 1e6)
+            copy_us.append((t2 - t1) * 1e6)
+            wait_us.append((t3 - t2) * 1e6)
     e2e = {"value": round(1000.0 / statistics.mean(e2e_ms) * world, 1), "unit": "tok/s",
            "h2d_bytes_per_step": 4, "d2h_bytes_per_step": layer.hidden * 4,
-           "how": "host wall clock per step: decode call with the token from pinned host "
-                  "memory, hidden state copied back to pinned host memory, stream synchronised"}
+           "us_per_step": round(statistics.mean(e2e_ms) * 1000, 2),
+           "host_breakdown_us": {"decode_call": round(statistics.mean(call_us), 2),
+                                 "copy_enqueue": round(statistics.mean(copy_us), 2),
+                                 "wait_for_device": round(statistics.mean(wait_us), 2),
+                                 "device_step_back_to_back": round(ms_per_step * 1000, 2)},
+           "how": "host wall clock per step over 56 steps: decode call with the token from "
+                  "pinned host memory, hidden state copied back to pinned host memory, "
+                  "stream synchronised"}
     del sess, m1
 
     line = {
         "metric": "decode tok/s (batch 1)", "value": round(value, 1), "unit": "tok/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(ms_per_step, 5), "repeats": repeats,
+        "timed_steps": args.steps * repeats, "timed_ms": round(total_ms, 2),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator)",
         "config": workload_config(layer), "roofline": roofline, "staged_kernels": staged,
         "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clk,
@@ -520,7 +583,7 @@ def main():
 
     if extra:
         line.update(extra_measurements(pdl, tw, torch, stack, emb, lm, layers, flush, hbm_peak,
-                                       bf16_peak, bf16_sus))
+                                       bf16_peak, bf16_sus, local))
 
     if rank == 0:
         rate, n, dt = oracle_decode_rate(layer, n_pre, args.cpu_seconds)
@@ -536,68 +599,54 @@ def main():
 
 
 def extra_measurements(pdl, tw, torch, stack, emb, lm, layers, flush, hbm_peak, bf16_peak,
-                       bf16_sus):
+                       bf16_sus, local=0):
+    """Secondary lines, each timed with CUDA events on the session stream and with
+    its own clock samples: layer-major prefill, the 8-layer stack with lm_head and
+    sampler, the common-prefix resync, and the same decode at depth 43."""
     out = {}
     model = pdl.Model(stack, emb, lm, layers)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     stream = torch.cuda.current_stream()
 
-    # layer-major prefill: 8 layers x 4096 tokens
+    # layer-major prefill: 8 layers x 4096 tokens; 3 untimed, then 20 timed back to back
     toks = synth.host_tokens(4096, stack.vocab, stream=31)
     sess = pdl.Session(model, 4200)
-    times = []
-    for rep in range(3):
-        assert sess.truncate(0) == 0
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        assert sess.prefill(toks) == 0
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        if rep > 0:
-            times.append(ev0.elapsed_time(ev1) / 1000.0)
-    t = min(times)
+    for _ in range(3):
+        assert sess.truncate(0) == 0 and sess.prefill(toks) == 0
+    torch.cuda.synchronize()
+    reps = 20
+    clk = ClockSampler(local)
+    clk.start()
+    ev0.record(stream)
+    for _ in range(reps):
+        assert sess.truncate(0) == 0 and sess.prefill(toks) == 0
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    assert sess.status() == 0
+    t = ev0.elapsed_time(ev1) / 1000.0 / reps
     flops = prefill_flops_per_token_layer(stack) * 4096 * stack.n_layers
     wbytes = sum(np.prod(s) for _, k, s, sg in synth.layer_tensors(stack) if sg) * 2 * stack.n_layers
     out["prefill"] = {
         "metric": "prefill tok/s", "value": round(4096 / t, 1), "unit": "tok/s",
         "workload": "8 layers of the full-width shapes, 4096 prompt tokens, layer-major",
-        "ms": round(t * 1000, 2),
+        "ms": round(t * 1000, 3), "reps": reps,
         "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 2),
                      "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": round(flops / t / 1e12 / bf16_peak, 4),
+                     "frac_of_sustained": round(flops / t / 1e12 / bf16_sus, 4),
                      "algorithmic_flops": flops,
                      "memory_floor_ms": round(wbytes / (hbm_peak * 1e9) * 1000, 2),
-                     "compute_floor_ms": round(flops / (bf16_peak * 1e12) * 1000, 2)},
+                     "compute_floor_ms": round(flops / (bf16_peak * 1e12) * 1000, 2),
+                     "frac_of_binding_floor": round(max(wbytes / (hbm_peak * 1e9),
+                                                        flops / (bf16_peak * 1e12)) / t, 4)},
+        "clocks": clocks,
     }
     del sess
 
     # decode stack + lm_head + top-p sampler: prompt 512, 256 generated tokens
-    sess = pdl.Session(model, 512 + 256 + 16)
-    prompt = synth.host_tokens(512, stack.vocab, stream=41)
-    assert sess.prefill(prompt) == 0
-    ws = torch.empty(pdl.sample_workspace_bytes(stack.vocab), dtype=torch.uint8, device="cuda")
-    state = 0x9E3779B97F4A7C15
-    tok, state = pdl.sample(sess.logits(), 0.7, 0.95, state, ws)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    ev0.record(stream)
-    for i in range(256):
-        assert sess.decode(tok) == 0
-        tok, state = pdl.sample(sess.logits(), 0.7, 0.95, state, ws)
-        assert tok >= 0
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    t = ev0.elapsed_time(ev1) / 1000.0
-    tok_bytes = stack.n_layers * sum(layer_bytes(stack).values()) + lm_head_bytes(stack)
-    out["stack"] = {
-        "metric": "decode tok/s (8 layers + lm_head + top-p 0.95, T 0.7)",
-        "value": round(256 / t, 1), "unit": "tok/s",
-        "roofline": {"bound": "hbm", "bytes_per_token": int(tok_bytes),
-                     "achieved": round(tok_bytes * 256 / t / 1e9, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(tok_bytes * 256 / t / 1e9 / hbm_peak, 4)},
-        "note": "each token synchronises to return the sampled id to the host",
-    }
-    del sess
+    out["stack"] = sampled_decode_line(pdl, torch, model, stack, 256, local, hbm_peak)
+    out["stack"]["metric"] = "decode tok/s (8 layers + lm_head + top-p 0.95, T 0.7)"
 
     # common-prefix resync: live 16994 -> common 16846 -> canonical 16937
     P = synth.host_tokens(16846, stack.vocab, stream=51)
@@ -609,12 +658,21 @@ def extra_measurements(pdl, tw, torch, stack, emb, lm, layers, flush, hbm_peak, 
     assert live.prefill(np.concatenate([P, live_tail])) == 0
     torch.cuda.synchronize()
     cp = live.common_prefix(prompt)
-    ev0.record(stream)
-    assert live.truncate(cp) == 0
-    assert live.prefill(prompt[cp:]) == 0
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    resync_ms = ev0.elapsed_time(ev1)
+    # the resync itself, then 20 more times (truncating back to the common prefix
+    # redoes exactly the same work), timed as one region with its clock samples
+    reps = 20
+    times = []
+    clk = ClockSampler(local)
+    clk.start()
+    for rep in range(1 + reps):
+        ev0.record(stream)
+        assert live.truncate(cp) == 0
+        assert live.prefill(prompt[cp:]) == 0
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+    clocks = clk.stop()
+    resync_ms = statistics.mean(times[1:])
     ws2 = torch.empty(pdl.sample_workspace_bytes(stack.vocab), dtype=torch.uint8, device="cuda")
     ids_live = []
     t0 = time.perf_counter()
@@ -640,11 +698,57 @@ def extra_measurements(pdl, tw, torch, stack, emb, lm, layers, flush, hbm_peak, 
     out["resync"] = {
         "metric": "resync latency (truncate + 91-token prefill, 8 layers)",
         "value": round(resync_ms, 3), "unit": "ms", "common_prefix": cp,
+        "first_ms": round(times[0], 3), "reps": reps,
         "greedy_decode_tok_s": round(64 / dec_s, 1),
         "matches_scratch_prefill": bool(same),
-        "algorithmic_flops": sfl,
+        "algorithmic_flops": sfl, "clocks": clocks,
     }
+
+    # depth 43 (the pages' decode loop): the 8 generated layers used in turn, each of
+    # the 43 layers with its own K/V cache; same sampled workload as the stack line
+    deep_shape = stack.with_(name="depth43", n_layers=43)
+    deep = pdl.Model(deep_shape, emb, lm, [layers[l % stack.n_layers] for l in range(43)])
+    out["depth43"] = sampled_decode_line(pdl, torch, deep, deep_shape, 64, local, hbm_peak)
+    out["depth43"]["metric"] = "decode tok/s (43 layers + lm_head + top-p 0.95, T 0.7)"
+    out["depth43"]["note"] = ("layer l uses the weights of generated layer l mod 8; each layer "
+                              "streams 275 MB per token, more than L2 holds, so the aliasing "
+                              "gives no cache advantage")
     return out
+
+
+def sampled_decode_line(pdl, torch, model, shape, n_gen, local, hbm_peak):
+    """Decode with lm_head and top-p sampling after a 512-token prompt: n_gen tokens
+    at T 0.7 / top-p 0.95 from a seeded xorshift64* state, timed with CUDA events."""
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sess = pdl.Session(model, 512 + n_gen + 16)
+    prompt = synth.host_tokens(512, shape.vocab, stream=41)
+    assert sess.prefill(prompt) == 0
+    ws = torch.empty(pdl.sample_workspace_bytes(shape.vocab), dtype=torch.uint8, device="cuda")
+    state = 0x9E3779B97F4A7C15
+    tok, state = pdl.sample(sess.logits(), 0.7, 0.95, state, ws)
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    ev0.record(stream)
+    for i in range(n_gen):
+        assert sess.decode(tok) == 0
+        tok, state = pdl.sample(sess.logits(), 0.7, 0.95, state, ws)
+        assert tok >= 0
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    assert sess.status() == 0
+    t = ev0.elapsed_time(ev1) / 1000.0
+    tok_bytes = shape.n_layers * sum(layer_bytes(shape).values()) + lm_head_bytes(shape)
+    return {
+        "value": round(n_gen / t, 1), "unit": "tok/s", "tokens": n_gen,
+        "roofline": {"bound": "hbm", "bytes_per_token": int(tok_bytes),
+                     "achieved": round(tok_bytes * n_gen / t / 1e9, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(tok_bytes * n_gen / t / 1e9 / hbm_peak, 4)},
+        "note": "each token synchronises to return the sampled id to the host",
+        "clocks": clocks,
+    }
 
 
 if __name__ == "__main__":
