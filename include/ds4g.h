@@ -83,16 +83,20 @@ typedef struct {
     int decode_kernel; /* DS4G_DECODE_AUTO: one persistent launch per decode step when
                           the device supports cooperative launch, else one kernel per
                           stage; DS4G_DECODE_STAGED forces one kernel per stage */
-    int prefill_kernel; /* DS4G_PREFILL_AUTO: tensor-core GEMMs (tcgen05, activations
-                           as BF16 hi/lo pairs, FP32 accumulation) when the weights are
-                           BF16 and every weight piece is a multiple of 128 rows (64 for
-                           expert gate/up) and every reduction a multiple of 64, else
-                           SIMT GEMMs with FP32 activations; DS4G_PREFILL_SIMT forces the
-                           SIMT GEMMs */
+    int prefill_kernel; /* DS4G_PREFILL_AUTO: tensor-core GEMMs (tcgen05, BF16
+                           activations times BF16 weights, FP32 accumulation and FP32
+                           residual; the router's input as a BF16 hi/lo pair, so that its
+                           scores carry about 16 significant bits of the normalised
+                           residual) when the weights are BF16 and every weight piece is a
+                           multiple of 128 rows (64 for expert gate/up) and every
+                           reduction a multiple of 64, else SIMT GEMMs with FP32
+                           activations; DS4G_PREFILL_HILO: the same tensor-core GEMMs
+                           with every activation as a BF16 hi/lo pair (twice the tensor
+                           work); DS4G_PREFILL_SIMT forces the SIMT GEMMs */
 } ds4g_config;
 
 enum { DS4G_DECODE_AUTO = 0, DS4G_DECODE_STAGED = 1 };
-enum { DS4G_PREFILL_AUTO = 0, DS4G_PREFILL_SIMT = 1 };
+enum { DS4G_PREFILL_AUTO = 0, DS4G_PREFILL_SIMT = 1, DS4G_PREFILL_HILO = 2 };
 
 /* One layer's weights (device pointers).  Gains are f32; matrices weight_dtype. */
 typedef struct {

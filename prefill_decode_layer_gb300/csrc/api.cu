@@ -22,6 +22,7 @@ struct ds4g_model {
     int nsm;
     bool persistent;   // decode steps use the single cooperative launch
     bool tc;           // prefill GEMMs run on the tensor cores
+    bool hilo;         // ... with every activation as a BF16 hi/lo pair
     std::vector<TcLayerMaps> tcmaps;   // per layer, when tc
 };
 
@@ -99,6 +100,9 @@ bool cfg_ok(const ds4g_config *c)
     if (c->kv_dtype != DS4G_F32 && c->kv_dtype != DS4G_BF16) return false;
     if (c->prefill_chunk < 0 || c->prefill_chunk > 65536) return false;
     if (c->decode_kernel != DS4G_DECODE_AUTO && c->decode_kernel != DS4G_DECODE_STAGED) return false;
+    if (c->prefill_kernel != DS4G_PREFILL_AUTO && c->prefill_kernel != DS4G_PREFILL_SIMT &&
+        c->prefill_kernel != DS4G_PREFILL_HILO)
+        return false;
     if (!(c->rope_base > 0.f) || !(c->rms_eps >= 0.f)) return false;
     if (c->n_experts % 4) return false;  // 4-wide epilogues of the batched kernels
     // shared-memory footprints of the kernels (floats unless stated)
@@ -232,7 +236,9 @@ int ds4g_model_create(const ds4g_config *cfg, const ds4g_weights *w, ds4g_model 
     m->persistent = false;
     if (!e && cfg->decode_kernel == DS4G_DECODE_AUTO)
         e = persistent_setup(m->d, max_smem, m->nsm, &m->persistent);
-    m->tc = !e && cfg->prefill_kernel == DS4G_PREFILL_AUTO && tc_prefill_eligible(m->d);
+    m->tc = !e && (cfg->prefill_kernel == DS4G_PREFILL_AUTO || cfg->prefill_kernel == DS4G_PREFILL_HILO) &&
+            tc_prefill_eligible(m->d);
+    m->hilo = cfg->prefill_kernel == DS4G_PREFILL_HILO;
     if (m->tc) {
         e = attn_mma_setup(m->d, max_smem);
         if (!e) e = attn_tc_setup(m->d, max_smem);
@@ -382,7 +388,7 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
             e = s->m->tc ? prefill_chunk_tc(d, s->m->layers.data(), s->m->tcmaps.data(), s->tcact,
                                             s->tckv.empty() ? nullptr : s->tckv.data(), s->kc.data(),
                                             s->vc.data(), s->rope, s->m->tok_embd, s->pb, s->len + c, nc, s->st,
-                                            s->m->nsm)
+                                            s->m->nsm, s->m->hilo)
                          : prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,
                                          s->m->tok_embd, s->pb, s->len + c, nc, s->st, s->m->nsm);
         if (!e && c + nc == n) {  // last token's hidden state, then its logits

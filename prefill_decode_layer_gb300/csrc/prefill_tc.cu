@@ -21,8 +21,9 @@ namespace ds4g {
 
 // ------------------------------------------------------------------ small kernels
 
-// RMSNorm of each residual row into hi/lo BF16: one CTA per token row, H/4 threads
-// (at most 1024), each keeping its float4s in registers between the two passes.
+// RMSNorm of each residual row into hi/lo BF16 (lo == nullptr: hi only): one CTA per
+// token row, H/4 threads (at most 1024), each keeping its float4s in registers
+// between the two passes.
 __global__ void __launch_bounds__(1024) k_rmsnorm_hilo(const float *X, const float *g, bf16 *hi, bf16 *lo,
                                                        int H, float eps)
 {
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(1024) k_rmsnorm_hilo(const float *X, const flo
         split_hilo(v[u].z * inv * gv.z, h[2], l[2]);
         split_hilo(v[u].w * inv * gv.w, h[3], l[3]);
         *reinterpret_cast<uint2 *>(hi + (size_t)t * H + 4 * i) = *reinterpret_cast<const uint2 *>(h);
-        *reinterpret_cast<uint2 *>(lo + (size_t)t * H + 4 * i) = *reinterpret_cast<const uint2 *>(l);
+        if (lo) *reinterpret_cast<uint2 *>(lo + (size_t)t * H + 4 * i) = *reinterpret_cast<const uint2 *>(l);
     }
 }
 static int rmsnorm_threads(int H) { return H / 4 < 1024 ? ((H / 4 + 31) / 32) * 32 : 1024; }
@@ -289,7 +290,7 @@ cudaError_t attn_mma_setup(const Dims &d, int max_smem)
 // Functors of the tensor-core GEMM: load4 fetches what a 4-feature store needs
 // from global memory (issued in batches by the GEMM), store4 writes.
 
-struct EpiHiLo {   // out[m][n..n+3] as hi/lo BF16 (the next GEMM's input)
+struct EpiHiLo {   // out[m][n..n+3] as hi/lo BF16 (the next GEMM's input; lo may be null)
     bf16 *hi, *lo;
     int ld;
     using Aux = tc::NoAux;
@@ -300,7 +301,7 @@ struct EpiHiLo {   // out[m][n..n+3] as hi/lo BF16 (the next GEMM's input)
 #pragma unroll
         for (int j = 0; j < 4; ++j) split_hilo(v[j], h[j], l[j]);
         *reinterpret_cast<uint2 *>(hi + (size_t)m * ld + n) = *reinterpret_cast<const uint2 *>(h);
-        *reinterpret_cast<uint2 *>(lo + (size_t)m * ld + n) = *reinterpret_cast<const uint2 *>(l);
+        if (lo) *reinterpret_cast<uint2 *>(lo + (size_t)m * ld + n) = *reinterpret_cast<const uint2 *>(l);
     }
 };
 
@@ -403,7 +404,7 @@ struct EpiRoutedRows {   // routed expert output of grouped row m into its (toke
     }
 };
 
-struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16, 16-byte stores
+struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16 (lo may be null), 16-byte stores
     bf16 *hi, *lo;
     int ld;
     __device__ void store_row(int m, int i0, const float (&h)[32], int) const
@@ -422,7 +423,7 @@ struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16, 16-by
                 wl[j] = pack_bf16x2(l0, l1);
             }
             ph[v] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            pl[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            if (lo) pl[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
     }
 };
@@ -430,7 +431,7 @@ struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16, 16-by
 // x[t] += sum over slots s (in order) of w[t][s] * YS[t*K + s]: the selected experts'
 // outputs, after the shared expert's down projection was added by its GEMM.
 // With gnext (H <= 8192): also the next layer's attention RMSNorm of the new row,
-// as BF16 hi/lo into hi, lo (what k_rmsnorm_hilo would write next).
+// as BF16 hi/lo into hi, lo (what k_rmsnorm_hilo would write next; lo may be null).
 __global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, const float *wts, int H, int K,
                                                      const float *gnext, float eps, bf16 *nhi, bf16 *nlo)
 {
@@ -483,7 +484,7 @@ __global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, 
         split_hilo(xr[u].z * inv * gv.z, h[2], l[2]);
         split_hilo(xr[u].w * inv * gv.w, h[3], l[3]);
         *reinterpret_cast<uint2 *>(nhi + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(h);
-        *reinterpret_cast<uint2 *>(nlo + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(l);
+        if (nlo) *reinterpret_cast<uint2 *>(nlo + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(l);
     }
 }
 
@@ -558,7 +559,7 @@ cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m)
 
 // ------------------------------------------------------------------ one chunk
 
-template <typename TKV>
+template <typename TKV, bool HL>
 static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
                               const TcActMaps &am, const TcKVMaps *kvm, void *const *kcs, void *const *vcs,
                               const float2 *rope,
@@ -587,25 +588,25 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         // ---- attention half (its RMSNorm came with the previous layer's combine)
         if (!normed &&
             (e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
-                            (const float *)w.attn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
+                            (const float *)w.attn_norm, ap.xn_hi, HL ? ap.xn_lo : nullptr, H, d.eps)))
             return e;
         a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ, a.x_col0 = 0;
-        if ((e = tc::launch<false>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a, EpiHiLo{ap.c_hi, ap.c_lo, d.RQ + d.RKV},
+        if ((e = tc::launch<false, HL>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a, EpiHiLo{ap.c_hi, HL ? ap.c_lo : nullptr, d.RQ + d.RKV},
                                    ny, nsm, st)))
             return e;
         a.n_out = d.QD, a.k = d.RQ, a.piece_rows = 0, a.x_col0 = 0;
         const bool attn_tc = kvm != nullptr;   // tcgen05 attention: queries as hi/lo BF16
         if (attn_tc) {
             bf16 *q_hi = (bf16 *)pb.Q, *q_lo = q_hi + (size_t)pb.P * d.QD;
-            if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
+            if ((e = tc::launch<false, HL>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
                                        EpiQRopeHiLo{q_hi, q_lo, rope, d.QD, d.HD, p0}, ny, nsm, st)))
                 return e;
-        } else if ((e = tc::launch<false>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
+        } else if ((e = tc::launch<false, HL>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
                                           EpiQRope{(float *)pb.Q, rope, d.QD, d.HD, p0}, ny, nsm, st))) {
             return e;
         }
         a.n_out = 2 * d.HD, a.k = d.RKV, a.piece_rows = d.HD, a.x_col0 = d.RQ;
-        if ((e = tc::launch<false>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, EpiKVRope<TKV>{kc, vc, rope, d.HD, p0}, ny,
+        if ((e = tc::launch<false, HL>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, EpiKVRope<TKV>{kc, vc, rope, d.HD, p0}, ny,
                                    nsm, st)))
             return e;
         if (attn_tc) {
@@ -625,14 +626,14 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             return e;
         }
         a.n_out = H, a.k = d.QD, a.piece_rows = 0, a.x_col0 = 0;
-        if ((e = tc::launch<false>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
+        if ((e = tc::launch<false, HL>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
         // ---- MoE half
         if ((e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
                             (const float *)w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
             return e;
         a.n_out = d.E, a.k = H;
-        if ((e = tc::launch<false>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, ny, nsm, st)))
+        if ((e = tc::launch<false, true>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, ny, nsm, st)))
             return e;
         if ((e = launch_pdl(k_router_topk, dim3((n * 32 + 255) / 256), dim3(256), 0, st, (const float *)pb.S, pb.ids,
                             pb.wts, n, d.E, K, pb.status)))
@@ -644,26 +645,26 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         g.status = pb.status;
         g.n_out = I, g.k = H, g.tiles = pb.tiles, g.off = pb.off;
         g.grow = pb.rows, g.gdiv = K, g.gx_hi = ap.xn_hi, g.gx_lo = ap.xn_lo, g.gld = H;
-        if ((e = tc::launch<true>(m.wg, m.wu, am.xn_hi, am.xn_lo, g, EpiSwiGLU{ap.hg_hi, ap.hg_lo, I}, max_tiles,
+        if ((e = tc::launch<true, HL>(m.wg, m.wu, am.xn_hi, am.xn_lo, g, EpiSwiGLU{ap.hg_hi, HL ? ap.hg_lo : nullptr, I}, max_tiles,
                                   nsm, st)))
             return e;
         g.grow = nullptr;
         a.n_out = I, a.k = H;
-        if ((e = tc::launch<true>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, ap.hs_lo, I}, ny, nsm,
+        if ((e = tc::launch<true, HL>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, HL ? ap.hs_lo : nullptr, I}, ny, nsm,
                                   st)))
             return e;
         // routed down (grouped) into per-(token, slot) rows; the shared expert's down
         // projection into the residual; then the weighted routed rows, slot order
         g.n_out = H, g.k = I;
-        if ((e = tc::launch<false>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H}, max_tiles,
+        if ((e = tc::launch<false, HL>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H}, max_tiles,
                                    nsm, st)))
             return e;
         a.n_out = H, a.k = I;
-        if ((e = tc::launch<false>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
+        if ((e = tc::launch<false, HL>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
         const float *gn = l + 1 < d.L && H <= 8 * 1024 ? layers[l + 1].attn_norm : nullptr;
         if ((e = launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, st, pb.X, (const float *)pb.YS,
-                            (const float *)pb.wts, H, K, gn, d.eps, ap.xn_hi, ap.xn_lo)))
+                            (const float *)pb.wts, H, K, gn, d.eps, ap.xn_hi, HL ? ap.xn_lo : nullptr)))
             return e;
         normed = gn != nullptr;
     }
@@ -673,11 +674,14 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
 cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
                              const TcActMaps &am, const TcKVMaps *kvm, void *const *kc, void *const *vc,
                              const float2 *rope, const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n,
-                             cudaStream_t st, int nsm)
+                             cudaStream_t st, int nsm, bool hilo)
 {
-    return d.kvdt == DS4G_BF16
-               ? chunk_tc_t<bf16>(d, layers, lm, am, kvm, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
-               : chunk_tc_t<float>(d, layers, lm, am, nullptr, kc, vc, rope, tok_embd, pb, p0, n, st, nsm);
+    if (d.kvdt != DS4G_BF16)
+        return hilo ? chunk_tc_t<float, true>(d, layers, lm, am, nullptr, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
+                    : chunk_tc_t<float, false>(d, layers, lm, am, nullptr, kc, vc, rope, tok_embd, pb, p0, n, st,
+                                               nsm);
+    return hilo ? chunk_tc_t<bf16, true>(d, layers, lm, am, kvm, kc, vc, rope, tok_embd, pb, p0, n, st, nsm)
+                : chunk_tc_t<bf16, false>(d, layers, lm, am, kvm, kc, vc, rope, tok_embd, pb, p0, n, st, nsm);
 }
 
 }  // namespace ds4g

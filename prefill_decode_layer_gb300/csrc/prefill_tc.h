@@ -43,10 +43,12 @@ cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m);
 TcActPtrs tc_act_ptrs(const Dims &d, const PrefillBufs &pb);
 cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m);
 // kvm: per-layer K/V maps for the tcgen05 attention (nullptr: the warp-MMA one).
+// hilo: every GEMM takes its activations as BF16 hi/lo pairs; otherwise only the
+// router's (the other GEMMs multiply BF16 activations).
 cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLayerMaps *lm,
                              const TcActMaps &am, const TcKVMaps *kvm, void *const *kc, void *const *vc,
                              const float2 *rope, const uint16_t *tok_embd, const PrefillBufs &pb, int p0, int n,
-                             cudaStream_t st, int nsm);
+                             cudaStream_t st, int nsm, bool hilo);
 
 // prefill.cu kernels the tensor-core form shares
 __global__ void k_embed_rows(const uint16_t *table, const int *tok, float *X, int H);

@@ -62,14 +62,15 @@ static constexpr int CH = 32;                                // features per epi
 static constexpr uint32_t EPI_BYTES = 8 * 32 * CH * 4;       // 32 KB: [8 warps][32 tokens][CH]
 static constexpr int EPI_BATCH = 8;                          // functor loads in flight
 
-// Tile geometry.  WN weight rows per tile: 256 -> 3 stages of 64 KB, 128 -> 4
-// stages of 48 KB; plain tiles add the epilogue's staging rows.
-template <bool GU, int WN> struct Geo {
+// Tile geometry.  WN weight rows per tile; with the lo token tile (LO), 256 -> 3
+// stages of 64 KB and 128 -> 4 stages of 48 KB; without it, 256 -> 4 stages of 48 KB
+// and 128 -> 6 stages of 32 KB.  Plain tiles add the epilogue's staging rows.
+template <bool GU, int WN, bool LO> struct Geo {
     static_assert(WN == 128 || WN == 256, "weight tile width");
     static_assert(!GU || WN == 256, "gate/up tiles hold 128 gate + 128 up rows");
     static constexpr uint32_t TILE_W = WN * BK * 2;
-    static constexpr uint32_t STAGE = TILE_W + 2 * TILE_X;   // W, X hi, X lo
-    static constexpr int STAGES = WN == 256 ? 3 : 4;
+    static constexpr uint32_t STAGE = TILE_W + (LO ? 2 : 1) * TILE_X;   // W, X hi[, X lo]
+    static constexpr int STAGES = LO ? (WN == 256 ? 3 : 4) : (WN == 256 ? 4 : 6);
     static constexpr uint32_t TMEM_COLS = 2 * WN;           // two tiles in flight
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (GU ? 0 : EPI_BYTES) + 256;
 };
@@ -124,13 +125,15 @@ __device__ __forceinline__ float4 staged(const float *wstg, int t, int g)
 // and  store4(m, n, v[4], aux, e).
 // GA (grouped only): the token tiles are gathered row by row from a.gx_hi / a.gx_lo
 // by GWARPS extra warps with 16-byte cp.async copies (the maps xhi, xlo are unused).
-template <class Epi, bool GU, int WN, bool GA = false>
+// LO: the activations' lo half takes part (two MMAs per K step); without it the
+// products are taken with the BF16 activations alone (xlo / gx_lo are not read).
+template <class Epi, bool GU, int WN, bool GA, bool LO>
 __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
               const __grid_constant__ CUtensorMap xhi, const __grid_constant__ CUtensorMap xlo,
               const Args a, const Epi epi)
 {
-    using G = Geo<GU, WN>;
+    using G = Geo<GU, WN, LO>;
     constexpr int STAGES = G::STAGES;
     constexpr uint32_t STAGE_BYTES = G::STAGE;
     extern __shared__ unsigned char smem_raw[];
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
             tma_prefetch_desc(&w0);
             tma_prefetch_desc(&w1);
             tma_prefetch_desc(&xhi);
-            tma_prefetch_desc(&xlo);
+            if (LO) tma_prefetch_desc(&xlo);
             unsigned it = 0;
             bool ok = true;
             for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                     for (int h = 0; h < WN / BOXW; ++h) tma_load_2d(st + h * BOX_BYTES, bm[h], kx, brow[h], &full[s]);
                     if constexpr (!GA) {
                         tma_load_2d(st + G::TILE_W, &xhi, a.x_col0 + kx, r0, &full[s]);
-                        tma_load_2d(st + G::TILE_W + TILE_X, &xlo, a.x_col0 + kx, r0, &full[s]);
+                        if constexpr (LO) tma_load_2d(st + G::TILE_W + TILE_X, &xlo, a.x_col0 + kx, r0, &full[s]);
                     }
                 }
             }
@@ -277,9 +280,11 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t wd = sdesc_kmajor_sw128(sa + kk * 32);
                         const uint64_t xh = sdesc_kmajor_sw128(sa + G::TILE_W + kk * 32);
-                        const uint64_t xl = sdesc_kmajor_sw128(sa + G::TILE_W + TILE_X + kk * 32);
                         tc_mma_bf16(acc, xh, wd, idesc, (i | kk) != 0);
-                        tc_mma_bf16(acc, xl, wd, idesc, 1u);
+                        if constexpr (LO) {
+                            const uint64_t xl = sdesc_kmajor_sw128(sa + G::TILE_W + TILE_X + kk * 32);
+                            tc_mma_bf16(acc, xl, wd, idesc, 1u);
+                        }
                     }
                     tc_commit(&empty[s]);   // the stage is free once these MMAs complete
                 }
@@ -338,7 +343,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                         const int off = row * 128 + ((c ^ (row & 7)) << 4);
                         const size_t so = (size_t)src[q] * a.gld + col + kx;
                         cp_async16(xt + off, a.gx_hi + so);
-                        cp_async16(xt + TILE_X + off, a.gx_lo + so);
+                        if constexpr (LO) cp_async16(xt + TILE_X + off, a.gx_lo + so);
                     }
                     cp_async_commit();
                     cp_async_wait_group<1>();   // the previous stage's copies have landed
@@ -443,27 +448,28 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
 // `rows` read as zeros.
 cudaError_t make_map_bf16(CUtensorMap *m, const void *base, int rows, int cols, int ld, int box_rows);
 
-template <bool GU, int WN, class Epi, bool GA = false>
+template <bool GU, int WN, bool LO, class Epi, bool GA = false>
 static cudaError_t launch_wn(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
                              const CUtensorMap &xlo, const Args &a, const Epi &epi, long long work, int nsm,
                              cudaStream_t st)
 {
     static bool attr_set = false;   // per instantiation; set before the first launch
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU, WN, GA>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Geo<GU, WN>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU, WN, GA, LO>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Geo<GU, WN, LO>::SMEM);
         if (e) return e;
         attr_set = true;
     }
     const int grid = (int)(work < nsm ? work : nsm);
-    return launch_pdl(k_tc_gemm<Epi, GU, WN, GA>, dim3(grid), dim3(GA ? THREADS_GA : THREADS), Geo<GU, WN>::SMEM,
-                      st, w0, w1, xhi, xlo, a, epi);
+    return launch_pdl(k_tc_gemm<Epi, GU, WN, GA, LO>, dim3(grid), dim3(GA ? THREADS_GA : THREADS),
+                      Geo<GU, WN, LO>::SMEM, st, w0, w1, xhi, xlo, a, epi);
 }
 
 // ntile_bound: token tiles at most (dense: exact; grouped: the tile list's bound).
 // Plain GEMMs take 256-row weight tiles when that still gives every SM two tiles,
 // else 128-row tiles (twice the tiles, half the reuse of each token tile).
-template <bool GU, class Epi>
+template <bool GU, bool LO, class Epi>
 static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
                           const CUtensorMap &xlo, const Args &a, const Epi &epi, int ntile_bound, int nsm,
                           cudaStream_t st)
@@ -471,13 +477,13 @@ static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CU
     if (ntile_bound <= 0 || a.n_out <= 0) return cudaSuccess;
     if constexpr (GU) {
         const long long work = (long long)(a.n_out / BOXW) * ntile_bound;
-        if (a.grow) return launch_wn<true, 256, Epi, true>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
-        return launch_wn<true, 256>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
+        if (a.grow) return launch_wn<true, 256, LO, Epi, true>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
+        return launch_wn<true, 256, LO>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
     } else {
         const long long w256 = (long long)((a.n_out + 255) / 256) * ntile_bound;
-        if (w256 >= 2ll * nsm) return launch_wn<false, 256>(w0, w1, xhi, xlo, a, epi, w256, nsm, st);
-        return launch_wn<false, 128>(w0, w1, xhi, xlo, a, epi, (long long)((a.n_out + 127) / 128) * ntile_bound,
-                                     nsm, st);
+        if (w256 >= 2ll * nsm) return launch_wn<false, 256, LO>(w0, w1, xhi, xlo, a, epi, w256, nsm, st);
+        return launch_wn<false, 128, LO>(w0, w1, xhi, xlo, a, epi,
+                                         (long long)((a.n_out + 127) / 128) * ntile_bound, nsm, st);
     }
 }
 

@@ -113,7 +113,7 @@ def _check(rc: int, what: str) -> int:
 
 
 DECODE_AUTO, DECODE_STAGED = 0, 1
-PREFILL_AUTO, PREFILL_SIMT = 0, 1
+PREFILL_AUTO, PREFILL_SIMT, PREFILL_HILO = 0, 1, 2
 
 
 def config_struct(shape, prefill_chunk: int = 0, decode_kernel: int = DECODE_AUTO,

@@ -28,13 +28,18 @@ SMALL_TCA128 = SMALL_TC.with_(name="small_bf16_tc_attn128", n_heads=128, window=
 SMALL_TCA64 = SMALL_TC.with_(name="small_bf16_tc_attn64", n_heads=64, window=128)
 
 
-@pytest.fixture(scope="module", params=[SMALL, SMALL_TC, SMALL_TCA128, SMALL_TCA64],
-                ids=["simt", "tensor_core", "tensor_core_attn128", "tensor_core_attn64"])
+# (shape, prefill_kernel): 0 the default GEMM form for the shape, 2 the tensor-core
+# GEMMs with every activation as a BF16 hi/lo pair
+@pytest.fixture(scope="module", params=[(SMALL, 0), (SMALL_TC, 0), (SMALL_TC, 2), (SMALL_TCA128, 0),
+                                        (SMALL_TCA64, 0)],
+                ids=["simt", "tensor_core", "tensor_core_hilo", "tensor_core_attn128",
+                     "tensor_core_attn64"])
 def small(request):
     import torch
     torch.cuda.init()
-    shape = request.param
-    return gpu_model(shape, prefill_chunk=32), LazyOracleModel(shape).full(), shape
+    shape, kernel = request.param
+    return (gpu_model(shape, prefill_chunk=32, prefill_kernel=kernel), LazyOracleModel(shape).full(),
+            shape)
 
 
 def kv_np(sess, layer, n):
@@ -73,7 +78,7 @@ def test_chunk_size_invariance_bitwise(small):
     import torch
     import prefill_decode_layer_gb300 as pdl
     gm, _, SMALL = small
-    big = pdl.Model(SMALL, *gm._keep, prefill_chunk=0)
+    big = pdl.Model(SMALL, *gm._keep, prefill_chunk=0, prefill_kernel=gm.cfg.prefill_kernel)
     toks = synth.host_tokens(77, SMALL.vocab, stream=23)
     a = pdl.Session(gm, 128)
     b = pdl.Session(big, 128)
