@@ -238,16 +238,19 @@ template <> struct XFrag<bf16> {
         a = x4[(blk << 6) + t];
         b = x4[(blk << 6) + m + t];
     }
-    __device__ __forceinline__ float dot(const uint4 &w, float acc) const
+    // Two-wide FP32 FMAs: the even and the odd weights of the vector accumulate in
+    // the two halves of acc (a BF16 pair widens to two floats with one shift and one
+    // mask).
+    __device__ __forceinline__ float2 dot(const uint4 &w, float2 acc) const
     {
-        acc = fmaf(__uint_as_float(w.x << 16), a.x, acc);
-        acc = fmaf(__uint_as_float(w.x & 0xffff0000u), a.y, acc);
-        acc = fmaf(__uint_as_float(w.y << 16), a.z, acc);
-        acc = fmaf(__uint_as_float(w.y & 0xffff0000u), a.w, acc);
-        acc = fmaf(__uint_as_float(w.z << 16), b.x, acc);
-        acc = fmaf(__uint_as_float(w.z & 0xffff0000u), b.y, acc);
-        acc = fmaf(__uint_as_float(w.w << 16), b.z, acc);
-        acc = fmaf(__uint_as_float(w.w & 0xffff0000u), b.w, acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u)),
+                         make_float2(a.x, a.y), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u)),
+                         make_float2(a.z, a.w), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u)),
+                         make_float2(b.x, b.y), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u)),
+                         make_float2(b.z, b.w), acc);
         return acc;
     }
 };
@@ -255,15 +258,14 @@ template <> struct XFrag<float> {
     float4 a;
     __device__ __forceinline__ void zero() { a = make_float4(0.f, 0.f, 0.f, 0.f); }
     __device__ __forceinline__ void load(const float4 *x4, int v, int) { a = x4[v]; }
-    __device__ __forceinline__ float dot(const uint4 &w, float acc) const
+    __device__ __forceinline__ float2 dot(const uint4 &w, float2 acc) const
     {
-        acc = fmaf(__uint_as_float(w.x), a.x, acc);
-        acc = fmaf(__uint_as_float(w.y), a.y, acc);
-        acc = fmaf(__uint_as_float(w.z), a.z, acc);
-        acc = fmaf(__uint_as_float(w.w), a.w, acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), make_float2(a.x, a.y), acc);
+        acc = __ffma2_rn(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), make_float2(a.z, a.w), acc);
         return acc;
     }
 };
+__device__ __forceinline__ float hsum(float2 v) { return v.x + v.y; }
 
 // Vectors per lane kept in registers by the short-row path (32 floats of x).
 template <typename TW> struct ShortRow { static constexpr int NU = 32 / VecOf<TW>::n; };
@@ -304,7 +306,7 @@ __device__ __noinline__ void warp_dots(const TW *rows, int nr, int K, const floa
                 q0[u] = v < nvec ? r0[v] : make_uint4(0, 0, 0, 0);
                 q1[u] = v < nvec ? r1[v] : make_uint4(0, 0, 0, 0);
             }
-            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+            float2 a0 = {0.f, 0.f}, a1 = {0.f, 0.f}, b0 = {0.f, 0.f}, b1 = {0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < NU; u += 2) {
                 a0 = xf[u].dot(q0[u], a0);
@@ -314,31 +316,31 @@ __device__ __noinline__ void warp_dots(const TW *rows, int nr, int K, const floa
                     b1 = xf[u + 1].dot(q1[u + 1], b1);
                 }
             }
-            a0 = warp_sum(a0 + b0);
-            a1 = warp_sum(a1 + b1);
+            const float s0 = warp_sum(hsum(a0) + hsum(b0));
+            const float s1 = warp_sum(hsum(a1) + hsum(b1));
             if (lane == 0) {
-                res[r] = a0;
-                res[r + 1] = a1;
+                res[r] = s0;
+                res[r + 1] = s1;
             }
         }
         if (r < nr) {
             const uint4 *r0 = w4 + (size_t)r * nvec;
-            float a0 = 0.f, b0 = 0.f;
+            float2 a0 = {0.f, 0.f}, b0 = {0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < NU; u += 2) {
                 const int v = lane + 32 * u;
                 if (v < nvec) a0 = xf[u].dot(r0[v], a0);
                 if (u + 1 < NU && v + 32 < nvec) b0 = xf[u + 1].dot(r0[v + 32], b0);
             }
-            a0 = warp_sum(a0 + b0);
-            if (lane == 0) res[r] = a0;
+            const float s0 = warp_sum(hsum(a0) + hsum(b0));
+            if (lane == 0) res[r] = s0;
         }
         return;
     }
     int r = 0;
     for (; r + 1 < nr; r += 2) {
         const uint4 *r0 = w4 + (size_t)r * nvec, *r1 = r0 + nvec;
-        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+        float2 a0 = {0.f, 0.f}, a1 = {0.f, 0.f}, b0 = {0.f, 0.f}, b1 = {0.f, 0.f};
         int v = lane;
         for (; v + 96 < nvec; v += 128) {
             uint4 q0[4], q1[4];
@@ -364,16 +366,16 @@ __device__ __noinline__ void warp_dots(const TW *rows, int nr, int K, const floa
             a0 = xa.dot(r0[v], a0);
             a1 = xa.dot(r1[v], a1);
         }
-        a0 = warp_sum(a0 + b0);
-        a1 = warp_sum(a1 + b1);
+        const float s0 = warp_sum(hsum(a0) + hsum(b0));
+        const float s1 = warp_sum(hsum(a1) + hsum(b1));
         if (lane == 0) {
-            res[r] = a0;
-            res[r + 1] = a1;
+            res[r] = s0;
+            res[r + 1] = s1;
         }
     }
     if (r < nr) {
         const uint4 *r0 = w4 + (size_t)r * nvec;
-        float a0 = 0.f, b0 = 0.f;
+        float2 a0 = {0.f, 0.f}, b0 = {0.f, 0.f};
         int v = lane;
         for (; v + 96 < nvec; v += 128) {
             uint4 q0[4];
@@ -393,8 +395,8 @@ __device__ __noinline__ void warp_dots(const TW *rows, int nr, int K, const floa
             xa.load(x4, v, nvec);
             a0 = xa.dot(r0[v], a0);
         }
-        a0 = warp_sum(a0 + b0);
-        if (lane == 0) res[r] = a0;
+        const float s0 = warp_sum(hsum(a0) + hsum(b0));
+        if (lane == 0) res[r] = s0;
     }
 }
 
