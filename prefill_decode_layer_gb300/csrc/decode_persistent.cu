@@ -708,7 +708,6 @@ __device__ __forceinline__ void producer_warp(const PersistArgs &a, Shared &S, u
     const Dims &d = a.d;
     const int I = d.I, H = d.H, K = d.K;
     const int RB = min(kMaxR, max(1, kSlot / (I * (int)sizeof(TW))));  // rows per down chunk
-    const int nrb = (H + RB - 1) / RB;
     const int vmax = max(max(H, d.QD), max(d.RQ + d.RKV, (K + 1) * I));
     unsigned char *ring = sm_raw;                                          // [kNSlot][kSlot]
     float *res_all = reinterpret_cast<float *>(ring + kNSlot * kSlot);     // [kNC][kMaxR]
@@ -879,11 +878,11 @@ __device__ __forceinline__ void producer_warp(const PersistArgs &a, Shared &S, u
             if (!finite) atomicCAS(a.status, 0, DS4G_ENONFINITE);
             S.w[K] = 1.f;
             mbar_arrive(&S.ids_ready);   // consumers start stage 6; the combine reads S.w
-            int lo, hi;
-            cta_range(nrb, lo, hi);
+            int dlo, dhi;   // this CTA's output rows of the down projections, in chunks of RB
+            cta_range(H, dlo, dhi);
             for (int j = rlo; ok && j < rhi; ++j) ok = issue_gu(xp, S.ids[j / I], j % I);
-            for (int b = lo; ok && b < hi; ++b) {
-                const int r0 = b * RB, nr = min(RB, H - r0);
+            for (int r0 = dlo; ok && r0 < dhi; r0 += RB) {
+                const int nr = min(RB, dhi - r0);
                 for (int t = 0; ok && t <= K; ++t) {
                     const TW *base = t == 0 ? static_cast<const TW *>(xp.s_down)
                                             : static_cast<const TW *>(xp.down) +
@@ -913,13 +912,12 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
     const Dims &d = a.d;
     const int I = d.I, H = d.H, K = d.K;
     const int RB = min(kMaxR, max(1, kSlot / (I * (int)sizeof(TW))));  // rows per down chunk
-    const int nrb = (H + RB - 1) / RB;
     const int vmax = max(max(H, d.QD), max(d.RQ + d.RKV, (K + 1) * I));
     unsigned char *ring = sm_raw;                                          // [kNSlot][kSlot]
     float *res_all = reinterpret_cast<float *>(ring + kNSlot * kSlot);     // [kNC][kMaxR]
     float *xs = res_all + kNC * kMaxR;                                     // [vmax]
     float *sc = xs + vmax;                                                 // [E] producer's
-    float *ybuf = sc + d.E;   // [(rows blocks per CTA + 1) * (K + 1) * RB] stage-7 results
+    float *ybuf = sc + d.E;   // [(row chunks per CTA) * (K + 1) * RB] stage-7 results
     float *att = xs + d.RQ + d.RKV;   // stages 2-3: q, scores, partial outputs (after the latents)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // ========================= consumers =========================
@@ -1141,10 +1139,10 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                 prefetch_range(static_cast<const TW *>(w.ws_gate) + (size_t)slo * H, (size_t)(shi - slo) * H * sizeof(TW));
                 prefetch_range(static_cast<const TW *>(w.ws_up) + (size_t)slo * H, (size_t)(shi - slo) * H * sizeof(TW));
             }
-            int lo, hi;
-            cta_range(nrb, lo, hi);
-            if (hi > lo)
-                prefetch_range(static_cast<const TW *>(w.ws_down) + (size_t)lo * RB * I, (size_t)(min(H, hi * RB) - lo * RB) * I * sizeof(TW));
+            int dlo, dhi;
+            cta_range(H, dlo, dhi);
+            if (dhi > dlo)
+                prefetch_range(static_cast<const TW *>(w.ws_down) + (size_t)dlo * I, (size_t)(dhi - dlo) * I * sizeof(TW));
         }
         float inv2;
         {
@@ -1215,16 +1213,18 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
             float *hs = xs;  // [(K+1) * I]
             cload<TW>(a.b.h, hs, (K + 1) * I, I);
             csync();
-            int lo, hi;
-            cta_range(nrb, lo, hi);
+            // this CTA's output rows [dlo, dhi) (balanced to one row), in chunks of RB rows
+            int dlo, dhi;
+            cta_range(H, dlo, dhi);
+            const int nch = (dhi - dlo + RB - 1) / RB;
             const unsigned base = it;
-            const int nitems = (hi - lo) * (K + 1);
+            const int nitems = nch * (K + 1);
             it = base + (unsigned)nitems;
             for (int j = 0; j < nitems; ++j) {
                 const unsigned idx = base + (unsigned)j;
                 if ((int)(idx % kNC) != warp) continue;
-                const int b = lo + j / (K + 1), t = j % (K + 1);
-                const int r0 = b * RB, nr = min(RB, H - r0);
+                const int b = j / (K + 1), t = j % (K + 1);
+                const int r0 = dlo + b * RB, nr = min(RB, dhi - r0);
                 const int slot = t == 0 ? K : t - 1;
                 if (!consume(idx,
                              [&](const unsigned char *sl) {
@@ -1232,20 +1232,19 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                                                hs + (size_t)slot * I, res, lane);
                              },
                              [&]() {
-                                 float *yy = ybuf + ((size_t)(b - lo) * (K + 1) + t) * RB;
+                                 float *yy = ybuf + ((size_t)b * (K + 1) + t) * RB;
                                  for (int r = lane; r < nr; r += 32) yy[r] = res[r];
                              }))
                     return;
             }
             csync();
             // combine in fixed order: shared expert first, then the selected experts
-            for (int rr = threadIdx.x; rr < (hi - lo) * RB; rr += kCT) {
-                const int b = lo + rr / RB, r = rr % RB, row = b * RB + r;
-                if (row >= H) continue;
+            for (int rr = threadIdx.x; rr < dhi - dlo; rr += kCT) {
+                const int b = rr / RB, r = rr % RB, row = dlo + rr;
                 float tot = 0.f;
                 for (int t = 0; t <= K; ++t) {
                     const int slot = t == 0 ? K : t - 1;
-                    tot = fmaf(S.w[slot], ybuf[((size_t)(b - lo) * (K + 1) + t) * RB + r], tot);
+                    tot = fmaf(S.w[slot], ybuf[((size_t)b * (K + 1) + t) * RB + r], tot);
                 }
                 const float xo = __ldcg(a.b.xm + row) + tot;
                 a.b.x[row] = xo;
