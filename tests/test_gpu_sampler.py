@@ -175,3 +175,34 @@ def test_min_p_draws_match_oracle(sigma, T, top_p, min_p, max_undecided):
     print(f"sigma={sigma} T={T} top_p={top_p} min_p={min_p}: {undecided} of {n} draws "
           f"undecided, {differ} of them differ")
     assert undecided <= max_undecided, undecided
+
+
+# Vocabularies above 256 chunks of 1024 tokens (the one-launch form reads one chunk
+# sum per thread in its draw) take the per-pass kernels instead; 700000 tokens
+# exercise them.  Undecided draws (oracle only): 2 and 7 of 100; the flat sigma = 1
+# logits over 700000 tokens have dense CDF boundaries.
+@pytest.mark.parametrize("sigma,T,top_p,max_undecided", [(2.0, 0.7, 0.95, 4), (1.0, 1.0, 1.0, 9)])
+def test_large_vocabulary_draws_match_oracle(sigma, T, top_p, max_undecided):
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    from synth import torch_weights as tw
+    V = 700000
+    ws = workspace(V)
+    dev = tw.dev_logits(V, sigma, stream_id=13)
+    host = synth.host_logits(V, sigma, stream=13)
+    state = 0x9E3779B97F4A7C15
+    undecided = 0
+    for i in range(100):
+        tok, new_state = pdl.sample(dev, T, top_p, state, ws)
+        u, _ = oracle.uniform(state)
+        otok, info = oracle.sample(host, T, top_p, u)
+        band = undecided_band(info, otok)
+        if band > 0.0:
+            undecided += 1
+            assert within_band(host, T, top_p, u, band, tok, info), f"draw {i}"
+        else:
+            assert tok == otok, f"draw {i}: {tok} vs {otok}"
+        state = new_state
+    print(f"V={V} sigma={sigma} T={T} top_p={top_p}: {undecided} of 100 draws undecided")
+    assert undecided <= max_undecided, undecided
+    assert pdl.sample(dev, 0.0, 1.0, None, ws)[0] == oracle.argmax(host)
