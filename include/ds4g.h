@@ -161,6 +161,23 @@ int ds4g_decode_step(ds4g_session *s, int32_t token);
  * Same errors as ds4g_decode_step. */
 int ds4g_decode_layers(ds4g_session *s, int32_t token);
 
+/* ds4g_decode_layers with the final hidden state returned to the caller:
+ * hidden_host (host memory, hidden floats; pinned memory copies faster) receives
+ * it before the call returns (the call synchronises the session stream).  One call
+ * per token for a host loop that consumes the hidden state.  DS4G_EINVAL if
+ * hidden_host is NULL; otherwise the errors of ds4g_decode_step (the session is
+ * unchanged on DS4G_ETOKEN / DS4G_ECONTEXT). */
+int ds4g_decode_layers_host(ds4g_session *s, int32_t token, float *hidden_host);
+
+/* [P3] 阶段四 4.2 + 4.3 in one call: token through every layer and the lm_head
+ * (as ds4g_decode_step), then the next token drawn from the logits (as
+ * ds4g_sample, with its workspace, temperature, top_p and rng_state rules).
+ * Returns the drawn token id (>= 0) or a negative DS4G_* code; the call
+ * synchronises the session stream.  The one call per generated token of a
+ * sampling loop. */
+int32_t ds4g_decode_sample(ds4g_session *s, int32_t token, float temperature, float top_p,
+                           uint64_t *rng_state, void *workspace, size_t workspace_bytes);
+
 /* [P1] section 3 ds4_session_common_prefix: number of leading tokens shared by
  * the session's history and tokens[0..n). */
 int ds4g_session_common_prefix(const ds4g_session *s, const int32_t *tokens, int n);

@@ -498,6 +498,16 @@ int ds4g_decode_step(ds4g_session *s, int32_t token) { return decode_common(s, t
 
 int ds4g_decode_layers(ds4g_session *s, int32_t token) { return decode_common(s, token, false); }
 
+int ds4g_decode_layers_host(ds4g_session *s, int32_t token, float *hidden_host)
+{
+    if (!s || !hidden_host) return DS4G_EINVAL;
+    const int rc = decode_common(s, token, false);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(hidden_host, s->b.x, (size_t)s->m->d.H * 4, cudaMemcpyDeviceToHost, s->st);
+    if (!e) e = cudaStreamSynchronize(s->st);
+    return cuda_status(e);
+}
+
 int ds4g_session_common_prefix(const ds4g_session *s, const int32_t *tokens, int n)
 {
     if (!s || n < 0 || (n > 0 && !tokens)) return DS4G_EINVAL;
@@ -874,6 +884,20 @@ int32_t ds4g_sample_static(const float *logits, int n_vocab, float temperature, 
     unsigned u24 = 0;
     if (temperature > 0.f) u24 = (unsigned)(xorshift64s(rng_state) >> 40);
     return sample_common(logits, n_vocab, temperature, top_p, 0.f, u24, scratch, kSampleStaticBytes, stream);
+}
+
+int32_t ds4g_decode_sample(ds4g_session *s, int32_t token, float temperature, float top_p, uint64_t *rng_state,
+                           void *workspace, size_t workspace_bytes)
+{
+    if (!s) return DS4G_EINVAL;
+    const int rc = sample_args_ok(s->b.logits, s->m->d.V, temperature, top_p, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (temperature > 0.f && (!rng_state || *rng_state == 0)) return DS4G_EINVAL;
+    const int drc = decode_common(s, token, true);
+    if (drc) return drc;
+    unsigned u24 = 0;
+    if (temperature > 0.f) u24 = (unsigned)(xorshift64s(rng_state) >> 40);
+    return sample_common(s->b.logits, s->m->d.V, temperature, top_p, 0.f, u24, workspace, workspace_bytes, s->st);
 }
 
 const char *ds4g_strerror(int code)

@@ -89,6 +89,8 @@ def lib():
             "ds4g_session_status": ([vp], i32),
             "ds4g_session_set_trace": ([vp, vp, sz], i32),
             "ds4g_session_set_probe": ([vp, vp, i32, vp], i32),
+            "ds4g_decode_layers_host": ([vp, C.c_int32, vp], i32),
+            "ds4g_decode_sample": ([vp, C.c_int32, C.c_float, C.c_float, vp, vp, sz], C.c_int32),
             "ds4g_session_set_timing": ([vp, i32], i32),
             "ds4g_session_timing": ([vp, vp, vp, i32], i32),
             "ds4g_sample": ([vp, i32, C.c_float, C.c_float, vp, vp, sz, vp], C.c_int32),
@@ -200,6 +202,21 @@ class Session:
     def decode_layers(self, token: int) -> int:
         """One token through every layer without the lm_head."""
         return lib().ds4g_decode_layers(self.ptr, int(token))
+
+    def decode_layers_host(self, token: int, hidden_host: torch.Tensor) -> int:
+        """ds4g_decode_layers with the final hidden state copied into hidden_host (a
+        host float32 tensor of hidden elements, pinned for speed)."""
+        assert hidden_host.dtype == torch.float32 and not hidden_host.is_cuda
+        assert hidden_host.numel() == self.model.shape.hidden and hidden_host.is_contiguous()
+        return lib().ds4g_decode_layers_host(self.ptr, int(token), hidden_host.data_ptr())
+
+    def decode_sample(self, token: int, temperature: float, top_p: float, rng_state, ws: torch.Tensor):
+        """ds4g_decode_sample: one decode step and the next token's draw; returns
+        (token or negative code, new rng state)."""
+        st = C.c_uint64(rng_state if rng_state is not None else 0)
+        tok = lib().ds4g_decode_sample(self.ptr, int(token), float(temperature), float(top_p), C.byref(st),
+                                       ws.data_ptr(), ws.numel() * ws.element_size())
+        return tok, st.value
 
     def hidden(self) -> torch.Tensor:
         return self._view(lib().ds4g_session_hidden(self.ptr), self.model.shape.hidden,
