@@ -10,7 +10,9 @@
 // [token][head] query array).  All of them read the same keys: the union of their
 // windows, staged once.  Per block:
 //   S = (Qhi + Qlo) K^T      M 128 rows x N keys (<= KR) x K 128 dims, hi and lo
-//                            query tiles into one FP32 accumulator in TMEM;
+//                            query tiles into one FP32 accumulator in TMEM (with
+//                            hilo = 0 the queries, probabilities and output are
+//                            single BF16: no lo tiles, MMAs or stores);
 //   softmax                  the warps of a row read its S from TMEM, mask it to
 //                            the token's window, and write P = exp(scale (S - max))
 //                            as BF16 hi/lo rows into shared memory (the row sum
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kTaThreads, 1)
     k_attn_prefill_tc(const __grid_constant__ CUtensorMap qhi, const __grid_constant__ CUtensorMap qlo,
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap ohi, const __grid_constant__ CUtensorMap olo, int p0,
-                      int n, int NH, int W, int KR, int *status)
+                      int n, int NH, int W, int KR, int *status, int hilo)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -149,17 +151,19 @@ __global__ void __launch_bounds__(kTaThreads, 1)
         if (lane == 0) {
             // ---------------- TMA and MMA issue
             tma_prefetch_desc(&qhi);
-            tma_prefetch_desc(&qlo);
+            if (hilo) tma_prefetch_desc(&qlo);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
             auto issue_qk = [&](int blk) {
                 int kbase, span;
                 block_keys(blk, kbase, span);
-                mbar_expect_tx(bar_qk, 4 * kTaQBox + 2 * kvbox);
+                mbar_expect_tx(bar_qk, (hilo ? 4 : 2) * kTaQBox + 2 * kvbox);
                 tma_load_2d(sm + L.qhi, &qhi, 0, blk * kTaRows, bar_qk);
                 tma_load_2d(sm + L.qhi + kTaQBox, &qhi, 64, blk * kTaRows, bar_qk);
-                tma_load_2d(sm + L.qlo, &qlo, 0, blk * kTaRows, bar_qk);
-                tma_load_2d(sm + L.qlo + kTaQBox, &qlo, 64, blk * kTaRows, bar_qk);
+                if (hilo) {
+                    tma_load_2d(sm + L.qlo, &qlo, 0, blk * kTaRows, bar_qk);
+                    tma_load_2d(sm + L.qlo + kTaQBox, &qlo, 64, blk * kTaRows, bar_qk);
+                }
                 tma_load_2d(sm + L.k, &kmap, 0, kbase, bar_qk);
                 tma_load_2d(sm + L.k + kvbox, &kmap, 64, kbase, bar_qk);
             };
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kTaThreads, 1)
                     const uint64_t kd = sdesc_kmajor_sw128(sbase + L.k + (uint32_t)(ks >> 2) * kvbox +
                                                            (uint32_t)(ks & 3) * 32);
                     tc_mma_bf16(acc, sdesc_kmajor_sw128(sbase + L.qhi + qoff), kd, id_s, ks > 0);
-                    tc_mma_bf16(acc, sdesc_kmajor_sw128(sbase + L.qlo + qoff), kd, id_s, 1u);
+                    if (hilo) tc_mma_bf16(acc, sdesc_kmajor_sw128(sbase + L.qlo + qoff), kd, id_s, 1u);
                 }
                 tc_commit(&bar_s[it & 1]);
             };
@@ -197,7 +201,9 @@ __global__ void __launch_bounds__(kTaThreads, 1)
                     const uint32_t poff = (uint32_t)ks * 256;
                     tc_mma_bf16(acc, sdesc_kmajor_plain(sbase + L.phi + poff, 128, (uint32_t)KR * 16), vd, id_o,
                                 ks > 0);
-                    tc_mma_bf16(acc, sdesc_kmajor_plain(sbase + L.plo + poff, 128, (uint32_t)KR * 16), vd, id_o, 1u);
+                    if (hilo)
+                        tc_mma_bf16(acc, sdesc_kmajor_plain(sbase + L.plo + poff, 128, (uint32_t)KR * 16), vd, id_o,
+                                    1u);
                 }
                 tc_commit(bar_o);
             };
@@ -342,8 +348,10 @@ __global__ void __launch_bounds__(kTaThreads, 1)
                 const uint32_t off = pbase + (uint32_t)(c0 >> 3) * 128;
                 *reinterpret_cast<uint4 *>(sm + L.phi + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
                 *reinterpret_cast<uint4 *>(sm + L.phi + off + 128) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-                *reinterpret_cast<uint4 *>(sm + L.plo + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-                *reinterpret_cast<uint4 *>(sm + L.plo + off + 128) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+                if (hilo) {
+                    *reinterpret_cast<uint4 *>(sm + L.plo + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                    *reinterpret_cast<uint4 *>(sm + L.plo + off + 128) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+                }
             }
             red[part * kTaRows + r] = sum;
             // staged V rows past the last key are multiplied by P = 0: make them zeros
@@ -384,7 +392,7 @@ __global__ void __launch_bounds__(kTaThreads, 1)
                         split2_hilo(o[8 * j + 2 * u] * inv, o[8 * j + 2 * u + 1] * inv, wh[u], wl[u]);
                     const uint32_t cj = (uint32_t)r * 128 + (uint32_t)((((part & 1) * 4 + j) ^ (r & 7)) * 16);
                     *reinterpret_cast<uint4 *>(bh + cj) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                    *reinterpret_cast<uint4 *>(bl + cj) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                    if (hilo) *reinterpret_cast<uint4 *>(bl + cj) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                 }
                 fence_proxy_async_smem();   // the staged rows, before the tensor store reads them
                 tc_fence_before();
@@ -397,8 +405,10 @@ __global__ void __launch_bounds__(kTaThreads, 1)
             if (threadIdx.x == 0) {   // rows blk * 128 .. of the [token][head] output
                 tma_store_2d(&ohi, sm + L.phi, 0, blk * kTaRows);
                 tma_store_2d(&ohi, sm + L.phi + kTaQBox, 64, blk * kTaRows);
-                tma_store_2d(&olo, sm + L.phi + 2 * kTaQBox, 0, blk * kTaRows);
-                tma_store_2d(&olo, sm + L.phi + 3 * kTaQBox, 64, blk * kTaRows);
+                if (hilo) {
+                    tma_store_2d(&olo, sm + L.phi + 2 * kTaQBox, 0, blk * kTaRows);
+                    tma_store_2d(&olo, sm + L.phi + 3 * kTaQBox, 64, blk * kTaRows);
+                }
                 bulk_commit();   // read out of the P region while the next block's S and maxima run
             }
         }
@@ -437,14 +447,14 @@ cudaError_t attn_tc_row_map(const Dims &d, int P, const bf16 *base, CUtensorMap 
 
 cudaError_t attn_prefill_tc(const Dims &d, const CUtensorMap &qhi, const CUtensorMap &qlo, const TcKVMaps &kv,
                             const CUtensorMap &ohi, const CUtensorMap &olo, int p0, int n, int *status,
-                            cudaStream_t st, int nsm)
+                            cudaStream_t st, int nsm, bool hilo)
 {
     const int TB = kTaRows / d.NH, nblk = (n + TB - 1) / TB;
     if (nblk <= 0) return cudaSuccess;
     const int KR = ta_key_rows(d.W, d.NH);
     const int grid = nblk < nsm ? nblk : nsm;
     return launch_pdl(k_attn_prefill_tc, dim3(grid), dim3(kTaThreads), attn_tc_smem(d), st, qhi, qlo, kv.k, kv.v, ohi,
-                      olo, p0, n, (int)d.NH, (int)d.W, KR, status);
+                      olo, p0, n, (int)d.NH, (int)d.W, KR, status, hilo ? 1 : 0);
 }
 
 }  // namespace ds4g

@@ -324,7 +324,7 @@ struct EpiQRope {   // Q[m][n..n+3] = RoPE(q) in FP32 (the attention's input)
     }
 };
 
-struct EpiQRopeHiLo {   // RoPE(q) as hi/lo BF16 [token][head][dim] rows (the tcgen05 attention's input)
+struct EpiQRopeHiLo {   // RoPE(q) as hi/lo BF16 [token][head][dim] rows (the tcgen05 attention's input; lo may be null)
     bf16 *hi, *lo;
     const float2 *rope;
     int QD, HD, p0;
@@ -339,8 +339,9 @@ struct EpiQRopeHiLo {   // RoPE(q) as hi/lo BF16 [token][head][dim] rows (the tc
         for (int j = 0; j < 4; ++j) split_hilo(r[j], h[j], l[j]);
         *reinterpret_cast<uint2 *>(hi + (size_t)m * QD + n) =
             make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
-        *reinterpret_cast<uint2 *>(lo + (size_t)m * QD + n) =
-            make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+        if (lo)
+            *reinterpret_cast<uint2 *>(lo + (size_t)m * QD + n) =
+                make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
     }
 };
 
@@ -599,7 +600,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         if (attn_tc) {
             bf16 *q_hi = (bf16 *)pb.Q, *q_lo = q_hi + (size_t)pb.P * d.QD;
             if ((e = tc::launch<false, HL>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
-                                       EpiQRopeHiLo{q_hi, q_lo, rope, d.QD, d.HD, p0}, ny, nsm, st)))
+                                       EpiQRopeHiLo{q_hi, HL ? q_lo : nullptr, rope, d.QD, d.HD, p0}, ny, nsm, st)))
                 return e;
         } else if ((e = tc::launch<false, HL>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
                                           EpiQRope{(float *)pb.Q, rope, d.QD, d.HD, p0}, ny, nsm, st))) {
@@ -611,7 +612,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             return e;
         if (attn_tc) {
             if ((e = attn_prefill_tc(d, am.q_hi, am.q_lo, kvm[l], am.oa_hi, am.oa_lo, p0, n, pb.status, st,
-                                     nsm)))
+                                     nsm, HL)))
                 return e;
         } else if constexpr (std::is_same<TKV, bf16>::value) {
             if (attn_mma_eligible(d)) {

@@ -36,9 +36,10 @@ cudaError_t attn_tc_setup(const Dims &d, int max_smem);
 cudaError_t attn_tc_kv_maps(const Dims &d, const void *kc, const void *vc, int n_ctx, TcKVMaps &m);
 // Map of a [P * NH][128] BF16 array of [token][head] rows in 128-row boxes.
 cudaError_t attn_tc_row_map(const Dims &d, int P, const bf16 *base, CUtensorMap &m);
+// hilo: queries, probabilities and output as BF16 hi/lo pairs; otherwise single BF16.
 cudaError_t attn_prefill_tc(const Dims &d, const CUtensorMap &qhi, const CUtensorMap &qlo, const TcKVMaps &kv,
                             const CUtensorMap &ohi, const CUtensorMap &olo, int p0, int n, int *status,
-                            cudaStream_t st, int nsm);
+                            cudaStream_t st, int nsm, bool hilo);
 cudaError_t tc_layer_maps(const Dims &d, const LayerPtrs &w, TcLayerMaps &m);
 TcActPtrs tc_act_ptrs(const Dims &d, const PrefillBufs &pb);
 cudaError_t tc_act_maps(const Dims &d, const PrefillBufs &pb, TcActMaps &m);
