@@ -1,26 +1,24 @@
 // Tensor-core GEMM for the layer-major prefill (sm_103a, tcgen05 + TMA).
 //
-//   out[token][n] = sum_k (Xhi[token][k] + Xlo[token][k]) * W[n][k]
+//   out[token][n] = sum_k X[token][k] * W[n][k]
 //
-// W is a BF16 weight matrix ([out][in], K contiguous).  The activations are
-// carried as two BF16 arrays: hi = bf16(x) and lo = bf16(x - hi), so that every
-// product is taken with about 16 significant bits of x and accumulated in FP32.
-// With single BF16 activations the prefill's hidden states drift by about 0.5 %
-// per layer, which flips router top-6 decisions (the 6th-to-7th score gaps are
-// small); the split keeps the decisions of an FP32 computation.
+// W is a BF16 weight matrix ([out][in], K contiguous) and X BF16 activations;
+// products accumulate in FP32.  With LO the activations are carried as two BF16
+// arrays, hi = bf16(x) and lo = bf16(x - hi), and X = hi + lo: every product is
+// then taken with about 16 significant bits of x (two MMAs per K step into the
+// same accumulator).  The router's GEMM uses the pair, so that its top-6
+// decisions are those of an FP32 computation outside the rounding band.
 //
 // Orientation: 128 tokens are the MMA's M side and WN weight rows (256, or 128 for
-// GEMMs with few output tiles) its N side.  Per 16-wide K step the hi and the lo
-// token tile are each multiplied with the same weight tile into one FP32
-// accumulator in tensor memory (128 lanes = tokens, WN columns = features).  With
-// the weights on the wide side, every byte the tensor core reads from shared
-// memory feeds twice the products of a 128 x 128 tile, which is what bounds these
-// GEMMs (shared-memory bandwidth), not the tensor pipe.
+// GEMMs with few output tiles) its N side.  With the weights on the wide side,
+// every byte the tensor core reads from shared memory feeds twice the products of
+// a 128 x 128 tile; shared-memory bandwidth, not the tensor pipe, bounds the dense
+// GEMMs, and the weight stream from HBM bounds the routed ones.
 //
 // Persistent: one CTA per SM walks the output tiles (weight block fastest, so CTAs
 // running together share a token tile in L2) with 320 threads:
 //   warp 0 lane 0   TMA producer: per 64-wide K stage, the weight tile (WN rows, as
-//                   128-row boxes) and the hi and lo token tiles (16 KB each),
+//                   128-row boxes) and the token tile (16 KB; hi and lo with LO),
 //                   128-byte swizzled, into a shared-memory ring (full / empty
 //                   mbarriers) that runs on across tile boundaries;
 //   warp 1          allocates two accumulators in TMEM (2 x WN columns); lane 0
@@ -97,10 +95,11 @@ struct Args {
     int gld;
 };
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait_group()
+// An arrive-on of *bar that fires once every earlier cp.async of this thread has
+// completed; the barrier's expected count includes this arrival (noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
 {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 struct NoAux {};
@@ -169,7 +168,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], GA ? 1 + GWARPS : 1);   // TMA, and each gather warp
+            mbar_init(&full[s], GA ? 1 + 32 * GWARPS : 1);   // TMA, and each gather lane
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -275,6 +274,9 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    // gathered token rows were written by cp.async (generic proxy); the
+                    // tensor core reads them through the async proxy
+                    if constexpr (GA) fence_proxy_async_smem();
                     const uint32_t sa = smem_u32(sm + s * STAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -301,21 +303,15 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
             // [64 gw, 64 gw + 64), hi and lo, in the stage's 128-byte-swizzled token tiles
             // (16-byte chunk c of row t at chunk c ^ (t & 7) of its 128-byte row, as TMA lays
             // it).  Lane l copies chunk l % 8 of rows 4 q + l / 8, so that each copy
-            // instruction reads four whole 128-byte row segments.  A warp arrives on a
-            // stage's full barrier once its copies of that stage have landed (cp.async
-            // groups), right after issuing the next stage: two stages are in flight, and
-            // the arrival never waits for the tensor core to free a later stage.  Rows past
-            // the group's end are not copied: their products only reach accumulator rows
-            // the epilogue skips.
+            // instruction reads four whole 128-byte row segments.  Every lane arrives on the
+            // stage's full barrier through cp.async.mbarrier.arrive.noinc: the arrival fires
+            // when the lane's copies have landed, so the warp never waits for its copies and
+            // runs as far ahead as the free stages allow (the L2 latency of the token rows
+            // under a saturated weight stream is longer than two stages).  Rows past the
+            // group's end are not copied: their products only reach accumulator rows the
+            // epilogue skips.
             const int gw = warp - THREADS / 32, c = lane & 7;
-            unsigned it = 0, arrived = 0;
-            auto arrive_upto = [&](unsigned n) {
-                fence_proxy_async_smem();   // the copies are read by the tensor core next
-                __syncwarp();
-                if (lane == 0)
-                    for (unsigned q = arrived; q < n; ++q) mbar_arrive(&full[q % STAGES]);
-                arrived = n;
-            };
+            unsigned it = 0;
             bool ok = true;
             for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
                 int mb, e, r0, rend;
@@ -345,13 +341,10 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                         cp_async16(xt + off, a.gx_hi + so);
                         if constexpr (LO) cp_async16(xt + TILE_X + off, a.gx_lo + so);
                     }
-                    cp_async_commit();
-                    cp_async_wait_group<1>();   // the previous stage's copies have landed
-                    arrive_upto(it);
+                    cp_async_arrive_noinc(&full[s]);
                 }
             }
-            cp_async_wait_group<0>();   // nothing in flight at exit; the last stages land
-            arrive_upto(it);
+            cp_async_wait_all();   // nothing in flight at exit
         }
     } else {
         // ---------------- epilogue (warps 2-9): warp w reads TMEM lane quarter w % 4
