@@ -162,9 +162,15 @@ int ds4g_decode_step(ds4g_session *s, int32_t token);
 int ds4g_decode_layers(ds4g_session *s, int32_t token);
 
 /* ds4g_decode_layers with the final hidden state returned to the caller:
- * hidden_host (host memory, hidden floats; pinned memory copies faster) receives
- * it before the call returns (the call synchronises the session stream).  One call
- * per token for a host loop that consumes the hidden state.  DS4G_EINVAL if
+ * hidden_host (host memory, hidden floats) holds it when the call returns.  Pinned
+ * (page-locked) memory is written by the persistent decode kernel itself through its
+ * device view, and the kernel's last CTA signals completion through a pinned word of
+ * the session (64 bytes of pinned host memory, allocated on first use and freed by
+ * ds4g_session_destroy); the call returns on that signal, while the kernel may still
+ * be exiting (later work on the session stream is ordered after it).  Other memory
+ * gets a device-to-host copy and a stream synchronisation.  DS4G_ETIMEOUT if the
+ * kernel gave up a wait (see ds4g_session_status).  One call per token for a host
+ * loop that consumes the hidden state.  DS4G_EINVAL if
  * hidden_host is NULL; otherwise the errors of ds4g_decode_step (the session is
  * unchanged on DS4G_ETOKEN / DS4G_ECONTEXT). */
 int ds4g_decode_layers_host(ds4g_session *s, int32_t token, float *hidden_host);

@@ -53,6 +53,9 @@ struct ds4g_session {
     float *last_x = nullptr;          // [L+1][H] layer inputs of the last prefilled token
     std::vector<int32_t> probe_pos;   // positions whose layer inputs are recorded
     float *probe_buf = nullptr;       // caller's [n][L+1][H] record buffer
+    unsigned *done_h = nullptr;       // pinned host word the persistent kernel signals through
+    unsigned *done_d = nullptr;       // its device view
+    unsigned done_seq = 0;            // value of the last signal asked for
     bool timing = false;
     cudaEvent_t ev[DS4G_K_COUNT][2];
     double t_ms[DS4G_K_COUNT] = {};
@@ -303,6 +306,7 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     b.logits = (float *)take((size_t)d.V * 4);
     b.counters = (unsigned *)take(64);
     b.layer_x = nullptr;
+    b.x_out = nullptr;
     s->bar = (unsigned *)take(64);
     s->status = (int *)(s->bar + 4);
     s->qflag = (unsigned *)take((size_t)d.NH * 4);
@@ -347,6 +351,7 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
 void ds4g_session_destroy(ds4g_session *s)
 {
     if (!s) return;
+    if (s->done_h) cudaFreeHost(s->done_h);
     if (s->timing)
         for (int k = 0; k < DS4G_K_COUNT; ++k) {
             cudaEventDestroy(s->ev[k][0]);
@@ -403,7 +408,15 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
     return DS4G_OK;
 }
 
-static int decode_common(ds4g_session *s, int32_t token, bool logits)
+// Where a persistent launch hands its result to a waiting host thread: the final
+// hidden state into x_out (a device view of pinned host memory) and a completion
+// signal into the session's pinned word.  `used` tells whether the launch took it.
+struct HostOut {
+    float *x_out = nullptr;
+    bool used = false;
+};
+
+static int decode_common(ds4g_session *s, int32_t token, bool logits, HostOut *ho = nullptr)
 {
     if (!s) return DS4G_EINVAL;
     const Dims &d = s->m->d;
@@ -424,6 +437,12 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
         pa.rope = s->rope;
         pa.b = s->b;
         pa.b.layer_x = rec;
+        if (ho && s->done_d) {
+            pa.b.x_out = ho->x_out;
+            if (++s->done_seq == 0) s->done_seq = 1;   // 0 is the word's initial value
+            pa.done_flag = s->done_d;
+            pa.done_seq = s->done_seq;
+        }
         pa.tok_embd = s->m->tok_embd;
         pa.lm_head = s->m->lm_head;
         pa.pos = s->len;
@@ -446,6 +465,7 @@ static int decode_common(ds4g_session *s, int32_t token, bool logits)
         if (pa.split_q) s->q_count += (unsigned)d.L;   // one query half per head and layer
         s->hist[s->len] = token;
         s->len += 1;
+        if (ho) ho->used = pa.done_flag != nullptr;
         return DS4G_OK;
     }
     StepArgs a = step_base(s);
@@ -498,11 +518,64 @@ int ds4g_decode_step(ds4g_session *s, int32_t token) { return decode_common(s, t
 
 int ds4g_decode_layers(ds4g_session *s, int32_t token) { return decode_common(s, token, false); }
 
+// The session's pinned completion word (allocated on first use; host memory).
+static bool done_word(ds4g_session *s)
+{
+    if (s->done_h) return true;
+    void *h = nullptr, *dv = nullptr;
+    if (cudaHostAlloc(&h, 64, cudaHostAllocMapped) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (cudaHostGetDevicePointer(&dv, h, 0) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeHost(h);
+        return false;
+    }
+    s->done_h = static_cast<unsigned *>(h);
+    s->done_d = static_cast<unsigned *>(dv);
+    __atomic_store_n(s->done_h, 0u, __ATOMIC_RELEASE);
+    return true;
+}
+
+// Waits for the launch's completion signal.  Every wait inside the kernel is
+// bounded, so the stream drains in any case; a drained stream without the signal
+// means the kernel gave up (DS4G_ETIMEOUT), and the ticket is cleared for the next
+// launch.
+static int wait_done(ds4g_session *s, unsigned seq)
+{
+    for (unsigned n = 1;; ++n) {
+        if (__atomic_load_n(s->done_h, __ATOMIC_ACQUIRE) == seq) return DS4G_OK;
+        if ((n & 255u) == 0) {
+            const cudaError_t q = cudaStreamQuery(s->st);
+            if (q == cudaErrorNotReady) continue;
+            if (q != cudaSuccess) return cuda_status(q);
+            if (__atomic_load_n(s->done_h, __ATOMIC_ACQUIRE) == seq) return DS4G_OK;
+            cudaError_t e = cudaMemsetAsync(s->b.counters, 0, 64, s->st);
+            if (!e) e = cudaStreamSynchronize(s->st);
+            return e ? cuda_status(e) : DS4G_ETIMEOUT;
+        }
+    }
+}
+
 int ds4g_decode_layers_host(ds4g_session *s, int32_t token, float *hidden_host)
 {
     if (!s || !hidden_host) return DS4G_EINVAL;
-    const int rc = decode_common(s, token, false);
+    // Pinned (page-locked) host memory has a device view: the persistent kernel writes
+    // the hidden state there itself and signals completion through a pinned word, so
+    // the step needs neither a copy-engine transfer nor a stream synchronisation.
+    // Other memory gets the copy.
+    HostOut ho;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, hidden_host) == cudaSuccess) {
+        if (at.type == cudaMemoryTypeHost && at.devicePointer && done_word(s))   // dereferenceable here
+            ho.x_out = static_cast<float *>(at.devicePointer);
+    } else {
+        cudaGetLastError();   // not a pointer the runtime knows: plain host memory
+    }
+    const int rc = decode_common(s, token, false, ho.x_out ? &ho : nullptr);
     if (rc) return rc;
+    if (ho.used) return wait_done(s, s->done_seq);
     cudaError_t e = cudaMemcpyAsync(hidden_host, s->b.x, (size_t)s->m->d.H * 4, cudaMemcpyDeviceToHost, s->st);
     if (!e) e = cudaStreamSynchronize(s->st);
     return cuda_status(e);

@@ -45,6 +45,8 @@ struct DecodeBufs {
     int *status;         // session status word (DS4G_* error raised on the device)
     float *layer_x;      // optional [L+1][H]: the residual entering each layer (row 0 the
                          // embedding), then the final hidden state; null: not recorded
+    float *x_out;        // optional [H]: the final hidden state written here as well (the
+                         // device view of a pinned host buffer); persistent kernel only
 };
 
 // Arguments of every decode kernel: one layer at one position.
@@ -79,6 +81,9 @@ struct PersistArgs {
     int *status;               // DS4G_ETIMEOUT if a barrier wait gave up
     unsigned long long *trace; // optional [events][gridDim] stage start times (ns)
     int trace_events;
+    unsigned *done_flag;       // optional: device view of a pinned host word; the last CTA to
+    unsigned done_seq;         // finish writes done_seq there (system-scope release) once every
+                               // output of the launch is written
 };
 
 // ------------------------------------------------------------------ device helpers

@@ -38,6 +38,7 @@ static constexpr int kNSlot = 11;                   // ring slots
 static constexpr int kNC = kNSlot;                  // consumer warps, one per slot
 static constexpr int kCT = kNC * 32;                // consumer threads
 static constexpr int kPThreads = kCT + 32;          // + the producer warp
+static constexpr int kDoneTicket = 1;              // DecodeBufs::counters slot of the completion ticket
 static constexpr int kSlot = 16384;                 // bytes per ring slot
 static constexpr int kMaxR = 32;                    // rows per item at most
 
@@ -1249,6 +1250,7 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
                 const float xo = __ldcg(a.b.xm + row) + tot;
                 a.b.x[row] = xo;
                 if (a.b.layer_x) a.b.layer_x[(size_t)(l + 1) * H + row] = xo;
+                if (a.b.x_out && l + 1 == d.L) a.b.x_out[row] = xo;
             }
         }
         if (l + 1 < d.L || a.logits)
@@ -1268,6 +1270,17 @@ __device__ __forceinline__ void consumer_warps(const PersistArgs &a, Shared &S, 
     }
     csync();
     stamp(a, d.L * 7 + 1);
+    if (a.done_flag && threadIdx.x == 0) {
+        // every consumer thread's outputs of this launch precede the csync above; the
+        // last CTA through the ticket tells the waiting host thread
+        __threadfence_system();
+        const unsigned t = atomicAdd(&a.b.counters[kDoneTicket], 1u);
+        if (t == gridDim.x - 1) {
+            a.b.counters[kDoneTicket] = 0u;   // ready for the next launch
+            __threadfence_system();
+            st_release_sys(a.done_flag, a.done_seq);
+        }
+    }
 }
 
 template <typename TW, typename TKV>

@@ -132,6 +132,11 @@ __device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Release store at system scope (a host thread reads the word with acquire).
+__device__ __forceinline__ void st_release_sys(unsigned *p, unsigned v)
+{
+    asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05
 

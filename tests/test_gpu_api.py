@@ -28,20 +28,25 @@ def test_decode_layers_host_equals_decode_layers(model):
     prompt = synth.host_tokens(40, SHAPE.vocab, stream=81)
     a, b = pdl.Session(model, 64), pdl.Session(model, 64)
     assert a.prefill(prompt) == 0 and b.prefill(prompt) == 0
-    host = torch.empty(SHAPE.hidden, dtype=torch.float32, pin_memory=True)
-    for t in synth.host_tokens(5, SHAPE.vocab, stream=82):
+    # pinned memory (written by the kernel through its device view) and pageable
+    # memory (copied) take the two routes of the call
+    pinned = torch.empty(SHAPE.hidden, dtype=torch.float32, pin_memory=True)
+    pageable = torch.empty(SHAPE.hidden, dtype=torch.float32)
+    for i, t in enumerate(synth.host_tokens(6, SHAPE.vocab, stream=82)):
+        host = pinned if i % 2 == 0 else pageable
+        host.fill_(float("nan"))
         assert a.decode_layers(int(t)) == 0
         assert b.decode_layers_host(int(t), host) == 0
+        assert torch.equal(b.hidden().cpu(), host)   # complete when the call returns
         torch.cuda.synchronize()
         assert torch.equal(a.hidden().cpu(), host)
-        assert torch.equal(b.hidden().cpu(), host)
-    assert a.len == b.len == 45
+    assert a.len == b.len == 46
     for l in range(SHAPE.n_layers):
         for x, y in zip(a.kv(l), b.kv(l)):
             assert torch.equal(x[:45], y[:45])
     # errors: a token out of range leaves the session as it was; NULL host buffer
-    assert b.decode_layers_host(SHAPE.vocab, host) == pdl.ds4g.ETOKEN and b.len == 45
-    assert pdl.ds4g.lib().ds4g_decode_layers_host(b.ptr, 1, None) == pdl.ds4g.EINVAL and b.len == 45
+    assert b.decode_layers_host(SHAPE.vocab, pinned) == pdl.ds4g.ETOKEN and b.len == 46
+    assert pdl.ds4g.lib().ds4g_decode_layers_host(b.ptr, 1, None) == pdl.ds4g.EINVAL and b.len == 46
 
 
 @pytest.mark.parametrize("temperature,top_p", [(0.0, 1.0), (0.7, 0.95), (1.0, 1.0)])
