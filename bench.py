@@ -266,9 +266,12 @@ def workload_config(m):
 #   each step truncates the session to 0 and prefills the same prompt again.
 # prefill-small: one full-width layer with 128 routed experts and 2048 tokens (about
 #   3 GB on the device; still 96 tokens per expert, as in prefill-full).
+# prefill-layer: one full-width layer with 128 routed experts and 4096 tokens (about
+#   5 GB on the device): the dense GEMMs and the attention at prefill-full's shapes.
 CASES = {"decode-full": dict(), "decode-small": dict(n_experts=32, vocab=8192),
-         "prefill-full": dict(n_layers=8), "prefill-small": dict(n_layers=1, n_experts=128)}
-PREFILL_TOKENS = {"prefill-full": 4096, "prefill-small": 2048}
+         "prefill-full": dict(n_layers=8), "prefill-small": dict(n_layers=1, n_experts=128),
+         "prefill-layer": dict(n_layers=1, n_experts=128)}
+PREFILL_TOKENS = {"prefill-full": 4096, "prefill-small": 2048, "prefill-layer": 4096}
 
 
 def run_case(args):

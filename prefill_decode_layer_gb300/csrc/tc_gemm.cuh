@@ -63,12 +63,15 @@ static constexpr int EPI_BATCH = 8;                          // functor loads in
 // Tile geometry.  WN weight rows per tile; with the lo token tile (LO), 256 -> 3
 // stages of 64 KB and 128 -> 4 stages of 48 KB; without it, 256 -> 4 stages of 48 KB
 // and 128 -> 6 stages of 32 KB.  Plain tiles add the epilogue's staging rows.
-template <bool GU, int WN, bool LO> struct Geo {
+// CG = 2 (CTA pairs, WN = 256): each CTA holds one 128-row half of the weight tile,
+// so a stage is 32 KB (48 KB with LO) and 6 (4) stages fit.
+template <bool GU, int WN, bool LO, int CG = 1> struct Geo {
     static_assert(WN == 128 || WN == 256, "weight tile width");
     static_assert(!GU || WN == 256, "gate/up tiles hold 128 gate + 128 up rows");
-    static constexpr uint32_t TILE_W = WN * BK * 2;
+    static_assert(CG == 1 || WN == 256, "CTA pairs split a 256-row weight tile");
+    static constexpr uint32_t TILE_W = WN / CG * BK * 2;             // this CTA's weight rows
     static constexpr uint32_t STAGE = TILE_W + (LO ? 2 : 1) * TILE_X;   // W, X hi[, X lo]
-    static constexpr int STAGES = LO ? (WN == 256 ? 3 : 4) : (WN == 256 ? 4 : 6);
+    static constexpr int STAGES = CG == 2 ? (LO ? 4 : 6) : LO ? (WN == 256 ? 3 : 4) : (WN == 256 ? 4 : 6);
     static constexpr uint32_t TMEM_COLS = 2 * WN;           // two tiles in flight
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (GU ? 0 : EPI_BYTES) + 256;
 };
@@ -126,13 +129,23 @@ __device__ __forceinline__ float4 staged(const float *wstg, int t, int g)
 // by GWARPS extra warps with 16-byte cp.async copies (the maps xhi, xlo are unused).
 // LO: the activations' lo half takes part (two MMAs per K step); without it the
 // products are taken with the BF16 activations alone (xlo / gx_lo are not read).
-template <class Epi, bool GU, int WN, bool GA, bool LO>
+// CG = 2 (dense only; launched in clusters of 2): the two CTAs of a cluster compute
+// the two token tiles 2j, 2j + 1 against the same 256 weight rows with one
+// tcgen05.mma.cta_group::2 of M = 256 per K step, issued by the even CTA.  Each CTA
+// loads its own token tile and one 128-row half of the weight tile (the even CTA
+// the first half; for GU the gate rows, the odd one the up rows), both completing
+// on the even CTA's full barrier; the MMA completions arrive on both CTAs' empty
+// and accumulator barriers (multicast commit), and the epilogue warps of both
+// report a drained accumulator to the even CTA.  Per CTA and K step the tensor core
+// reads half the weight bytes from shared memory, and TMA writes half as many.
+template <class Epi, bool GU, int WN, bool GA, bool LO, int CG = 1>
 __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUtensorMap w1,
               const __grid_constant__ CUtensorMap xhi, const __grid_constant__ CUtensorMap xlo,
               const Args a, const Epi epi)
 {
-    using G = Geo<GU, WN, LO>;
+    static_assert(CG == 1 || (CG == 2 && !GA), "CTA pairs: dense GEMMs");
+    using G = Geo<GU, WN, LO, CG>;
     constexpr int STAGES = G::STAGES;
     constexpr uint32_t STAGE_BYTES = G::STAGE;
     extern __shared__ unsigned char smem_raw[];
@@ -141,7 +154,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + (GU ? 0 : EPI_BYTES));
     uint64_t *empty = full + STAGES;
     uint64_t *accf = empty + STAGES;   // [2] accumulator ready (MMA commit)
-    uint64_t *acce = accf + 2;         // [2] accumulator drained (256 epilogue threads)
+    uint64_t *acce = accf + 2;         // [2] accumulator drained (256 epilogue threads; CG 2: 16 warps)
     uint64_t *done = acce + 2;         // every MMA of this CTA completed
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *abort_flag = reinterpret_cast<int *>(tslot + 1);
@@ -149,13 +162,21 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
 
     const int mtiles = GU ? a.n_out / BOXW : (a.n_out + WN - 1) / WN;
     const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BT - 1) / BT;
-    const int total = mtiles * ntiles;
+    // CG 2: a work item is a pair of token tiles; the cluster's CTAs share it
+    const int total = mtiles * (CG == 2 ? (ntiles + 1) / 2 : ntiles);
     const int nk = a.k / BK;
+    const int rank = CG == 2 ? (int)cluster_rank() : 0;
+    const bool leader = rank == 0;
+    const int first = blockIdx.x / CG, stride = gridDim.x / CG;
     // tile -> (weight block mb, expert e, first token row r0, end row)
     auto tile_of = [&](int tau, int &mb, int &e, int &r0, int &rend) {
         mb = tau % mtiles;
         const int j = tau / mtiles;
-        if (a.tiles) {
+        if (CG == 2) {
+            e = 0;
+            r0 = (2 * j + rank) * BT;
+            rend = min(r0 + BT, a.m_tok);   // <= r0: no token of this CTA in the tile
+        } else if (a.tiles) {
             e = a.tiles[1 + 2 * j];
             r0 = a.tiles[2 + 2 * j];
             rend = min(r0 + BT, a.off[e + 1]);
@@ -168,20 +189,22 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], GA ? 1 + 32 * GWARPS : 1);   // TMA, and each gather lane
+            // TMA, and each gather lane
+            mbar_init(&full[s], GA ? 1 + 32 * GWARPS : 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
-            mbar_init(&acce[b], 256);
+            mbar_init(&acce[b], CG == 2 ? 16 : 256);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 1) tmem_alloc(tslot, G::TMEM_COLS);
+    if (warp == 1) tmem_alloc<CG>(tslot, G::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync_all();   // the peer's barriers exist before any remote use
     tc_fence_after();
     // with a programmatic launch the set-up above overlaps the previous kernel's tail;
     // its outputs (this GEMM's inputs) are complete past this point
@@ -203,26 +226,28 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
             if (LO) tma_prefetch_desc(&xlo);
             unsigned it = 0;
             bool ok = true;
-            for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
+            constexpr int NB = WN / BOXW / CG;   // 128-row weight boxes this CTA loads
+            for (int tau = first; ok && tau < total; tau += stride) {
                 int mb, e, r0, rend;
                 tile_of(tau, mb, e, r0, rend);
                 // the tile's weight boxes: (map, first row) of each 128-row box
-                const void *bm[WN / BOXW];
-                int brow[WN / BOXW];
+                const void *bm[NB];
+                int brow[NB];
 #pragma unroll
-                for (int h = 0; h < WN / BOXW; ++h) {
+                for (int hb = 0; hb < NB; ++hb) {
+                    const int h = hb + rank;   // CG 2: this CTA's half
                     if (GU) {
-                        bm[h] = h ? &w1 : &w0;
-                        brow[h] = e * a.n_out + mb * BOXW;
+                        bm[hb] = h ? &w1 : &w0;
+                        brow[hb] = e * a.n_out + mb * BOXW;
                     } else {
                         int row = mb * WN + h * BOXW;
                         if (row >= a.n_out) row = mb * WN;   // ragged last block: its features are skipped
                         if (a.piece_rows > 0 && row >= a.piece_rows) {
-                            bm[h] = &w1;
-                            brow[h] = row - a.piece_rows;
+                            bm[hb] = &w1;
+                            brow[hb] = row - a.piece_rows;
                         } else {
-                            bm[h] = &w0;
-                            brow[h] = e * a.n_out + row;
+                            bm[hb] = &w0;
+                            brow[hb] = e * a.n_out + row;
                         }
                     }
                 }
@@ -234,31 +259,52 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                         break;
                     }
                     unsigned char *st = sm + s * STAGE_BYTES;
-                    mbar_expect_tx(&full[s], GA ? G::TILE_W : STAGE_BYTES);
                     const int kx = i * BK;
+                    if constexpr (CG == 2) {
+                        // both CTAs' copies complete on the even CTA's full barrier, whose
+                        // one arrival expects the bytes of both (the odd CTA's copies may
+                        // land first: the transaction count goes below zero meanwhile, and
+                        // the phase cannot complete before the arrival)
+                        const uint32_t fb = cluster_map(&full[s], 0);
+                        if (leader) mbar_expect_tx(&full[s], 2 * STAGE_BYTES);
+                        tma_load_2d_pair(st, bm[0], kx, brow[0], fb);
+                        tma_load_2d_pair(st + G::TILE_W, &xhi, a.x_col0 + kx, r0, fb);
+                        if constexpr (LO) tma_load_2d_pair(st + G::TILE_W + TILE_X, &xlo, a.x_col0 + kx, r0, fb);
+                        continue;
+                    }
+                    mbar_expect_tx(&full[s], GA ? G::TILE_W : STAGE_BYTES);
 #pragma unroll
-                    for (int h = 0; h < WN / BOXW; ++h) tma_load_2d(st + h * BOX_BYTES, bm[h], kx, brow[h], &full[s]);
+                    for (int h = 0; h < NB; ++h) tma_load_2d(st + h * BOX_BYTES, bm[h], kx, brow[h], &full[s]);
                     if constexpr (!GA) {
                         tma_load_2d(st + G::TILE_W, &xhi, a.x_col0 + kx, r0, &full[s]);
                         if constexpr (LO) tma_load_2d(st + G::TILE_W + TILE_X, &xlo, a.x_col0 + kx, r0, &full[s]);
                     }
                 }
             }
-            // no copy may still be in flight when the CTA exits
+            // no copy may still be in flight when the CTA exits (CG 2: the copies complete
+            // on the even CTA's barrier; the stage's release by the MMA implies them)
             const unsigned n = it < (unsigned)STAGES ? it : (unsigned)STAGES;
             for (unsigned q = 1; q <= n; ++q) {
                 const unsigned i = it - q;
                 volatile int never = 0;
-                mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &never);
+                if constexpr (CG == 2)
+                    mbar_wait(&empty[i % STAGES], (i / STAGES) & 1, &never);
+                else
+                    mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &never);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && !leader) {
+            // CG 2, odd CTA: the even CTA issues the pair's MMAs, which read this CTA's
+            // shared memory and write its TMEM; wait for their completion
+            volatile int never = 0;
+            mbar_wait(done, 0, &never);
+        } else if (lane == 0) {
             // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(BT, WN);
+            constexpr uint32_t idesc = idesc_bf16_f32(BT * CG, WN);
             unsigned it = 0, tc = 0;
             bool ok = true;
-            for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x, ++tc) {
+            for (int tau = first; ok && tau < total; tau += stride, ++tc) {
                 const int b = tc & 1;
                 if (!mbar_wait(&acce[b], ((tc >> 1) & 1) ^ 1, ab)) {
                     give_up();
@@ -282,18 +328,18 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t wd = sdesc_kmajor_sw128(sa + kk * 32);
                         const uint64_t xh = sdesc_kmajor_sw128(sa + G::TILE_W + kk * 32);
-                        tc_mma_bf16(acc, xh, wd, idesc, (i | kk) != 0);
+                        tc_mma_bf16<CG>(acc, xh, wd, idesc, (i | kk) != 0);
                         if constexpr (LO) {
                             const uint64_t xl = sdesc_kmajor_sw128(sa + G::TILE_W + TILE_X + kk * 32);
-                            tc_mma_bf16(acc, xl, wd, idesc, 1u);
+                            tc_mma_bf16<CG>(acc, xl, wd, idesc, 1u);
                         }
                     }
-                    tc_commit(&empty[s]);   // the stage is free once these MMAs complete
+                    tc_commit<CG>(&empty[s]);   // the stage is free once these MMAs complete
                 }
-                if (ok) tc_commit(&accf[b]);   // the tile is complete once every MMA is
+                if (ok) tc_commit<CG>(&accf[b]);   // the tile is complete once every MMA is
             }
             // TMEM may be freed only after every MMA issued here has completed
-            tc_commit(done);
+            tc_commit<CG>(done);
             volatile int never = 0;
             mbar_wait(done, 0, &never);
         }
@@ -313,7 +359,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
             const int gw = warp - THREADS / 32, c = lane & 7;
             unsigned it = 0;
             bool ok = true;
-            for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
+            for (int tau = first; ok && tau < total; tau += stride) {
                 int mb, e, r0, rend;
                 tile_of(tau, mb, e, r0, rend);
                 int src[16];   // source row of this lane's tile rows in gx (-1: not copied)
@@ -353,8 +399,18 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
         const int half = (warp - 2) >> 2;
         const int tok = 32 * q + lane;     // this thread's token row in the tile
         float *wstg = stg + (warp - 2) * 32 * CH;   // this warp's [32 tokens][CH] staging rows
+        // the accumulator is drained: every thread (CG 1), or each warp to the even CTA (CG 2)
+        auto drained = [&](int b) {
+            tc_fence_before();
+            if constexpr (CG == 2) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(cluster_map(&acce[b], 0));
+            } else {
+                mbar_arrive(&acce[b]);
+            }
+        };
         unsigned tc = 0;
-        for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++tc) {
+        for (int tau = first; tau < total; tau += stride, ++tc) {
             int mb, e, r0, rend;
             tile_of(tau, mb, e, r0, rend);
             const int b = tc & 1;
@@ -375,10 +431,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                         tmem_ld32(lane_base + (uint32_t)c0, g);
                         tmem_ld32(lane_base + (uint32_t)(BOXW + c0), u);
                     }
-                    if (c0 + 64 >= BOXW) {   // this warp's share of the accumulator is drained
-                        tc_fence_before();
-                        mbar_arrive(&acce[b]);
-                    }
+                    if (c0 + 64 >= BOXW) drained(b);   // this warp's share of the accumulator
                     if (wlive && m < rend) {
                         float h[32];
 #pragma unroll
@@ -392,8 +445,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                     if (c + 2 >= WN / CH) {   // arrive once this warp's last chunk is read
                         float v[32];
                         if (wlive) tmem_ld32(lane_base + (uint32_t)(c * CH), v);
-                        tc_fence_before();
-                        mbar_arrive(&acce[b]);
+                        drained(b);
                         if (!wlive) break;
                         stage_row(wstg, lane, v);
                     } else {
@@ -428,9 +480,11 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // CG 2: neither CTA leaves while the other may still signal its barriers
+    if constexpr (CG == 2) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, G::TMEM_COLS);
+        tmem_dealloc<CG>(tmem, G::TMEM_COLS);
     }
 }
 
@@ -459,21 +513,68 @@ static cudaError_t launch_wn(const CUtensorMap &w0, const CUtensorMap &w1, const
                       Geo<GU, WN, LO>::SMEM, st, w0, w1, xhi, xlo, a, epi);
 }
 
+// The CTA-pair form (256-row weight tiles, dense): clusters of 2, as many as can be
+// resident at once (some GPCs may hold an odd number of SMs), at most one per pair of
+// token tiles and weight block.  0 clusters resident: cudaErrorNotSupported.
+template <bool GU, bool LO, class Epi>
+static cudaError_t launch_pair(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
+                               const CUtensorMap &xlo, const Args &a, const Epi &epi, long long work,
+                               cudaStream_t st)
+{
+    auto kern = k_tc_gemm<Epi, GU, 256, false, LO, 2>;
+    constexpr size_t smem = Geo<GU, 256, LO, 2>::SMEM;
+    static int clusters = -1;   // per instantiation: resident clusters of 2
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    if (clusters < 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e) return e;
+        cfg.gridDim = dim3(2);
+        cfg.numAttrs = 1;
+        int n = 0;
+        if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg))) return e;
+        clusters = n;
+    }
+    if (clusters <= 0) return cudaErrorNotSupported;
+    const long long nc = work < clusters ? work : clusters;
+    cfg.gridDim = dim3((unsigned)(2 * nc));
+    cfg.numAttrs = 2;
+    ++launch_count();
+    return cudaLaunchKernelEx(&cfg, kern, w0, w1, xhi, xlo, a, epi);
+}
+
 // ntile_bound: token tiles at most (dense: exact; grouped: the tile list's bound).
-// Plain GEMMs take 256-row weight tiles when that still gives every SM two tiles,
-// else 128-row tiles (twice the tiles, half the reuse of each token tile).
+// Dense GEMMs whose 256-row weight blocks times token-tile pairs give every SM pair
+// a work item run on CTA pairs; other plain GEMMs take 256-row weight tiles when
+// that still gives every SM two tiles, else 128-row tiles (twice the tiles, half the
+// reuse of each token tile).
 template <bool GU, bool LO, class Epi>
 static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &xhi,
                           const CUtensorMap &xlo, const Args &a, const Epi &epi, int ntile_bound, int nsm,
                           cudaStream_t st)
 {
     if (ntile_bound <= 0 || a.n_out <= 0) return cudaSuccess;
+    const long long blocks256 = GU ? a.n_out / BOXW : (a.n_out + 255) / 256;
+    if (!a.tiles && ntile_bound >= 2) {
+        const long long pairs = blocks256 * ((ntile_bound + 1) / 2);
+        if (2 * pairs >= nsm) return launch_pair<GU, LO>(w0, w1, xhi, xlo, a, epi, pairs, st);
+    }
     if constexpr (GU) {
-        const long long work = (long long)(a.n_out / BOXW) * ntile_bound;
+        const long long work = blocks256 * ntile_bound;
         if (a.grow) return launch_wn<true, 256, LO, Epi, true>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
         return launch_wn<true, 256, LO>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
     } else {
-        const long long w256 = (long long)((a.n_out + 255) / 256) * ntile_bound;
+        const long long w256 = blocks256 * ntile_bound;
         if (w256 >= 2ll * nsm) return launch_wn<false, 256, LO>(w0, w1, xhi, xlo, a, epi, w256, nsm, st);
         return launch_wn<false, 128, LO>(w0, w1, xhi, xlo, a, epi,
                                          (long long)((a.n_out + 127) / 128) * ntile_bound, nsm, st);
