@@ -30,6 +30,10 @@ cudaError_t sample_launch(const float *logits, int n, float temperature, float t
 // plus the last prefilled token (DS4G_DBG_PREFILL_LAYER_X).
 constexpr int kMaxProbe = 64;
 constexpr int kMaxRec = kMaxProbe + 1;
+// Parts of the tensor-core router GEMM's reduction (work items on twice the SMs;
+// the parts' scores are summed in order by k_router_topk), when E <= 256.
+constexpr int kRouterParts = 2;
+inline int router_parts(int E) { return E <= 256 ? kRouterParts : 1; }
 struct PrefillBufs {
     int P;            // chunk capacity (tokens)
     int *tok;         // [P]
@@ -39,7 +43,8 @@ struct PrefillBufs {
     void *C;          // [P][RQ+RKV] latents
     void *Q;          // [P][QD] queries after RoPE
     void *O;          // [P][QD] attention output
-    float *S;         // [P][E] router scores
+    float *S;         // [kRouterParts][P][E] router scores (partial sums of the reduction's parts)
+    char *end;        // one past the last byte laid out
     int *ids;         // [P][K]
     float *wts;       // [P][K]
     int *cnt;         // [E] tokens per expert

@@ -54,8 +54,11 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *X, const floa
 }
 
 // Router decision per token: top-k of the scores (ties to the lower id), softmax
-// over the selected scores.  One warp per token.
-__global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E, int K, int *status)
+// over the selected scores.  One warp per token.  The scores may come as two
+// partial sums (of the reduction's two parts, `part` elements apart; E <= 256),
+// added in part order (nparts 2; otherwise 1).
+__global__ void k_router_topk(const float *S, int nparts, size_t part, int *ids, float *wts, int n, int E, int K,
+                              int *status)
 {
     pdl_wait();      // inputs of the previous kernel (programmatic launch)
     pdl_trigger();
@@ -63,7 +66,22 @@ __global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E
     if (warp >= n) return;
     float sel[8];
     int sid[8];
-    const bool finite = warp_topk(S + (size_t)warp * E, E, K, sel, sid, lane);
+    bool finite;
+    if (nparts == 2) {   // both parts' loads in flight before the adds
+        const float *s0 = S + (size_t)warp * E, *s1 = s0 + part;
+        float x[8], y[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = lane + 32 * u;
+            x[u] = e < E ? s0[e] : 0.f;
+            y[u] = e < E ? s1[e] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] += y[u];
+        finite = warp_topk_r256(x, E, K, sel, sid, lane);
+    } else {
+        finite = warp_topk(S + (size_t)warp * E, E, K, sel, sid, lane);
+    }
     if (!finite && lane == 0) atomicCAS(status, 0, DS4G_ENONFINITE);
     if (lane == 0) {
         float sum = 0.f, w[8];
@@ -309,35 +327,16 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const TA *Q, void *Ov, bf1
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t prefill_bytes(const Dims &d, int P)
-{
-    const size_t ta = 4;  // activation element size
-    const size_t PK = (size_t)P * d.K;
-    size_t b = 0;
-    b += align256((size_t)P * 4);                        // tok
-    b += align256((size_t)P * d.H * 4);                  // X
-    b += align256((size_t)P * d.H * ta);                 // XN
-    b += align256((size_t)P * d.H * 4);                  // XN32
-    b += align256((size_t)P * (d.RQ + d.RKV) * ta);      // C
-    b += 2 * align256((size_t)P * d.QD * ta);            // Q, O
-    b += align256((size_t)P * d.E * 4);                  // S
-    b += 2 * align256(PK * 4);                           // ids, wts
-    b += align256((size_t)d.E * 4) + align256((size_t)(d.E + 1) * 4);
-    b += align256(PK * 4);                               // rows
-    b += align256(sort_segments(PK) * d.E * 4);          // segcnt
-    b += align256((PK / 16 + d.E + 2) * 2 * 4);          // tiles
-    b += align256(PK * d.I * ta);                        // HG
-    b += align256((size_t)P * d.I * ta);                 // HS
-    b += align256(PK * d.H * 4);                         // YS
-    return b;
-}
-
 void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb)
 {
     const size_t ta = 4;
     const size_t PK = (size_t)P * d.K;
-    char *p = base;
-    auto take = [&](size_t n) { char *r = p; p += align256(n); return (void *)r; };
+    size_t o = 0;   // offsets as integers: prefill_bytes walks from a null base
+    auto take = [&](size_t n) {
+        const size_t r = o;
+        o += align256(n);
+        return reinterpret_cast<void *>(reinterpret_cast<uintptr_t>(base) + r);
+    };
     pb.P = P;
     pb.tok = (int *)take((size_t)P * 4);
     pb.X = (float *)take((size_t)P * d.H * 4);
@@ -346,7 +345,7 @@ void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb)
     pb.C = take((size_t)P * (d.RQ + d.RKV) * ta);
     pb.Q = take((size_t)P * d.QD * ta);
     pb.O = take((size_t)P * d.QD * ta);
-    pb.S = (float *)take((size_t)P * d.E * 4);
+    pb.S = (float *)take((size_t)kRouterParts * P * d.E * 4);
     pb.ids = (int *)take(PK * 4);
     pb.wts = (float *)take(PK * 4);
     pb.cnt = (int *)take((size_t)d.E * 4);
@@ -357,6 +356,15 @@ void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb)
     pb.HG = take(PK * d.I * ta);
     pb.HS = take((size_t)P * d.I * ta);
     pb.YS = (float *)take(PK * d.H * 4);
+    pb.end = reinterpret_cast<char *>(reinterpret_cast<uintptr_t>(base) + o);
+}
+
+// The bytes prefill_carve lays out (the same walk from address 0).
+size_t prefill_bytes(const Dims &d, int P)
+{
+    PrefillBufs pb{};
+    prefill_carve(d, P, nullptr, pb);
+    return (size_t)reinterpret_cast<uintptr_t>(pb.end);
 }
 
 static size_t attn_prefill_smem(const Dims &d)
@@ -430,7 +438,7 @@ static cudaError_t chunk_t(const Dims &d, const LayerPtrs *layers, void *const *
         ++launch_count();
         ProbRouter<TW> pr{pb.XN32, (const TW *)w.w_router, pb.S, H, d.E};
         if ((e = gemm_dense<float, TW>(pr, n, d.E, H, st, nsm))) return e;
-        k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, pb.ids, pb.wts, n, d.E, K, pb.status);
+        k_router_topk<<<(n * 32 + 255) / 256, 256, 0, st>>>(pb.S, 1, 0, pb.ids, pb.wts, n, d.E, K, pb.status);
         ++launch_count();
         if ((e = group_by_expert(pb, nent, d.E, kGroupBM, st))) return e;
         const int max_tiles = nent / kGroupBM + d.E + 1;

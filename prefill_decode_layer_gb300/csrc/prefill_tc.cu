@@ -382,14 +382,15 @@ struct EpiAddX {   // residual: X[m][n..n+3] += v
     }
 };
 
-struct EpiScores {   // router scores S[m][n..n+3] in FP32
+struct EpiScores {   // router scores of reduction part s: S[s][m][n..n+3] in FP32
     float *S;
     int E;
+    size_t part;   // elements between the parts' score arrays
     using Aux = tc::NoAux;
     __device__ Aux load4(int, int, int) const { return {}; }
-    __device__ void store4(int m, int n, const float (&v)[4], const Aux &, int) const
+    __device__ void store4(int m, int n, const float (&v)[4], const Aux &, int s) const
     {
-        *reinterpret_cast<float4 *>(S + (size_t)m * E + n) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4 *>(S + s * part + (size_t)m * E + n) = make_float4(v[0], v[1], v[2], v[3]);
     }
 };
 
@@ -633,11 +634,17 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         if ((e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
                             (const float *)w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
             return e;
-        a.n_out = d.E, a.k = H;
-        if ((e = tc::launch<false, true>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E}, ny, nsm, st)))
+        // The router's reduction in fixed parts (twice the tiles on the SMs; the parts'
+        // scores are summed in order by the top-k), whatever the chunk.
+        const int parts = router_parts(d.E);
+        a.n_out = d.E, a.k = H, a.ksplit = parts;
+        const size_t part = (size_t)pb.P * d.E;
+        if ((e = tc::launch<false, true>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E, part}, ny, nsm,
+                                         st)))
             return e;
-        if ((e = launch_pdl(k_router_topk, dim3((n * 32 + 255) / 256), dim3(256), 0, st, (const float *)pb.S, pb.ids,
-                            pb.wts, n, d.E, K, pb.status)))
+        a.ksplit = 0;
+        if ((e = launch_pdl(k_router_topk, dim3((n * 32 + 255) / 256), dim3(256), 0, st, (const float *)pb.S,
+                            parts, part, pb.ids, pb.wts, n, d.E, K, pb.status)))
             return e;
         if ((e = group_by_expert(pb, nent, d.E, tc::BT, st))) return e;
         // routed gate/up + SwiGLU (grouped; the GEMM gathers each group's token rows of

@@ -53,7 +53,8 @@ cudaError_t prefill_chunk_tc(const Dims &d, const LayerPtrs *layers, const TcLay
 
 // prefill.cu kernels the tensor-core form shares
 __global__ void k_embed_rows(const uint16_t *table, const int *tok, float *X, int H);
-__global__ void k_router_topk(const float *S, int *ids, float *wts, int n, int E, int K, int *status);
+__global__ void k_router_topk(const float *S, int nparts, size_t part, int *ids, float *wts, int n, int E, int K,
+                              int *status);
 template <typename TKV>
 cudaError_t attn_prefill_hilo(const Dims &d, const float *Q, bf16 *o_hi, bf16 *o_lo, const TKV *kc,
                               const TKV *vc, int p0, int n, cudaStream_t st);

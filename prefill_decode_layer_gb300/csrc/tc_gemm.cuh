@@ -87,6 +87,8 @@ struct Args {
     int x_col0;       // first activation column read (a multiple of 8)
     int piece_rows;   // dense: rows of map w0 before map w1 starts (0: w0 only); a multiple of 128
     int m_tok;        // dense: token rows
+    int ksplit;       // dense, one CTA per tile: the reduction is cut into ksplit equal parts
+                      // (0 or 1: none); part s of a tile reaches the functor as e = s
     const int *tiles; // grouped: [0] = count, then (expert, first row) pairs
     const int *off;   // grouped: expert row offsets [E + 1]
     int *status;      // DS4G_ETIMEOUT on a wait that gave up
@@ -162,9 +164,11 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
 
     const int mtiles = GU ? a.n_out / BOXW : (a.n_out + WN - 1) / WN;
     const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BT - 1) / BT;
-    // CG 2: a work item is a pair of token tiles; the cluster's CTAs share it
-    const int total = mtiles * (CG == 2 ? (ntiles + 1) / 2 : ntiles);
-    const int nk = a.k / BK;
+    // CG 2: a work item is a pair of token tiles; the cluster's CTAs share it.
+    // Split reductions (CG 1, dense): ksplit work items per tile, one per part.
+    const int ksplit = CG == 1 && !a.tiles && a.ksplit > 1 ? a.ksplit : 1;
+    const int total = mtiles * (CG == 2 ? (ntiles + 1) / 2 : ntiles) * ksplit;
+    const int nk = a.k / ksplit / BK;
     const int rank = CG == 2 ? (int)cluster_rank() : 0;
     const bool leader = rank == 0;
     const int first = blockIdx.x / CG, stride = gridDim.x / CG;
@@ -181,8 +185,8 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
             r0 = a.tiles[2 + 2 * j];
             rend = min(r0 + BT, a.off[e + 1]);
         } else {
-            e = 0;
-            r0 = j * BT;
+            e = j / ntiles;   // the part of a split reduction (0 without)
+            r0 = (j % ntiles) * BT;
             rend = min(r0 + BT, a.m_tok);
         }
     };
@@ -230,6 +234,8 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
             for (int tau = first; ok && tau < total; tau += stride) {
                 int mb, e, r0, rend;
                 tile_of(tau, mb, e, r0, rend);
+                const int we = a.tiles ? e : 0;   // the expert (grouped) whose weights are read
+                const int ks = a.tiles ? 0 : e;   // the reduction part (dense; 0 unless split)
                 // the tile's weight boxes: (map, first row) of each 128-row box
                 const void *bm[NB];
                 int brow[NB];
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                     const int h = hb + rank;   // CG 2: this CTA's half
                     if (GU) {
                         bm[hb] = h ? &w1 : &w0;
-                        brow[hb] = e * a.n_out + mb * BOXW;
+                        brow[hb] = we * a.n_out + mb * BOXW;
                     } else {
                         int row = mb * WN + h * BOXW;
                         if (row >= a.n_out) row = mb * WN;   // ragged last block: its features are skipped
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                             brow[hb] = row - a.piece_rows;
                         } else {
                             bm[hb] = &w0;
-                            brow[hb] = e * a.n_out + row;
+                            brow[hb] = we * a.n_out + row;
                         }
                     }
                 }
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                         break;
                     }
                     unsigned char *st = sm + s * STAGE_BYTES;
-                    const int kx = i * BK;
+                    const int kx = (ks * nk + i) * BK;
                     if constexpr (CG == 2) {
                         // both CTAs' copies complete on the even CTA's full barrier, whose
                         // one arrival expects the bytes of both (the odd CTA's copies may
@@ -565,7 +571,8 @@ static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CU
 {
     if (ntile_bound <= 0 || a.n_out <= 0) return cudaSuccess;
     const long long blocks256 = GU ? a.n_out / BOXW : (a.n_out + 255) / 256;
-    if (!a.tiles && ntile_bound >= 2) {
+    const long long parts = !a.tiles && a.ksplit > 1 ? a.ksplit : 1;
+    if (!a.tiles && ntile_bound >= 2 && parts == 1) {
         const long long pairs = blocks256 * ((ntile_bound + 1) / 2);
         if (2 * pairs >= nsm) return launch_pair<GU, LO>(w0, w1, xhi, xlo, a, epi, pairs, st);
     }
@@ -574,10 +581,10 @@ static cudaError_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CU
         if (a.grow) return launch_wn<true, 256, LO, Epi, true>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
         return launch_wn<true, 256, LO>(w0, w1, xhi, xlo, a, epi, work, nsm, st);
     } else {
-        const long long w256 = blocks256 * ntile_bound;
+        const long long w256 = blocks256 * ntile_bound * parts;
         if (w256 >= 2ll * nsm) return launch_wn<false, 256, LO>(w0, w1, xhi, xlo, a, epi, w256, nsm, st);
         return launch_wn<false, 128, LO>(w0, w1, xhi, xlo, a, epi,
-                                         (long long)((a.n_out + 127) / 128) * ntile_bound, nsm, st);
+                                         (long long)((a.n_out + 127) / 128) * ntile_bound * parts, nsm, st);
     }
 }
 
