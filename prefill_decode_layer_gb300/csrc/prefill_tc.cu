@@ -287,21 +287,112 @@ cudaError_t attn_mma_setup(const Dims &d, int max_smem)
 }
 
 // ------------------------------------------------------------------ epilogues
-// Functors of the tensor-core GEMM: load4 fetches what a 4-feature store needs
-// from global memory (issued in batches by the GEMM), store4 writes.
+// Functors of the tensor-core GEMM.  Direct form (kDirect): the thread of the
+// epilogue that owns token m passes 32 adjacent features f0 .. f0 + 31 of it at a
+// time; load32 fetches what their store needs from global memory (issued ahead by
+// the GEMM), store32 writes.  Staged form: the same for 4 features at a time
+// (load4, store4), with the GEMM's instructions covering 4 tokens x 32 features.
+
+// 32 values as BF16 hi (and lo, unless null) halves: 4 16-byte stores each
+__device__ __forceinline__ void store_hilo32(bf16 *hi, bf16 *lo, const float (&v)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) split2_hilo(v[8 * q + 2 * j], v[8 * q + 2 * j + 1], wh[j], wl[j]);
+        reinterpret_cast<uint4 *>(hi)[q] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        if (lo) reinterpret_cast<uint4 *>(lo)[q] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    }
+}
+// 32 values as FP32 (8 16-byte stores) or BF16, rounded to nearest even (4)
+__device__ __forceinline__ void store32(float *p, const float (&v)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4 *>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+__device__ __forceinline__ void store32(bf16 *p, const float (&v)[32])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = pack_bf16x2(__float2bfloat16_rn(v[8 * q + 2 * j]), __float2bfloat16_rn(v[8 * q + 2 * j + 1]));
+        reinterpret_cast<uint4 *>(p)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// (cos, sin) of the 16 RoPE pairs of features f0 .. f0 + 31 of a head (f0 % 32 == 0)
+struct Rope16 {
+    float4 cs[8];   // pairs 2k and 2k + 1 in cs[k]
+};
+__device__ __forceinline__ Rope16 rope16(const float2 *rope, int pos, int HD, int f0)
+{
+    Rope16 r;
+    const float4 *p = reinterpret_cast<const float4 *>(rope + (size_t)pos * (HD / 2) + (f0 % HD) / 2);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r.cs[k] = p[k];
+    return r;
+}
+// v rotated pair by pair: (v[2i], v[2i+1]) by the angle of pair i
+__device__ __forceinline__ void rotate32(const float (&v)[32], const Rope16 &r, float (&o)[32])
+{
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float4 c = r.cs[k];
+        o[4 * k] = v[4 * k] * c.x - v[4 * k + 1] * c.y;
+        o[4 * k + 1] = v[4 * k] * c.y + v[4 * k + 1] * c.x;
+        o[4 * k + 2] = v[4 * k + 2] * c.z - v[4 * k + 3] * c.w;
+        o[4 * k + 3] = v[4 * k + 2] * c.w + v[4 * k + 3] * c.z;
+    }
+}
 
 struct EpiHiLo {   // out[m][n..n+3] as hi/lo BF16 (the next GEMM's input; lo may be null)
     bf16 *hi, *lo;
     int ld;
+    static constexpr bool kDirect = false;
     using Aux = tc::NoAux;
     __device__ Aux load4(int, int, int) const { return {}; }
     __device__ void store4(int m, int n, const float (&v)[4], const Aux &, int) const
     {
-        __align__(8) bf16 h[4], l[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) split_hilo(v[j], h[j], l[j]);
-        *reinterpret_cast<uint2 *>(hi + (size_t)m * ld + n) = *reinterpret_cast<const uint2 *>(h);
-        if (lo) *reinterpret_cast<uint2 *>(lo + (size_t)m * ld + n) = *reinterpret_cast<const uint2 *>(l);
+        uint32_t h0, l0, h1, l1;
+        split2_hilo(v[0], v[1], h0, l0);
+        split2_hilo(v[2], v[3], h1, l1);
+        *reinterpret_cast<uint2 *>(hi + (size_t)m * ld + n) = make_uint2(h0, h1);
+        if (lo) *reinterpret_cast<uint2 *>(lo + (size_t)m * ld + n) = make_uint2(l0, l1);
+    }
+};
+
+struct EpiQRope {   // Q[m][f0..f0+31] = RoPE(q) in FP32 (the attention's input)
+    float *Q;
+    const float2 *rope;
+    int QD, HD, p0;
+    static constexpr bool kDirect = true;
+    using Aux = Rope16;
+    __device__ Aux load32(int m, int f0, int) const { return rope16(rope, p0 + m, HD, f0); }
+    __device__ void store32(int m, int f0, const float (&v)[32], const Aux &cs, int) const
+    {
+        float r[32];
+        rotate32(v, cs, r);
+        ds4g::store32(Q + (size_t)m * QD + f0, r);
+    }
+};
+
+struct EpiQRopeHiLo {   // RoPE(q) as hi/lo BF16 [token][head][dim] rows (the tcgen05 attention's input; lo may be null)
+    bf16 *hi, *lo;
+    const float2 *rope;
+    int QD, HD, p0;
+    static constexpr bool kDirect = true;
+    using Aux = Rope16;
+    __device__ Aux load32(int m, int f0, int) const { return rope16(rope, p0 + m, HD, f0); }
+    __device__ void store32(int m, int f0, const float (&v)[32], const Aux &cs, int) const
+    {
+        float r[32];
+        rotate32(v, cs, r);
+        const size_t o = (size_t)m * QD + f0;
+        store_hilo32(hi + o, lo ? lo + o : nullptr, r);
     }
 };
 
@@ -310,46 +401,12 @@ __device__ __forceinline__ float4 rope_pairs(const float2 *rope, int pos, int HD
     return *reinterpret_cast<const float4 *>(rope + (size_t)pos * (HD / 2) + (n % HD) / 2);
 }
 
-struct EpiQRope {   // Q[m][n..n+3] = RoPE(q) in FP32 (the attention's input)
-    float *Q;
-    const float2 *rope;
-    int QD, HD, p0;
-    using Aux = float4;
-    __device__ Aux load4(int m, int n, int) const { return rope_pairs(rope, p0 + m, HD, n); }
-    __device__ void store4(int m, int n, const float (&v)[4], const Aux &cs, int) const
-    {
-        *reinterpret_cast<float4 *>(Q + (size_t)m * QD + n) =
-            make_float4(v[0] * cs.x - v[1] * cs.y, v[0] * cs.y + v[1] * cs.x, v[2] * cs.z - v[3] * cs.w,
-                        v[2] * cs.w + v[3] * cs.z);
-    }
-};
-
-struct EpiQRopeHiLo {   // RoPE(q) as hi/lo BF16 [token][head][dim] rows (the tcgen05 attention's input; lo may be null)
-    bf16 *hi, *lo;
-    const float2 *rope;
-    int QD, HD, p0;
-    using Aux = float4;
-    __device__ Aux load4(int m, int n, int) const { return rope_pairs(rope, p0 + m, HD, n); }
-    __device__ void store4(int m, int n, const float (&v)[4], const Aux &cs, int) const
-    {
-        const float r[4] = {v[0] * cs.x - v[1] * cs.y, v[0] * cs.y + v[1] * cs.x, v[2] * cs.z - v[3] * cs.w,
-                            v[2] * cs.w + v[3] * cs.z};
-        bf16 h[4], l[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) split_hilo(r[j], h[j], l[j]);
-        *reinterpret_cast<uint2 *>(hi + (size_t)m * QD + n) =
-            make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
-        if (lo)
-            *reinterpret_cast<uint2 *>(lo + (size_t)m * QD + n) =
-                make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
-    }
-};
-
 template <typename TKV>
 struct EpiKVRope {   // features [0, HD): K with RoPE, [HD, 2HD): V; appended at p0 + m
     TKV *kc, *vc;
     const float2 *rope;
     int HD, p0;
+    static constexpr bool kDirect = false;
     using Aux = float4;
     __device__ Aux load4(int m, int n, int) const
     {
@@ -373,6 +430,7 @@ struct EpiKVRope {   // features [0, HD): K with RoPE, [HD, 2HD): V; appended at
 struct EpiAddX {   // residual: X[m][n..n+3] += v
     float *X;
     int H;
+    static constexpr bool kDirect = false;
     using Aux = float4;
     __device__ Aux load4(int m, int n, int) const { return *reinterpret_cast<const float4 *>(X + (size_t)m * H + n); }
     __device__ void store4(int m, int n, const float (&v)[4], const Aux &x, int) const
@@ -386,6 +444,7 @@ struct EpiScores {   // router scores of reduction part s: S[s][m][n..n+3] in FP
     float *S;
     int E;
     size_t part;   // elements between the parts' score arrays
+    static constexpr bool kDirect = false;
     using Aux = tc::NoAux;
     __device__ Aux load4(int, int, int) const { return {}; }
     __device__ void store4(int m, int n, const float (&v)[4], const Aux &, int s) const
@@ -394,15 +453,53 @@ struct EpiScores {   // router scores of reduction part s: S[s][m][n..n+3] in FP
     }
 };
 
-struct EpiRoutedRows {   // routed expert output of grouped row m into its (token, slot) row
-    float *YS;
+// 4 consecutive values of a routed row as FP32 or BF16 (RNE)
+__device__ __forceinline__ void store_row4(float *p, const float (&v)[4])
+{
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store_row4(bf16 *p, const float (&v)[4])
+{
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(__float2bfloat16_rn(v[0]), __float2bfloat16_rn(v[1])),
+                                               pack_bf16x2(__float2bfloat16_rn(v[2]), __float2bfloat16_rn(v[3])));
+}
+// 16 bytes of a routed row (4 FP32 or 8 BF16 values), loaded raw; acc_row16 adds
+// w times its values, widened exactly, to r.
+__device__ __forceinline__ uint4 load_row16(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+__device__ __forceinline__ void acc_row16(float w, const uint4 &q, float (&r)[4], float)
+{
+    r[0] = fmaf(w, __uint_as_float(q.x), r[0]);
+    r[1] = fmaf(w, __uint_as_float(q.y), r[1]);
+    r[2] = fmaf(w, __uint_as_float(q.z), r[2]);
+    r[3] = fmaf(w, __uint_as_float(q.w), r[3]);
+}
+__device__ __forceinline__ void acc_row16(float w, const uint4 &q, float (&r)[8], bf16)
+{
+    const uint32_t a[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        r[2 * j] = fmaf(w, __uint_as_float(a[j] << 16), r[2 * j]);
+        r[2 * j + 1] = fmaf(w, __uint_as_float(a[j] & 0xffff0000u), r[2 * j + 1]);
+    }
+}
+
+template <typename TY>
+struct EpiRoutedRows {   // routed expert output of grouped row m into its (token, slot) row (FP32 or BF16)
+    TY *YS;
     const int *rows;
     int H;
+    int nrows;     // (token, slot) rows of the launch: a row index outside is never written
+    int *status;
+    static constexpr bool kDirect = false;
     using Aux = int;
     __device__ Aux load4(int m, int, int) const { return rows[m]; }
     __device__ void store4(int, int n, const float (&v)[4], const Aux &r, int) const
     {
-        *reinterpret_cast<float4 *>(YS + (size_t)r * H + n) = make_float4(v[0], v[1], v[2], v[3]);
+        if ((unsigned)r >= (unsigned)nrows) {
+            atomicCAS(status, 0, DS4G_EINVAL);
+            return;
+        }
+        store_row4(YS + (size_t)r * H + n, v);
     }
 };
 
@@ -411,83 +508,73 @@ struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16 (lo ma
     int ld;
     __device__ void store_row(int m, int i0, const float (&h)[32], int) const
     {
-        uint4 *ph = reinterpret_cast<uint4 *>(hi + (size_t)m * ld + i0);
-        uint4 *pl = reinterpret_cast<uint4 *>(lo + (size_t)m * ld + i0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            uint32_t wh[4], wl[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                bf16 h0, l0, h1, l1;
-                split_hilo(h[8 * v + 2 * j], h0, l0);
-                split_hilo(h[8 * v + 2 * j + 1], h1, l1);
-                wh[j] = pack_bf16x2(h0, h1);
-                wl[j] = pack_bf16x2(l0, l1);
-            }
-            ph[v] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            if (lo) pl[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
+        const size_t o = (size_t)m * ld + i0;
+        store_hilo32(hi + o, lo ? lo + o : nullptr, h);
     }
 };
 
 // x[t] += sum over slots s (in order) of w[t][s] * YS[t*K + s]: the selected experts'
-// outputs, after the shared expert's down projection was added by its GEMM.
-// With gnext (H <= 8192): also the next layer's attention RMSNorm of the new row,
-// as BF16 hi/lo into hi, lo (what k_rmsnorm_hilo would write next; lo may be null).
-__global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, const float *wts, int H, int K,
+// outputs (FP32, or BF16 rows widened exactly), after the shared expert's down
+// projection was added by its GEMM.  A thread takes 16 bytes of each slot's row a
+// step (4 FP32 or 8 BF16 values), the slots' loads in flight together.
+// With gnext: also the next layer's attention RMSNorm of the new row, as BF16 hi/lo
+// into hi, lo (what k_rmsnorm_hilo would write next; lo may be null); each thread
+// reads back the residual values it has just written.
+template <typename TY>
+__global__ void __launch_bounds__(256) k_moe_combine(float *X, const TY *YS, const float *wts, int H, int K,
                                                      const float *gnext, float eps, bf16 *nhi, bf16 *nlo)
 {
     pdl_wait();      // inputs of the previous kernel (programmatic launch)
     pdl_trigger();
-    const int t = blockIdx.x;
+    constexpr int VEC = 16 / (int)sizeof(TY);   // values per thread and step
+    const int t = blockIdx.x, step = blockDim.x * VEC;
     float w[8];
 #pragma unroll
     for (int s = 0; s < 8; ++s) w[s] = s < K ? wts[(size_t)t * K + s] : 0.f;
-    float4 xr[8];   // the new row, for the fused RMSNorm
-    for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
-        float4 y[8];
+    float *xrow = X + (size_t)t * H;
+    for (int i = threadIdx.x * VEC; i < H; i += step) {
+        uint4 y[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            if (s < K) y[s] = *reinterpret_cast<const float4 *>(YS + ((size_t)t * K + s) * H + i);
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < K) y[s] = load_row16(YS + ((size_t)t * K + s) * H + i);
+        float r[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) r[k] = 0.f;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            if (s < K) {
-                r.x = fmaf(w[s], y[s].x, r.x);
-                r.y = fmaf(w[s], y[s].y, r.y);
-                r.z = fmaf(w[s], y[s].z, r.z);
-                r.w = fmaf(w[s], y[s].w, r.w);
-            }
-        float4 *x = reinterpret_cast<float4 *>(X + (size_t)t * H + i);
-        const float4 xv = *x;
-        const float4 xn = make_float4(xv.x + r.x, xv.y + r.y, xv.z + r.z, xv.w + r.w);
-        *x = xn;
-        const int u = i / (blockDim.x * 4);
-        if (u < 8) xr[u] = xn;
+            if (s < K) acc_row16(w[s], y[s], r, TY{});
+        float4 *x = reinterpret_cast<float4 *>(xrow + i);
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 xv = x[q];
+            x[q] = make_float4(xv.x + r[4 * q], xv.y + r[4 * q + 1], xv.z + r[4 * q + 2], xv.w + r[4 * q + 3]);
+        }
     }
     if (!gnext) return;
     __shared__ float red[32];
     float ss = 0.f;
+    for (int i = threadIdx.x * VEC; i < H; i += step)
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int i = threadIdx.x * 4 + u * blockDim.x * 4;
-        if (i < H) ss = fmaf(xr[u].x, xr[u].x, fmaf(xr[u].y, xr[u].y, fmaf(xr[u].z, xr[u].z, fmaf(xr[u].w, xr[u].w, ss))));
-    }
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 v = reinterpret_cast<const float4 *>(xrow + i)[q];
+            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        }
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / (float)H + eps);
+    for (int i = threadIdx.x * VEC; i < H; i += step)
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int i = threadIdx.x * 4 + u * blockDim.x * 4;
-        if (i >= H) continue;
-        const float4 gv = *reinterpret_cast<const float4 *>(gnext + i);
-        __align__(8) bf16 h[4], l[4];
-        split_hilo(xr[u].x * inv * gv.x, h[0], l[0]);
-        split_hilo(xr[u].y * inv * gv.y, h[1], l[1]);
-        split_hilo(xr[u].z * inv * gv.z, h[2], l[2]);
-        split_hilo(xr[u].w * inv * gv.w, h[3], l[3]);
-        *reinterpret_cast<uint2 *>(nhi + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(h);
-        if (nlo) *reinterpret_cast<uint2 *>(nlo + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(l);
-    }
+        for (int q = 0; q < VEC / 4; ++q) {
+            const int j = i + 4 * q;
+            const float4 v = *reinterpret_cast<const float4 *>(xrow + j);
+            const float4 gv = *reinterpret_cast<const float4 *>(gnext + j);
+            __align__(8) bf16 h[4], l[4];
+            split_hilo(v.x * inv * gv.x, h[0], l[0]);
+            split_hilo(v.y * inv * gv.y, h[1], l[1]);
+            split_hilo(v.z * inv * gv.z, h[2], l[2]);
+            split_hilo(v.w * inv * gv.w, h[3], l[3]);
+            *reinterpret_cast<uint2 *>(nhi + (size_t)t * H + j) = *reinterpret_cast<const uint2 *>(h);
+            if (nlo) *reinterpret_cast<uint2 *>(nlo + (size_t)t * H + j) = *reinterpret_cast<const uint2 *>(l);
+        }
 }
 
 // ------------------------------------------------------------------ maps and eligibility
@@ -651,6 +738,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         // the normalised input itself), then the shared expert's
         tc::Args g{};
         g.status = pb.status;
+        g.m_tok = n;
         g.n_out = I, g.k = H, g.tiles = pb.tiles, g.off = pb.off;
         g.grow = pb.rows, g.gdiv = K, g.gx_hi = ap.xn_hi, g.gx_lo = ap.xn_lo, g.gld = H;
         if ((e = tc::launch<true, HL>(m.wg, m.wu, am.xn_hi, am.xn_lo, g, EpiSwiGLU{ap.hg_hi, HL ? ap.hg_lo : nullptr, I}, max_tiles,
@@ -663,15 +751,19 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             return e;
         // routed down (grouped) into per-(token, slot) rows; the shared expert's down
         // projection into the residual; then the weighted routed rows, slot order
+        // The routed rows are FP32 with hi/lo activations, else BF16 (each expert's
+        // output rounded once before the weighted sum; half the bytes written and read).
+        using TY = std::conditional_t<HL, float, bf16>;
+        TY *ys = reinterpret_cast<TY *>(pb.YS);
         g.n_out = H, g.k = I;
-        if ((e = tc::launch<false, HL>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H}, max_tiles,
+        if ((e = tc::launch<false, HL>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows<TY>{ys, pb.rows, H, nent, pb.status}, max_tiles,
                                    nsm, st)))
             return e;
         a.n_out = H, a.k = I;
         if ((e = tc::launch<false, HL>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
-        const float *gn = l + 1 < d.L && H <= 8 * 1024 ? layers[l + 1].attn_norm : nullptr;
-        if ((e = launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, st, pb.X, (const float *)pb.YS,
+        const float *gn = l + 1 < d.L ? layers[l + 1].attn_norm : nullptr;
+        if ((e = launch_pdl(k_moe_combine<TY>, dim3(n), dim3(256), 0, st, pb.X, (const TY *)ys,
                             (const float *)pb.wts, H, K, gn, d.eps, ap.xn_hi, HL ? ap.xn_lo : nullptr)))
             return e;
         normed = gn != nullptr;

@@ -27,11 +27,15 @@
 //                   producer and each tile to the epilogue;
 //   warps 2-9       epilogue, overlapping the next tile's MMAs.  Warp w reads TMEM
 //                   lanes 32 (w % 4).. (its 32 tokens) and every other 32-feature
-//                   chunk, stages a chunk as [token][feature] rows in its own
-//                   shared-memory slice and hands the problem's functor four
-//                   adjacent features of one token at a time (so RoPE pairs are
-//                   local to one call); a functor's global loads (load4) are issued
-//                   eight at a time before the stores.
+//                   chunk.  Direct form: each thread hands the problem's functor the
+//                   chunk's 32 adjacent features of its token (RoPE pairs local,
+//                   16-byte stores).  Staged form: the chunk goes through the warp's
+//                   shared-memory rows and the functor gets four adjacent features of
+//                   one token at a time, an instruction covering 4 tokens x 32
+//                   features.  A functor's global loads depend on the tile's
+//                   coordinates only: the first chunk's are issued before the
+//                   accumulator is ready, each later chunk's while the previous chunk
+//                   is stored.
 // Gate/up tiles (GU): the weight tile is 128 gate rows followed by the same 128 up
 // rows, so a feature's gate and up sit in the same TMEM lane, 128 columns apart;
 // SwiGLU is applied straight from the accumulator and each thread writes 32
@@ -58,22 +62,26 @@ static constexpr uint32_t TILE_X = BT * BK * 2;              // 16 KB
 static constexpr uint32_t BOX_BYTES = BOXW * BK * 2;         // 16 KB
 static constexpr int CH = 32;                                // features per epilogue chunk
 static constexpr uint32_t EPI_BYTES = 8 * 32 * CH * 4;       // 32 KB: [8 warps][32 tokens][CH]
-static constexpr int EPI_BATCH = 8;                          // functor loads in flight
+static constexpr int EPI_BATCH = 8;                          // functor loads in flight (staged)
+static constexpr size_t SMEM_MAX = 232448;                   // shared memory a CTA may use (227 KB)
 
-// Tile geometry.  WN weight rows per tile; with the lo token tile (LO), 256 -> 3
-// stages of 64 KB and 128 -> 4 stages of 48 KB; without it, 256 -> 4 stages of 48 KB
-// and 128 -> 6 stages of 32 KB.  Plain tiles add the epilogue's staging rows.
+// Tile geometry.  WN weight rows per tile; the ring takes as many stages as fit in
+// the shared memory beside the staging rows of a staged epilogue (STG), at most 8:
+// with the lo token tile (LO), 256 -> 3 stages of 64 KB and 128 -> 4 of 48 KB;
+// without it, 256 -> 4 of 48 KB and 128 -> 6 of 32 KB (7 without staging).
 // CG = 2 (CTA pairs, WN = 256): each CTA holds one 128-row half of the weight tile,
-// so a stage is 32 KB (48 KB with LO) and 6 (4) stages fit.
-template <bool GU, int WN, bool LO, int CG = 1> struct Geo {
+// so a stage is 32 KB (48 KB with LO) and 6 or 7 (4) stages fit.
+template <bool GU, int WN, bool LO, int CG = 1, bool STG = !GU> struct Geo {
     static_assert(WN == 128 || WN == 256, "weight tile width");
     static_assert(!GU || WN == 256, "gate/up tiles hold 128 gate + 128 up rows");
     static_assert(CG == 1 || WN == 256, "CTA pairs split a 256-row weight tile");
     static constexpr uint32_t TILE_W = WN / CG * BK * 2;             // this CTA's weight rows
     static constexpr uint32_t STAGE = TILE_W + (LO ? 2 : 1) * TILE_X;   // W, X hi[, X lo]
-    static constexpr int STAGES = CG == 2 ? (LO ? 4 : 6) : LO ? (WN == 256 ? 3 : 4) : (WN == 256 ? 4 : 6);
+    static constexpr size_t EPI = STG ? EPI_BYTES : 0;
+    static constexpr int FIT = (int)((SMEM_MAX - 1024 - 256 - EPI) / STAGE);
+    static constexpr int STAGES = FIT < 8 ? FIT : 8;
     static constexpr uint32_t TMEM_COLS = 2 * WN;           // two tiles in flight
-    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (GU ? 0 : EPI_BYTES) + 256;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + EPI + 256;
 };
 
 // What a launch computes.  Dense: token rows [0, m_tok) in tiles of BT.  Grouped
@@ -86,7 +94,7 @@ struct Args {
     int k;            // reduction length, a multiple of BK
     int x_col0;       // first activation column read (a multiple of 8)
     int piece_rows;   // dense: rows of map w0 before map w1 starts (0: w0 only); a multiple of 128
-    int m_tok;        // dense: token rows
+    int m_tok;        // token rows (grouped: the bound of the gathered source rows)
     int ksplit;       // dense, one CTA per tile: the reduction is cut into ksplit equal parts
                       // (0 or 1: none); part s of a tile reaches the functor as e = s
     const int *tiles; // grouped: [0] = count, then (expert, first row) pairs
@@ -108,6 +116,12 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
 }
 
 struct NoAux {};
+template <class Epi, bool GU> struct AuxOf { using type = typename Epi::Aux; };
+template <class Epi> struct AuxOf<Epi, true> { using type = NoAux; };   // gate/up: no functor loads
+// Epilogue form of a (non gate/up) functor: Epi::kDirect selects the per-token form.
+template <class Epi, bool GU> struct DirectOf { static constexpr bool value = Epi::kDirect; };
+template <class Epi> struct DirectOf<Epi, true> { static constexpr bool value = false; };
+template <class Epi, bool GU> __host__ __device__ constexpr bool staged_epi() { return !GU && !DirectOf<Epi, GU>::value; }
 
 // A warp's staging rows: token t's 32 features as 8 float4 groups, group g stored at
 // slot g ^ (t & 7), so that eight threads writing (or reading) the same group of
@@ -125,8 +139,12 @@ __device__ __forceinline__ float4 staged(const float *wstg, int t, int g)
 
 // GU: the tile's gate rows come from w0 and its up rows from w1 (same row index);
 // the epilogue calls Epi::store_row(m, i0, h[32], e) with h = silu(gate) * up of
-// features i0 .. i0 + 31 of token m.  Otherwise Epi provides  Aux load4(m, n, e)
-// and  store4(m, n, v[4], aux, e).
+// features i0 .. i0 + 31 of token m.  Otherwise, with Epi::kDirect, Epi provides
+// Aux load32(m, f0, e) (what the features f0 .. f0 + 31 of token m need from global
+// memory) and store32(m, f0, v[32], aux, e), called by the thread that owns token m;
+// without it, Aux load4(m, n, e) and store4(m, n, v[4], aux, e) for four features,
+// the chunk staged through shared memory so that an instruction covers 4 tokens x 32
+// features (coalesced read-modify-write of the residual, for one).
 // GA (grouped only): the token tiles are gathered row by row from a.gx_hi / a.gx_lo
 // by GWARPS extra warps with 16-byte cp.async copies (the maps xhi, xlo are unused).
 // LO: the activations' lo half takes part (two MMAs per K step); without it the
@@ -147,13 +165,14 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
               const Args a, const Epi epi)
 {
     static_assert(CG == 1 || (CG == 2 && !GA), "CTA pairs: dense GEMMs");
-    using G = Geo<GU, WN, LO, CG>;
+    constexpr bool STG = staged_epi<Epi, GU>();
+    using G = Geo<GU, WN, LO, CG, STG>;
     constexpr int STAGES = G::STAGES;
     constexpr uint32_t STAGE_BYTES = G::STAGE;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // epilogue staging (plain)
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + (GU ? 0 : EPI_BYTES));
+    float *stg = reinterpret_cast<float *>(sm + STAGES * STAGE_BYTES);   // epilogue staging (STG)
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + STAGES * STAGE_BYTES + G::EPI);
     uint64_t *empty = full + STAGES;
     uint64_t *accf = empty + STAGES;   // [2] accumulator ready (MMA commit)
     uint64_t *acce = accf + 2;         // [2] accumulator drained (256 epilogue threads; CG 2: 16 warps)
@@ -163,34 +182,12 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int mtiles = GU ? a.n_out / BOXW : (a.n_out + WN - 1) / WN;
-    const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BT - 1) / BT;
-    // CG 2: a work item is a pair of token tiles; the cluster's CTAs share it.
     // Split reductions (CG 1, dense): ksplit work items per tile, one per part.
     const int ksplit = CG == 1 && !a.tiles && a.ksplit > 1 ? a.ksplit : 1;
-    const int total = mtiles * (CG == 2 ? (ntiles + 1) / 2 : ntiles) * ksplit;
     const int nk = a.k / ksplit / BK;
     const int rank = CG == 2 ? (int)cluster_rank() : 0;
     const bool leader = rank == 0;
     const int first = blockIdx.x / CG, stride = gridDim.x / CG;
-    // tile -> (weight block mb, expert e, first token row r0, end row)
-    auto tile_of = [&](int tau, int &mb, int &e, int &r0, int &rend) {
-        mb = tau % mtiles;
-        const int j = tau / mtiles;
-        if (CG == 2) {
-            e = 0;
-            r0 = (2 * j + rank) * BT;
-            rend = min(r0 + BT, a.m_tok);   // <= r0: no token of this CTA in the tile
-        } else if (a.tiles) {
-            e = a.tiles[1 + 2 * j];
-            r0 = a.tiles[2 + 2 * j];
-            rend = min(r0 + BT, a.off[e + 1]);
-        } else {
-            e = j / ntiles;   // the part of a split reduction (0 without)
-            r0 = (j % ntiles) * BT;
-            rend = min(r0 + BT, a.m_tok);
-        }
-    };
-
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             // TMA, and each gather lane
@@ -214,6 +211,28 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
     // its outputs (this GEMM's inputs) are complete past this point
     pdl_wait();
     pdl_trigger();
+    // The grouped tile list is an output of an earlier kernel: read only past pdl_wait.
+    // CG 2: a work item is a pair of token tiles; the cluster's CTAs share it.
+    const int ntiles = a.tiles ? a.tiles[0] : (a.m_tok + BT - 1) / BT;
+    const int total = mtiles * (CG == 2 ? (ntiles + 1) / 2 : ntiles) * ksplit;
+    // tile -> (weight block mb, expert e, first token row r0, end row)
+    auto tile_of = [&](int tau, int &mb, int &e, int &r0, int &rend) {
+        mb = tau % mtiles;
+        const int j = tau / mtiles;
+        if (CG == 2) {
+            e = 0;
+            r0 = (2 * j + rank) * BT;
+            rend = min(r0 + BT, a.m_tok);   // <= r0: no token of this CTA in the tile
+        } else if (a.tiles) {
+            e = a.tiles[1 + 2 * j];
+            r0 = a.tiles[2 + 2 * j];
+            rend = min(r0 + BT, a.off[e + 1]);
+        } else {
+            e = j / ntiles;   // the part of a split reduction (0 without)
+            r0 = (j % ntiles) * BT;
+            rend = min(r0 + BT, a.m_tok);
+        }
+    };
     const uint32_t tmem = *tslot;
     volatile int *ab = abort_flag;
     auto give_up = [&]() {
@@ -373,6 +392,10 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                 for (int q = 0; q < 16; ++q) {
                     const int r = r0 + 64 * gw + 4 * q + (lane >> 3);
                     src[q] = r < rend ? a.grow[r] / a.gdiv : -1;
+                    if (src[q] >= a.m_tok) {   // not a token of this launch: never copied
+                        atomicCAS(a.status, 0, DS4G_EINVAL);
+                        src[q] = -1;
+                    }
                 }
                 const int col = a.x_col0 + 8 * c;
                 for (int i = 0; i < nk; ++i, ++it) {
@@ -400,11 +423,12 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
         }
     } else {
         // ---------------- epilogue (warps 2-9): warp w reads TMEM lane quarter w % 4
-        // (tokens 32q ..) and takes every other 32-feature chunk of the tile
+        // (tokens 32q ..) and takes every other 32-feature chunk of the tile; each
+        // thread owns one token (its TMEM lane) and hands the functor the chunk's 32
+        // adjacent features of it, so RoPE pairs and 16-byte stores stay in registers
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         const int tok = 32 * q + lane;     // this thread's token row in the tile
-        float *wstg = stg + (warp - 2) * 32 * CH;   // this warp's [32 tokens][CH] staging rows
         // the accumulator is drained: every thread (CG 1), or each warp to the even CTA (CG 2)
         auto drained = [&](int b) {
             tc_fence_before();
@@ -415,21 +439,43 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                 mbar_arrive(&acce[b]);
             }
         };
+        using Aux = typename AuxOf<Epi, GU>::type;
+        // staged form: a batch of the functor's loads for chunk c, items (token, 4 features)
+        auto load_batch = [&](const auto &ep, int mb, int e, int r0, int rend, int c, auto &ax) {
+            const int f0 = mb * WN + c * CH;
+#pragma unroll
+            for (int u = 0; u < EPI_BATCH; ++u) {
+                const int idx = lane + 32 * u;
+                const int t = idx >> 3, j = (idx & 7) * 4, mm = r0 + 32 * q + t;
+                if (mm < rend && f0 + j < a.n_out) ax[u] = ep.load4(mm, f0 + j, e);
+            }
+        };
         unsigned tc = 0;
         for (int tau = first; tau < total; tau += stride, ++tc) {
             int mb, e, r0, rend;
             tile_of(tau, mb, e, r0, rend);
             const int b = tc & 1;
+            const bool wlive = r0 + 32 * q < rend;   // warp-uniform: any token of this warp in the tile
+            const int m = r0 + tok;
+            const bool tlive = m < rend;
+            // The functor's loads depend on the tile's coordinates only: the first chunk's
+            // are issued before the accumulator is ready, each later chunk's while the
+            // previous chunk is stored.
+            Aux aux[2];                       // direct form: per thread and chunk
+            Aux sax[STG ? 2 : 1][EPI_BATCH];  // staged form: per item of a batch
+            if constexpr (STG) {
+                if (wlive) load_batch(epi, mb, e, r0, rend, half, sax[0]);
+            } else if constexpr (!GU) {
+                if (tlive && mb * WN + half * CH < a.n_out) aux[0] = epi.load32(m, mb * WN + half * CH, e);
+            }
             if (!mbar_wait(&accf[b], (tc >> 1) & 1, ab)) {
                 give_up();
                 break;
             }
             tc_fence_after();
-            const bool wlive = r0 + 32 * q < rend;   // warp-uniform: any token of this warp in the tile
             const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * WN);
             if constexpr (GU) {
                 // gate columns c, up columns 128 + c of this thread's token
-                const int m = r0 + tok;
 #pragma unroll 1
                 for (int c0 = 32 * half; c0 < BOXW; c0 += 64) {
                     float g[32], u[32];
@@ -438,46 +484,50 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
                         tmem_ld32(lane_base + (uint32_t)(BOXW + c0), u);
                     }
                     if (c0 + 64 >= BOXW) drained(b);   // this warp's share of the accumulator
-                    if (wlive && m < rend) {
+                    if (wlive && tlive) {
                         float h[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) h[j] = silu_mul(g[j], u[j]);
                         epi.store_row(m, mb * BOXW + c0, h, e);
                     }
                 }
+            } else if constexpr (!STG) {
+                constexpr int NCW = WN / CH / 2;   // chunks per warp: half, half + 2, ...
+#pragma unroll
+                for (int k = 0; k < NCW; ++k) {
+                    const int f0 = mb * WN + (half + 2 * k) * CH;
+                    float v[32];
+                    if (wlive) tmem_ld32(lane_base + (uint32_t)(f0 - mb * WN), v);
+                    if (k == NCW - 1) drained(b);   // this warp's last chunk is read
+                    if (!wlive || !tlive) continue;
+                    if (k + 1 < NCW && f0 + 2 * CH < a.n_out) aux[(k + 1) & 1] = epi.load32(m, f0 + 2 * CH, e);
+                    if (f0 < a.n_out) epi.store32(m, f0, v, aux[k & 1], e);
+                }
             } else {
-#pragma unroll 1
-                for (int c = half; c < WN / CH; c += 2) {
-                    if (c + 2 >= WN / CH) {   // arrive once this warp's last chunk is read
-                        float v[32];
-                        if (wlive) tmem_ld32(lane_base + (uint32_t)(c * CH), v);
-                        drained(b);
-                        if (!wlive) break;
-                        stage_row(wstg, lane, v);
-                    } else {
-                        if (!wlive) continue;
-                        float v[32];
-                        tmem_ld32(lane_base + (uint32_t)(c * CH), v);
-                        stage_row(wstg, lane, v);
-                    }
+                // staged: the chunk goes through this warp's staging rows; an item is (token,
+                // 4 features), an instruction covers 4 tokens x 32 features, and a chunk's
+                // functor loads (eight per thread) are issued one chunk ahead
+                float *wstg = stg + (warp - 2) * 32 * CH;   // this warp's [32 tokens][CH] rows
+                constexpr int NCW = WN / CH / 2;
+#pragma unroll
+                for (int k = 0; k < NCW; ++k) {
+                    const int c = half + 2 * k;
+                    float v[32];
+                    if (wlive) tmem_ld32(lane_base + (uint32_t)(c * CH), v);
+                    if (k == NCW - 1) drained(b);
+                    if (!wlive) continue;
+                    stage_row(wstg, lane, v);
+                    if (k + 1 < NCW) load_batch(epi, mb, e, r0, rend, c + 2, sax[(k + 1) & 1]);
                     __syncwarp();
-                    // (token, 4 features) items: an instruction covers 4 tokens x 32 features
                     const int f0 = mb * WN + c * CH;
-                    typename Epi::Aux aux[EPI_BATCH];
 #pragma unroll
                     for (int u = 0; u < EPI_BATCH; ++u) {
                         const int idx = lane + 32 * u;
-                        const int t = idx >> 3, j = (idx & 7) * 4, m = r0 + 32 * q + t;
-                        if (m < rend && f0 + j < a.n_out) aux[u] = epi.load4(m, f0 + j, e);
-                    }
-#pragma unroll
-                    for (int u = 0; u < EPI_BATCH; ++u) {
-                        const int idx = lane + 32 * u;
-                        const int t = idx >> 3, j = (idx & 7) * 4, m = r0 + 32 * q + t;
-                        if (m >= rend || f0 + j >= a.n_out) continue;
+                        const int t = idx >> 3, j = (idx & 7) * 4, mm = r0 + 32 * q + t;
+                        if (mm >= rend || f0 + j >= a.n_out) continue;
                         const float4 v4 = staged(wstg, t, j >> 2);
-                        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-                        epi.store4(m, f0 + j, v, aux[u], e);
+                        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+                        epi.store4(mm, f0 + j, vv, sax[k & 1][u], e);
                     }
                     __syncwarp();   // the staging rows are rewritten next
                 }
@@ -510,13 +560,13 @@ static cudaError_t launch_wn(const CUtensorMap &w0, const CUtensorMap &w1, const
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<Epi, GU, WN, GA, LO>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Geo<GU, WN, LO>::SMEM);
+                                             (int)Geo<GU, WN, LO, 1, staged_epi<Epi, GU>()>::SMEM);
         if (e) return e;
         attr_set = true;
     }
     const int grid = (int)(work < nsm ? work : nsm);
     return launch_pdl(k_tc_gemm<Epi, GU, WN, GA, LO>, dim3(grid), dim3(GA ? THREADS_GA : THREADS),
-                      Geo<GU, WN, LO>::SMEM, st, w0, w1, xhi, xlo, a, epi);
+                      Geo<GU, WN, LO, 1, staged_epi<Epi, GU>()>::SMEM, st, w0, w1, xhi, xlo, a, epi);
 }
 
 // The CTA-pair form (256-row weight tiles, dense): clusters of 2, as many as can be
@@ -528,7 +578,7 @@ static cudaError_t launch_pair(const CUtensorMap &w0, const CUtensorMap &w1, con
                                cudaStream_t st)
 {
     auto kern = k_tc_gemm<Epi, GU, 256, false, LO, 2>;
-    constexpr size_t smem = Geo<GU, 256, LO, 2>::SMEM;
+    constexpr size_t smem = Geo<GU, 256, LO, 2, staged_epi<Epi, GU>()>::SMEM;
     static int clusters = -1;   // per instantiation: resident clusters of 2
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
