@@ -50,6 +50,7 @@ struct PrefillBufs {
     int *cnt;         // [E] tokens per expert
     int *off;         // [E+1] start of each expert's rows in the grouped order
     int *rows;        // [P*K] grouped order: token * K + slot
+    int *segcnt;      // [ceil(P*K / kSortSeg)][E] per-segment expert counts, then bases
     int *tiles;       // [P*K/16 + E + 1] (expert, first row) work items; tiles[0] = count
     void *HG;         // [P*K][I] routed SwiGLU hidden, grouped order
     void *HS;         // [P][I] shared SwiGLU hidden
@@ -61,6 +62,9 @@ struct PrefillBufs {
     int rec_row[kMaxRec];
     float *rec_dst[kMaxRec];
 };
+// Entries per segment of the counting sort that groups (token, slot) entries by expert.
+static constexpr int kSortSeg = 512;
+static inline size_t sort_segments(size_t nent) { return (nent + kSortSeg - 1) / kSortSeg; }
 // Stable counting sort of pb.ids[0, nent) by expert into pb.rows, with the expert
 // offsets pb.off[E + 1], counts pb.cnt[E] and the tile list pb.tiles (bm rows a tile).
 cudaError_t group_by_expert(const PrefillBufs &pb, int nent, int E, int bm, cudaStream_t st);

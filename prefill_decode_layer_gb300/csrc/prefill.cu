@@ -93,6 +93,26 @@ __global__ void k_router_topk(const float *S, int nparts, size_t part, int *ids,
     }
 }
 
+// Stable grouping of the (token, slot) entries by expert: a counting sort in three
+// passes over segments of kSortSeg entries.  Entry i = token * K + slot; an
+// expert's rows come out in increasing i, so the grouped order depends only on
+// the ids.  Pass 1: per-segment histograms (shared-memory atomics).
+__global__ void __launch_bounds__(256) k_group_hist(const int *ids, int nent, int E, int *segcnt)
+{
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
+    extern __shared__ int hist[];
+    const int seg = blockIdx.x, i0 = seg * kSortSeg, i1 = min(nent, i0 + kSortSeg);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+        const int id = ids[i];
+        if ((unsigned)id < (unsigned)E) atomicAdd(&hist[id], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) segcnt[(size_t)seg * E + e] = hist[e];
+}
+
 // Exclusive scan over the block's threads (blockDim.x a multiple of 32, <= 1024).
 __device__ int block_exclusive_scan(int v, int *tmp, int &total)
 {
@@ -121,119 +141,107 @@ __device__ int block_exclusive_scan(int v, int *tmp, int &total)
     return r;
 }
 
-// Stable grouping of the (token, slot) entries by expert: a counting sort in one CTA
-// of 32 warps.  Entry i = token * K + slot; warp w owns a contiguous range of
-// entries and keeps its per-expert counts, then its bases, in shared memory
-// ([32][E] ints): pass 1 counts, pass 2 (thread e for expert e) turns the counts into
-// bases over the warps, the expert offsets and the tile list (tiles of bm rows that
-// never cross an expert boundary), pass 3 places each warp's entries in index order.
-// An expert's rows come out in increasing i, so the grouped order depends only on
-// the ids.  Lanes holding the same expert find one another with ballots.
-__device__ __forceinline__ void group_ids8(const int *ids, int c, int i1, int lane, int (&v)[8])
-{
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int i = c + 32 * j + lane;
-        v[j] = i < i1 ? ids[i] : -1;
-    }
-}
-// The lanes of the warp whose (valid) id equals this lane's, as a mask: one ballot per
-// bit of the ids (nbits of them), each keeping the lanes that agree on that bit.
-__device__ __forceinline__ unsigned warp_peers(int id, bool ok, int nbits)
-{
-    unsigned m = __ballot_sync(0xffffffffu, ok);
-    for (int b = 0; b < nbits; ++b) {
-        const bool bit = (id >> b) & 1;
-        const unsigned bal = __ballot_sync(0xffffffffu, bit);
-        m &= bit ? bal : ~bal;
-    }
-    return ok ? m : 0u;
-}
-__global__ void __launch_bounds__(1024) k_group_one(const int *ids, int nent, int E, int bm, int *cnt, int *off,
-                                                    int *tiles, int *rows)
+// Pass 2 (one CTA): each expert's count and its segments' exclusive prefixes
+// (segcnt is rewritten in place), the expert offsets, and the (expert, first row)
+// tile list, tiles of bm rows that never cross an expert boundary.  Thread t owns
+// the experts [t * per, (t + 1) * per).
+__global__ void __launch_bounds__(1024) k_group_offsets(int *segcnt, int nseg, int E, int bm, int *cnt, int *off,
+                                                        int *tiles)
 {
     pdl_wait();      // inputs of the previous kernel (programmatic launch)
     pdl_trigger();
-    extern __shared__ int base[];   // [32][E]
     __shared__ int tmp[32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nbits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);   // bits of the largest id
-    const int per = (((nent + 31) / 32) + 31) / 32 * 32;   // entries per warp, a multiple of 32
-    const int i0 = min(nent, warp * per), i1 = min(nent, i0 + per);
-    int *hw = base + warp * E;
-    for (int e = lane; e < E; e += 32) hw[e] = 0;
-    __syncwarp();
-    // pass 1: this warp's counts (shared-memory atomics)
-    for (int c = i0; c < i1; c += 256) {
-        int v[8];
-        group_ids8(ids, c, i1, lane, v);
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+    int rows = 0, ntile = 0;
+    for (int e = e0; e < e1; ++e) {
+        int run = 0;
+        int s = 0;
+        for (; s + 8 <= nseg; s += 8) {   // eight independent loads in flight
+            int c[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if ((unsigned)v[j] < (unsigned)E) atomicAdd(&hw[v[j]], 1);
-    }
-    __syncthreads();
-    // pass 2: expert e's bases over the warps, its offset and tiles
-    const int e = threadIdx.x;
-    int run = 0, ntile = 0;
-    if (e < E) {
-        for (int w = 0; w < 32; ++w) {
-            const int c = base[w * E + e];
-            base[w * E + e] = run;
+            for (int j = 0; j < 8; ++j) c[j] = segcnt[(size_t)(s + j) * E + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                segcnt[(size_t)(s + j) * E + e] = run;
+                run += c[j];
+            }
+        }
+        for (; s < nseg; ++s) {
+            const int c = segcnt[(size_t)s * E + e];
+            segcnt[(size_t)s * E + e] = run;
             run += c;
         }
         cnt[e] = run;
-        ntile = (run + bm - 1) / bm;
+        rows += run;
+        ntile += (run + bm - 1) / bm;
     }
     int nrows, ntiles;
-    const int o = block_exclusive_scan(run, tmp, nrows);
+    int o = block_exclusive_scan(rows, tmp, nrows);
     int t = block_exclusive_scan(ntile, tmp, ntiles);
-    if (e < E) {
+    for (int e = e0; e < e1; ++e) {
+        const int c = cnt[e];
         off[e] = o;
-        for (int r = 0; r < run; r += bm, ++t) {
+        for (int r = 0; r < c; r += bm, ++t) {
             tiles[1 + 2 * t] = e;
             tiles[2 + 2 * t] = o + r;
         }
-        for (int w = 0; w < 32; ++w) base[w * E + e] += o;
+        o += c;
     }
     if (threadIdx.x == 0) {
         off[E] = nrows;
         tiles[0] = ntiles;
     }
-    __syncthreads();
-    // pass 3: place this warp's entries in index order
-    for (int c = i0; c < i1; c += 256) {
-        int v[8];
-        group_ids8(ids, c, i1, lane, v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int i = c + 32 * j + lane;
-            const int id = v[j];
-            const bool ok = (unsigned)id < (unsigned)E;
-            const unsigned peers = warp_peers(ok ? id : 0, ok, nbits);
-            const int rank = __popc(peers & ((1u << lane) - 1u));
-            int b = 0;
-            if (ok) b = hw[id];
-            __syncwarp();
-            if (ok) {
-                rows[b + rank] = i;
-                if (rank == __popc(peers) - 1) hw[id] = b + rank + 1;
-            }
-            __syncwarp();
+}
+
+// Pass 3: one warp per segment places its entries in index order.  Lanes holding
+// the same expert find one another with a match, rank by lane, and the group's
+// last lane advances the expert's running base.
+__global__ void __launch_bounds__(32) k_group_place(const int *ids, int nent, int E, const int *segcnt,
+                                                    const int *off, int *rows)
+{
+    pdl_wait();      // inputs of the previous kernel (programmatic launch)
+    pdl_trigger();
+    extern __shared__ int base[];
+    const int seg = blockIdx.x, lane = threadIdx.x;
+    const int i0 = seg * kSortSeg, i1 = min(nent, i0 + kSortSeg);
+    for (int e = lane; e < E; e += 32) base[e] = off[e] + segcnt[(size_t)seg * E + e];
+    __syncwarp();
+    for (int c = i0; c < i1; c += 32) {
+        const int i = c + lane;
+        int id = i < i1 ? ids[i] : -1;
+        const bool ok = (unsigned)id < (unsigned)E;
+        if (!ok) id = -1 - lane;   // matches no other lane
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int b = 0;
+        if (ok) b = base[id];
+        __syncwarp();
+        if (ok) {
+            rows[b + rank] = i;
+            if (rank == __popc(peers) - 1) base[id] = b + rank + 1;
         }
+        __syncwarp();
     }
 }
 
-static size_t group_smem(int E) { return (size_t)32 * E * sizeof(int); }
-
 cudaError_t group_by_expert(const PrefillBufs &pb, int nent, int E, int bm, cudaStream_t st)
 {
-    if (nent == 0) {
+    const int nseg = (nent + kSortSeg - 1) / kSortSeg;
+    if (nseg == 0) {
         cudaError_t e = cudaMemsetAsync(pb.tiles, 0, sizeof(int), st);
         if (e) return e;
         return cudaMemsetAsync(pb.off, 0, (size_t)(E + 1) * sizeof(int), st);
     }
-    return launch_pdl(k_group_one, dim3(1), dim3(1024), group_smem(E), st, (const int *)pb.ids, nent, E, bm, pb.cnt,
-                      pb.off, pb.tiles, pb.rows);
+    const size_t sh = (size_t)E * sizeof(int);
+    cudaError_t e = launch_pdl(k_group_hist, dim3(nseg), dim3(256), sh, st, (const int *)pb.ids, nent, E, pb.segcnt);
+    const int thr = E >= 1024 ? 1024 : ((E + 31) / 32) * 32;
+    if (!e)
+        e = launch_pdl(k_group_offsets, dim3(1), dim3(thr), 0, st, pb.segcnt, nseg, E, bm, pb.cnt, pb.off, pb.tiles);
+    if (!e)
+        e = launch_pdl(k_group_place, dim3(nseg), dim3(32), sh, st, (const int *)pb.ids, nent, E,
+                       (const int *)pb.segcnt, (const int *)pb.off, pb.rows);
+    return e;
 }
 
 // Windowed causal multi-query attention for a chunk: CTA (token t, group of heads).
@@ -343,6 +351,7 @@ void prefill_carve(const Dims &d, int P, char *base, PrefillBufs &pb)
     pb.cnt = (int *)take((size_t)d.E * 4);
     pb.off = (int *)take((size_t)(d.E + 1) * 4);
     pb.rows = (int *)take(PK * 4);
+    pb.segcnt = (int *)take(sort_segments(PK) * d.E * 4);
     pb.tiles = (int *)take((PK / 16 + d.E + 2) * 2 * 4);
     pb.HG = take(PK * d.I * ta);
     pb.HS = take((size_t)P * d.I * ta);
@@ -366,9 +375,7 @@ static size_t attn_prefill_smem(const Dims &d)
 
 cudaError_t prefill_setup(const Dims &d, int max_smem)
 {
-    cudaError_t e = allow_max_dyn_smem((const void *)k_group_one, max_smem);
-    if (e) return e;
-    e = d.kvdt == DS4G_BF16
+    cudaError_t e = d.kvdt == DS4G_BF16
                         ? allow_max_dyn_smem((const void *)k_attn_prefill<float, bf16>, max_smem)
                         : allow_max_dyn_smem((const void *)k_attn_prefill<float, float>, max_smem);
     if (e) return e;
