@@ -296,9 +296,25 @@ def run_case(args):
         torch.cuda.synchronize()
         assert s.status() == 0
         ms = ev0.elapsed_time(ev1) / max(1, args.steps)
-        print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup,
-                          "launches": int(s.launches), "ms_per_prefill": ms,
-                          "tok_per_s": nt / ms * 1e3}), flush=True)
+        line = {"case": args.case, "steps": args.steps, "warmup": args.warmup,
+                "launches": int(s.launches), "ms_per_prefill": ms, "tok_per_s": nt / ms * 1e3}
+        if args.timeline:
+            # per-launch times: an event after every launch (no overlap between launches)
+            s.set_timing(True)
+            s.timing()
+            for i in range(args.steps):
+                assert s.truncate(0) == 0 and s.prefill(toks) == 0
+            torch.cuda.synchronize()
+            t = {k: v for k, v in s.timing().items() if k.startswith("p_") and v[1] > 0}
+            s.set_timing(False)
+            tot = sum(v[0] for v in t.values())
+            line["timeline"] = {"note": "CUDA event after every launch; us per launch, share of "
+                                        "the evented prefill", "ms_per_prefill_with_events": tot / args.steps,
+                                "per_kind": {k[2:]: {"launches_per_prefill": v[1] / args.steps,
+                                                     "us_per_launch": round(1e3 * v[0] / v[1], 1),
+                                                     "share": round(v[0] / tot, 4)}
+                                             for k, v in sorted(t.items(), key=lambda kv: -kv[1][0])}}
+        print(json.dumps(line), flush=True)
         return
     emb, lm, layers = tw.dev_model(shape)
     m = pdl.Model(shape, emb, lm, layers)
@@ -374,7 +390,8 @@ def main():
                     help="the headline's K timed steps are repeated until the timed region "
                          "lasts about this long")
     ap.add_argument("--timeline", action="store_true",
-                    help="with --case decode-*: also print the kernel's stage start times")
+                    help="with --case decode-*: also print the kernel's stage start times; with "
+                         "--case prefill-*: per-launch times from events after every launch")
     ap.add_argument("--case", default=None, choices=list(CASES),
                     help="run only warmup + steps of one workload (the profiling commands "
                          "recorded in profiles/ use this) and print a one-line summary")

@@ -303,10 +303,12 @@ int ds4g_session_status(ds4g_session *s);
 /* Kernels this session has launched so far (all calls on it). */
 uint64_t ds4g_session_launches(const ds4g_session *s);
 
-/* Tracing: per-kernel timing of decode steps.  While on, decode steps run one
- * kernel per stage, every kernel is bracketed by CUDA events on the session
- * stream and the step synchronises the stream at its end (timing removes the
- * overlap that programmatic dependent launch gives consecutive kernels).  ds4g_session_timing
+/* Tracing: per-kernel timing.  While on, decode steps run one kernel per stage,
+ * every kernel is bracketed by CUDA events on the session stream and the step
+ * synchronises the stream at its end; a tensor-core prefill records an event after
+ * every launch of each chunk, synchronises at the chunk's end and charges each
+ * launch the time since the previous event (timing removes the overlap that
+ * programmatic dependent launch gives consecutive kernels).  ds4g_session_timing
  * copies the accumulated milliseconds and launch counts of each kernel kind
  * (DS4G_K_*) into ms[0..n) and counts[0..n), then resets them. */
 enum {
@@ -318,7 +320,23 @@ enum {
     DS4G_K_EXPERT_GU = 5,  /* routed + shared gate/up with SwiGLU */
     DS4G_K_EXPERT_DOWN = 6,/* down projections + combine + residual */
     DS4G_K_LM_HEAD = 7,
-    DS4G_K_COUNT = 8
+    /* tensor-core prefill ([P3] 阶段三, layer-major) */
+    DS4G_K_P_EMBED = 8,       /* embedding rows */
+    DS4G_K_P_NORM = 9,        /* RMSNorm rows (the first layer's attention norm, every FFN norm) */
+    DS4G_K_P_QKV_A = 10,      /* [W_qa; W_kva] GEMM */
+    DS4G_K_P_Q_B = 11,        /* W_qb GEMM + RoPE */
+    DS4G_K_P_KV_B = 12,       /* [W_kb; W_vb] GEMM + RoPE + K/V append */
+    DS4G_K_P_ATTN = 13,       /* windowed attention */
+    DS4G_K_P_WO = 14,         /* W_o GEMM + residual */
+    DS4G_K_P_ROUTER = 15,     /* router GEMM */
+    DS4G_K_P_TOPK = 16,       /* top-k + softmax of the selected scores */
+    DS4G_K_P_GROUP = 17,      /* grouping of (token, slot) entries by expert */
+    DS4G_K_P_GATE_UP = 18,    /* routed gate/up GEMM + SwiGLU */
+    DS4G_K_P_SHARED_GU = 19,  /* shared expert gate/up GEMM + SwiGLU */
+    DS4G_K_P_DOWN = 20,       /* routed down GEMM */
+    DS4G_K_P_SHARED_DOWN = 21,/* shared expert down GEMM + residual */
+    DS4G_K_P_COMBINE = 22,    /* slot-order combine + the next layer's RMSNorm */
+    DS4G_K_COUNT = 23
 };
 int ds4g_session_set_timing(ds4g_session *s, int on);
 

@@ -58,6 +58,7 @@ struct ds4g_session {
     unsigned done_seq = 0;            // value of the last signal asked for
     bool timing = false;
     cudaEvent_t ev[DS4G_K_COUNT][2];
+    PrefillBufs::Timing *ptm = nullptr;   // timing mode: the prefill's event chain
     double t_ms[DS4G_K_COUNT] = {};
     uint64_t t_n[DS4G_K_COUNT] = {};
 };
@@ -352,11 +353,15 @@ void ds4g_session_destroy(ds4g_session *s)
 {
     if (!s) return;
     if (s->done_h) cudaFreeHost(s->done_h);
-    if (s->timing)
+    if (s->timing) {
+        cudaStreamSynchronize(s->st);
         for (int k = 0; k < DS4G_K_COUNT; ++k) {
             cudaEventDestroy(s->ev[k][0]);
             cudaEventDestroy(s->ev[k][1]);
         }
+        for (int i = 0; i < PrefillBufs::Timing::kMax; ++i) cudaEventDestroy(s->ptm->ev[i]);
+        delete s->ptm;
+    }
     delete s;
 }
 
@@ -396,6 +401,19 @@ int ds4g_prefill(ds4g_session *s, const int32_t *tokens, int n)
                                             s->m->nsm, s->m->hilo)
                          : prefill_chunk(d, s->m->layers.data(), s->kc.data(), s->vc.data(), s->rope,
                                          s->m->tok_embd, s->pb, s->len + c, nc, s->st, s->m->nsm);
+        if (!e && s->ptm && s->ptm->n > 0) {   // timing mode: each launch's share of the chunk
+            PrefillBufs::Timing &tm = *s->ptm;
+            e = cudaEventSynchronize(tm.ev[tm.n - 1]);
+            for (int i = 1; !e && i < tm.n; ++i) {
+                float ms = 0.f;
+                e = cudaEventElapsedTime(&ms, tm.ev[i - 1], tm.ev[i]);
+                if (!e && tm.kind[i] >= 0 && tm.kind[i] < DS4G_K_COUNT) {
+                    s->t_ms[tm.kind[i]] += ms;
+                    s->t_n[tm.kind[i]] += 1;
+                }
+            }
+            tm.n = 0;
+        }
         if (!e && c + nc == n) {  // last token's hidden state, then its logits
             e = cudaMemcpyAsync(s->b.x, s->pb.X + (size_t)(nc - 1) * d.H, (size_t)d.H * 4,
                                 cudaMemcpyDeviceToDevice, s->st);
@@ -826,6 +844,11 @@ int ds4g_session_set_timing(ds4g_session *s, int on)
     if (on && !s->timing) {
         for (int k = 0; k < DS4G_K_COUNT; ++k)
             if (cudaEventCreate(&s->ev[k][0]) || cudaEventCreate(&s->ev[k][1])) return DS4G_ECUDA;
+        s->ptm = new PrefillBufs::Timing();
+        for (int i = 0; i < PrefillBufs::Timing::kMax; ++i)
+            if (cudaEventCreate(&s->ptm->ev[i])) return DS4G_ECUDA;
+        s->ptm->n = 0;
+        s->pb.tm = s->ptm;
         s->timing = true;
     } else if (!on && s->timing) {
         if (cudaStreamSynchronize(s->st)) return DS4G_ECUDA;
@@ -833,6 +856,10 @@ int ds4g_session_set_timing(ds4g_session *s, int on)
             cudaEventDestroy(s->ev[k][0]);
             cudaEventDestroy(s->ev[k][1]);
         }
+        s->pb.tm = nullptr;
+        for (int i = 0; i < PrefillBufs::Timing::kMax; ++i) cudaEventDestroy(s->ptm->ev[i]);
+        delete s->ptm;
+        s->ptm = nullptr;
         s->timing = false;
     }
     return DS4G_OK;

@@ -56,6 +56,14 @@ struct PrefillBufs {
     void *HS;         // [P][I] shared SwiGLU hidden
     float *YS;        // [P*K][H] routed expert outputs, token-slot order
     int *status;      // session status word (set after carving)
+    // Timing mode (tensor-core form): an event after every launch of a chunk, with
+    // the launch's kind (DS4G_K_P_*); ev[0] is recorded at the chunk's start.
+    struct Timing {
+        static constexpr int kMax = 1024;
+        cudaEvent_t ev[kMax];
+        int kind[kMax];
+        int n;
+    } *tm = nullptr;
     // Recorded rows: the residual of chunk row rec_row[i] entering each layer l, then
     // the final hidden state, is copied to rec_dst[i] + l * H ([L+1][H] each).
     int n_rec;

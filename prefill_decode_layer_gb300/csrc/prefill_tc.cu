@@ -621,7 +621,16 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
     const TcActPtrs ap = tc_act_ptrs(d, pb);
     const int ny = (n + tc::BT - 1) / tc::BT;
     const int max_tiles = nent / tc::BT + d.E + 1;
+    // timing mode: an event after every launch, tagged with its kind
+    auto mark = [&](int kind) {
+        PrefillBufs::Timing *tm = pb.tm;
+        if (!tm || tm->n >= PrefillBufs::Timing::kMax) return;
+        cudaEventRecord(tm->ev[tm->n], st);
+        tm->kind[tm->n++] = kind;
+    };
+    mark(-1);
     if ((e = launch_pdl(k_embed_rows, dim3(n), dim3(256), 0, st, tok_embd, (const int *)pb.tok, pb.X, H))) return e;
+        mark(DS4G_K_P_EMBED);
     bool normed = false;   // xn holds the next layer's attention RMSNorm already
     for (int l = 0; l <= d.L; ++l) {
         for (int i = 0; i < pb.n_rec; ++i)
@@ -640,10 +649,12 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             (e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
                             (const float *)w.attn_norm, ap.xn_hi, HL ? ap.xn_lo : nullptr, H, d.eps)))
             return e;
+        if (!normed) mark(DS4G_K_P_NORM);
         a.n_out = d.RQ + d.RKV, a.k = H, a.piece_rows = d.RQ, a.x_col0 = 0;
         if ((e = tc::launch<false, HL>(m.wqa, m.wkva, am.xn_hi, am.xn_lo, a, EpiHiLo{ap.c_hi, HL ? ap.c_lo : nullptr, d.RQ + d.RKV},
                                    ny, nsm, st)))
             return e;
+        mark(DS4G_K_P_QKV_A);
         a.n_out = d.QD, a.k = d.RQ, a.piece_rows = 0, a.x_col0 = 0;
         const bool attn_tc = kvm != nullptr;   // tcgen05 attention: queries as hi/lo BF16
         if (attn_tc) {
@@ -651,14 +662,17 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             if ((e = tc::launch<false, HL>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
                                        EpiQRopeHiLo{q_hi, HL ? q_lo : nullptr, rope, d.QD, d.HD, p0}, ny, nsm, st)))
                 return e;
+            mark(DS4G_K_P_Q_B);
         } else if ((e = tc::launch<false, HL>(m.wqb, m.wqb, am.c_hi, am.c_lo, a,
                                           EpiQRope{(float *)pb.Q, rope, d.QD, d.HD, p0}, ny, nsm, st))) {
             return e;
         }
+        if (!attn_tc) mark(DS4G_K_P_Q_B);
         a.n_out = 2 * d.HD, a.k = d.RKV, a.piece_rows = d.HD, a.x_col0 = d.RQ;
         if ((e = tc::launch<false, HL>(m.wkb, m.wvb, am.c_hi, am.c_lo, a, EpiKVRope<TKV>{kc, vc, rope, d.HD, p0}, ny,
                                    nsm, st)))
             return e;
+        mark(DS4G_K_P_KV_B);
         if (attn_tc) {
             if ((e = attn_prefill_tc(d, am.q_hi, am.q_lo, kvm[l], am.oa_hi, am.oa_lo, p0, n, pb.status, st,
                                      nsm, HL)))
@@ -675,13 +689,16 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         } else if ((e = attn_prefill_hilo<TKV>(d, (const float *)pb.Q, ap.o_hi, ap.o_lo, kc, vc, p0, n, st))) {
             return e;
         }
+        mark(DS4G_K_P_ATTN);
         a.n_out = H, a.k = d.QD, a.piece_rows = 0, a.x_col0 = 0;
         if ((e = tc::launch<false, HL>(m.wo, m.wo, am.o_hi, am.o_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
+        mark(DS4G_K_P_WO);
         // ---- MoE half
         if ((e = launch_pdl(k_rmsnorm_hilo, dim3(n), dim3(rmsnorm_threads(H)), 0, st, (const float *)pb.X,
                             (const float *)w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
             return e;
+        mark(DS4G_K_P_NORM);
         // The router's reduction in fixed parts (twice the tiles on the SMs; the parts'
         // scores are summed in order by the top-k), whatever the chunk.
         const int parts = router_parts(d.E);
@@ -690,11 +707,14 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         if ((e = tc::launch<false, true>(m.wr, m.wr, am.xn_hi, am.xn_lo, a, EpiScores{pb.S, d.E, part}, ny, nsm,
                                          st)))
             return e;
+        mark(DS4G_K_P_ROUTER);
         a.ksplit = 0;
         if ((e = launch_pdl(k_router_topk, dim3((n * 32 + 255) / 256), dim3(256), 0, st, (const float *)pb.S,
                             parts, part, pb.ids, pb.wts, n, d.E, K, pb.status)))
             return e;
+        mark(DS4G_K_P_TOPK);
         if ((e = group_by_expert(pb, nent, d.E, tc::BT, st))) return e;
+        mark(DS4G_K_P_GROUP);
         // routed gate/up + SwiGLU (grouped; the GEMM gathers each group's token rows of
         // the normalised input itself), then the shared expert's
         tc::Args g{};
@@ -705,24 +725,29 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         if ((e = tc::launch<true, HL>(m.wg, m.wu, am.xn_hi, am.xn_lo, g, EpiSwiGLU{ap.hg_hi, HL ? ap.hg_lo : nullptr, I}, max_tiles,
                                   nsm, st)))
             return e;
+        mark(DS4G_K_P_GATE_UP);
         g.grow = nullptr;
         a.n_out = I, a.k = H;
         if ((e = tc::launch<true, HL>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, HL ? ap.hs_lo : nullptr, I}, ny, nsm,
                                   st)))
             return e;
+        mark(DS4G_K_P_SHARED_GU);
         // routed down (grouped) into per-(token, slot) rows; the shared expert's down
         // projection into the residual; then the weighted routed rows, slot order
         g.n_out = H, g.k = I;
         if ((e = tc::launch<false, HL>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H, nent, pb.status},
                                    max_tiles, nsm, st)))
             return e;
+        mark(DS4G_K_P_DOWN);
         a.n_out = H, a.k = I;
         if ((e = tc::launch<false, HL>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
             return e;
+        mark(DS4G_K_P_SHARED_DOWN);
         const float *gn = l + 1 < d.L ? layers[l + 1].attn_norm : nullptr;
         if ((e = launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, st, pb.X, (const float *)pb.YS,
                             (const float *)pb.wts, H, K, gn, d.eps, ap.xn_hi, HL ? ap.xn_lo : nullptr)))
             return e;
+        mark(DS4G_K_P_COMBINE);
         normed = gn != nullptr;
     }
     return cudaGetLastError();

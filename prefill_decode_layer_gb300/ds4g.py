@@ -18,7 +18,9 @@ DEBUG = {"x": 0, "cqkv": 1, "q": 2, "attn": 3, "xmid": 4, "xn2": 5, "scores": 6,
          "hidden": 8, "prefill_x": 9, "status": 10, "prefill_layer_x": 11}
 
 
-KERNEL_KINDS = ("qkv_a", "qkv_b", "attn", "wo", "router", "expert_gu", "expert_down", "lm_head")
+KERNEL_KINDS = ("qkv_a", "qkv_b", "attn", "wo", "router", "expert_gu", "expert_down", "lm_head",
+                "p_embed", "p_norm", "p_qkv_a", "p_q_b", "p_kv_b", "p_attn", "p_wo", "p_router", "p_topk",
+                "p_group", "p_gate_up", "p_shared_gu", "p_down", "p_shared_down", "p_combine")
 
 
 class Ds4gError(RuntimeError):

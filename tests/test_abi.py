@@ -69,3 +69,15 @@ def test_library_loads_and_validates_without_gpu(lib_path):
     assert L.ds4g_checkpoint_bytes(C.byref(c3), -1) == 0
     assert L.ds4g_session_rewrite_from_common(None, None, 0, 0) == pdl.ds4g.EINVAL
     assert L.ds4g_sample_workspace_bytes(129280) > 0
+
+
+def test_timing_kinds_match_the_header():
+    """The binding's kernel-kind names follow the header's DS4G_K_* enumeration, in
+    order, and cover DS4G_K_COUNT entries."""
+    import prefill_decode_layer_gb300 as pdl
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    kinds = {name: int(v) for name, v in re.findall(r"\bDS4G_K_([A-Z_0-9]+)\s*=\s*(\d+)", src)}
+    count = kinds.pop("COUNT")
+    assert sorted(kinds.values()) == list(range(count))
+    names = [n.lower() for n, _ in sorted(kinds.items(), key=lambda kv: kv[1])]
+    assert list(pdl.ds4g.KERNEL_KINDS) == names

@@ -74,3 +74,30 @@ def test_decode_sample_equals_decode_then_sample(model, temperature, top_p):
     assert b.decode_sample(SHAPE.vocab, temperature, top_p, sb, ws_b)[0] == pdl.ds4g.ETOKEN and b.len == n
     if temperature > 0.0:
         assert b.decode_sample(tb, temperature, top_p, 0, ws_b)[0] == pdl.ds4g.EINVAL and b.len == n
+
+
+def test_prefill_timing_mode_counts_launches_and_keeps_results(model):
+    """Timing mode on a tensor-core prefill: every launch is charged to its kind
+    (one per layer and chunk for the per-layer GEMMs), the times are positive, and
+    the K/V rows and logits are those of a prefill without timing, bit for bit."""
+    import torch
+    import prefill_decode_layer_gb300 as pdl
+    prompt = synth.host_tokens(50, SHAPE.vocab, stream=84)
+    a, b = pdl.Session(model, 64), pdl.Session(model, 64)
+    b.set_timing(True)
+    b.timing()
+    assert a.prefill(prompt) == 0 and b.prefill(prompt) == 0
+    t = b.timing()
+    b.set_timing(False)
+    torch.cuda.synchronize()
+    assert torch.equal(a.logits(), b.logits())
+    for l in range(SHAPE.n_layers):
+        for x, y in zip(a.kv(l), b.kv(l)):
+            assert torch.equal(x[:50], y[:50])
+    chunks = -(-50 // model.cfg.prefill_chunk) if model.cfg.prefill_chunk > 0 else 1
+    for kind in ("p_qkv_a", "p_q_b", "p_kv_b", "p_attn", "p_wo", "p_router", "p_topk", "p_group",
+                 "p_gate_up", "p_shared_gu", "p_down", "p_shared_down", "p_combine"):
+        ms, n = t[kind]
+        assert n == SHAPE.n_layers * chunks, (kind, n)
+        assert ms > 0.0, kind
+    assert t["p_embed"][1] == chunks
