@@ -28,7 +28,12 @@
  *    allocated with malloc and freed by the destroy calls.
  *  - Streams: every device operation of a session is issued on the stream
  *    given at ds4g_session_create, in call order.  Calls that return data to the
- *    host (ds4g_sample, ds4g_session_router) synchronise that stream.
+ *    host (ds4g_sample, ds4g_session_router) synchronise that stream.  A session
+ *    of a model with the tensor-core prefill also owns one stream and two events
+ *    of its own (created with the session, destroyed with it): each layer's shared
+ *    expert GEMMs run on that stream, forked from and joined back into the
+ *    session stream within the same ds4g_prefill call, so the ordering the caller
+ *    sees is unchanged.
  *  - Threads: a session has one owner thread ([P1] section 2); the library is not
  *    thread-safe per session.  Different sessions may run on different threads.
  *  - Layouts are row-major [out][in] ("W x" is a dot product of each row with x).
@@ -140,7 +145,8 @@ size_t ds4g_session_bytes(const ds4g_config *cfg, int n_ctx);
 
 /* Lay a session out in dev_mem (256-byte aligned, >= ds4g_session_bytes) and
  * fill its RoPE table on `cuda_stream` (a cudaStream_t; NULL = legacy stream).
- * The session starts empty (len 0).  DS4G_ESIZE if bytes is too small. */
+ * The session starts empty (len 0).  DS4G_ESIZE if bytes is too small; DS4G_ECUDA
+ * if its side stream or events cannot be created (tensor-core prefill). */
 int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes,
                         void *cuda_stream, ds4g_session **out);
 void ds4g_session_destroy(ds4g_session *s);

@@ -266,6 +266,15 @@ size_t ds4g_session_bytes(const ds4g_config *cfg, int n_ctx)
     return layout(*cfg, n_ctx).total;
 }
 
+static void destroy_side(PrefillBufs &pb)
+{
+    if (pb.ev_fork) cudaEventDestroy(pb.ev_fork);
+    if (pb.ev_join) cudaEventDestroy(pb.ev_join);
+    if (pb.side) cudaStreamDestroy(pb.side);
+    pb.side = nullptr;
+    pb.ev_fork = pb.ev_join = nullptr;
+}
+
 int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, void *stream,
                         ds4g_session **out)
 {
@@ -283,6 +292,14 @@ int ds4g_session_create(ds4g_model *m, int n_ctx, void *dev_mem, size_t bytes, v
     s->len = 0;
     s->hist.assign((size_t)n_ctx, 0);
     s->st = static_cast<cudaStream_t>(stream);
+    if (m->tc &&
+        (cudaStreamCreateWithFlags(&s->pb.side, cudaStreamNonBlocking) ||
+         cudaEventCreateWithFlags(&s->pb.ev_fork, cudaEventDisableTiming) ||
+         cudaEventCreateWithFlags(&s->pb.ev_join, cudaEventDisableTiming))) {
+        destroy_side(s->pb);
+        delete s;
+        return DS4G_ECUDA;
+    }
     const size_t kvs = m->cfg.kv_dtype == DS4G_BF16 ? 2 : 4;
     const size_t per = al((size_t)n_ctx * d.HD * kvs);
     for (int l = 0; l < d.L; ++l) {
@@ -353,6 +370,8 @@ void ds4g_session_destroy(ds4g_session *s)
 {
     if (!s) return;
     if (s->done_h) cudaFreeHost(s->done_h);
+    if (s->pb.side) cudaStreamSynchronize(s->pb.side);
+    destroy_side(s->pb);
     if (s->timing) {
         cudaStreamSynchronize(s->st);
         for (int k = 0; k < DS4G_K_COUNT; ++k) {

@@ -56,6 +56,11 @@ struct PrefillBufs {
     void *HS;         // [P][I] shared SwiGLU hidden
     float *YS;        // [P*K][H] routed expert outputs, token-slot order
     int *status;      // session status word (set after carving)
+    // Side stream of the tensor-core form: the shared expert's GEMMs of a layer run
+    // on it, forked after the FFN RMSNorm and joined before the combine (null: all
+    // on the session stream).
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     // Timing mode (tensor-core form): an event after every launch of a chunk, with
     // the launch's kind (DS4G_K_P_*); ev[0] is recorded at the chunk's start.
     struct Timing {

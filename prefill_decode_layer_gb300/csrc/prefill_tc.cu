@@ -699,6 +699,31 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
                             (const float *)w.ffn_norm, ap.xn_hi, ap.xn_lo, H, d.eps)))
             return e;
         mark(DS4G_K_P_NORM);
+        // The shared expert's gate/up and down read only the FFN RMSNorm and write the
+        // residual before the combine: on the side stream they overlap the router, the
+        // top-k, the grouping and the routed GEMMs (not in timing mode).
+        const bool fork = pb.side && !pb.tm;
+        cudaStream_t sst = fork ? pb.side : st;
+        if (fork) {
+            if ((e = cudaEventRecord(pb.ev_fork, st))) return e;
+            if ((e = cudaStreamWaitEvent(pb.side, pb.ev_fork, 0))) return e;
+        }
+        auto shared_gu = [&]() -> cudaError_t {
+            tc::Args sa = a;
+            sa.ksplit = 0, sa.n_out = I, sa.k = H;
+            return tc::launch<true, HL>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, sa,
+                                        EpiSwiGLU{ap.hs_hi, HL ? ap.hs_lo : nullptr, I}, ny, nsm, sst);
+        };
+        auto shared_down = [&]() -> cudaError_t {
+            tc::Args sa = a;
+            sa.ksplit = 0, sa.n_out = H, sa.k = I;
+            return tc::launch<false, HL>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, sa, EpiAddX{pb.X, H}, ny, nsm, sst);
+        };
+        if (fork) {
+            if ((e = shared_gu())) return e;
+            if ((e = shared_down())) return e;
+            if ((e = cudaEventRecord(pb.ev_join, pb.side))) return e;
+        }
         // The router's reduction in fixed parts (twice the tiles on the SMs; the parts'
         // scores are summed in order by the top-k), whatever the chunk.
         const int parts = router_parts(d.E);
@@ -727,11 +752,10 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             return e;
         mark(DS4G_K_P_GATE_UP);
         g.grow = nullptr;
-        a.n_out = I, a.k = H;
-        if ((e = tc::launch<true, HL>(m.wsg, m.wsu, am.xn_hi, am.xn_lo, a, EpiSwiGLU{ap.hs_hi, HL ? ap.hs_lo : nullptr, I}, ny, nsm,
-                                  st)))
-            return e;
-        mark(DS4G_K_P_SHARED_GU);
+        if (!fork) {
+            if ((e = shared_gu())) return e;
+            mark(DS4G_K_P_SHARED_GU);
+        }
         // routed down (grouped) into per-(token, slot) rows; the shared expert's down
         // projection into the residual; then the weighted routed rows, slot order
         g.n_out = H, g.k = I;
@@ -739,10 +763,12 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
                                    max_tiles, nsm, st)))
             return e;
         mark(DS4G_K_P_DOWN);
-        a.n_out = H, a.k = I;
-        if ((e = tc::launch<false, HL>(m.wsd, m.wsd, am.hs_hi, am.hs_lo, a, EpiAddX{pb.X, H}, ny, nsm, st)))
+        if (!fork) {
+            if ((e = shared_down())) return e;
+            mark(DS4G_K_P_SHARED_DOWN);
+        } else if ((e = cudaStreamWaitEvent(st, pb.ev_join, 0))) {
             return e;
-        mark(DS4G_K_P_SHARED_DOWN);
+        }
         const float *gn = l + 1 < d.L ? layers[l + 1].attn_norm : nullptr;
         if ((e = launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, st, pb.X, (const float *)pb.YS,
                             (const float *)pb.wts, H, K, gn, d.eps, ap.xn_hi, HL ? ap.xn_lo : nullptr)))
