@@ -861,13 +861,40 @@ int ds4g_session_set_timing(ds4g_session *s, int on)
 {
     if (!s) return DS4G_EINVAL;
     if (on && !s->timing) {
-        for (int k = 0; k < DS4G_K_COUNT; ++k)
-            if (cudaEventCreate(&s->ev[k][0]) || cudaEventCreate(&s->ev[k][1])) return DS4G_ECUDA;
-        s->ptm = new PrefillBufs::Timing();
-        for (int i = 0; i < PrefillBufs::Timing::kMax; ++i)
-            if (cudaEventCreate(&s->ptm->ev[i])) return DS4G_ECUDA;
-        s->ptm->n = 0;
-        s->pb.tm = s->ptm;
+        // all events, or none (a failure destroys the ones already created)
+        PrefillBufs::Timing *tm = new (std::nothrow) PrefillBufs::Timing();
+        if (!tm) return DS4G_ECUDA;
+        bool ok = true;
+        int ke = 0;   // kinds whose two events exist
+        for (; ke < DS4G_K_COUNT; ++ke) {
+            if (cudaEventCreate(&s->ev[ke][0])) {
+                ok = false;
+                break;
+            }
+            if (cudaEventCreate(&s->ev[ke][1])) {
+                cudaEventDestroy(s->ev[ke][0]);
+                ok = false;
+                break;
+            }
+        }
+        int pe = 0;   // prefill events that exist
+        for (; ok && pe < PrefillBufs::Timing::kMax; ++pe)
+            if (cudaEventCreate(&tm->ev[pe])) {
+                ok = false;
+                break;
+            }
+        if (!ok) {
+            for (int i = 0; i < pe; ++i) cudaEventDestroy(tm->ev[i]);
+            for (int k = 0; k < ke; ++k) {
+                cudaEventDestroy(s->ev[k][0]);
+                cudaEventDestroy(s->ev[k][1]);
+            }
+            delete tm;
+            return DS4G_ECUDA;
+        }
+        tm->n = 0;
+        s->ptm = tm;
+        s->pb.tm = tm;
         s->timing = true;
     } else if (!on && s->timing) {
         if (cudaStreamSynchronize(s->st)) return DS4G_ECUDA;

@@ -391,10 +391,11 @@ __global__ void __launch_bounds__(GA ? THREADS_GA : THREADS, 1)
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                     const int r = r0 + 64 * gw + 4 * q + (lane >> 3);
-                    src[q] = r < rend ? a.grow[r] / a.gdiv : -1;
-                    if (src[q] >= a.m_tok) {   // not a token of this launch: never copied
-                        atomicCAS(a.status, 0, DS4G_EINVAL);
-                        src[q] = -1;
+                    src[q] = -1;
+                    if (r < rend) {
+                        const int v = a.grow[r] / a.gdiv;
+                        if ((unsigned)v < (unsigned)a.m_tok) src[q] = v;
+                        else atomicCAS(a.status, 0, DS4G_EINVAL);   // not a token of this launch: never copied
                     }
                 }
                 const int col = a.x_col0 + 8 * c;
