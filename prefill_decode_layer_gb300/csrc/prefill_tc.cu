@@ -455,8 +455,36 @@ struct EpiScores {   // router scores of reduction part s: S[s][m][n..n+3] in FP
     }
 };
 
-struct EpiRoutedRows {   // routed expert output of grouped row m into its (token, slot) row
-    float *YS;
+// Per-slot routed rows: 4 consecutive values as FP32 or BF16 (RNE); acc_row16 adds w
+// times the values of 16 bytes of a row (4 FP32 or 8 BF16, widened exactly) to r.
+__device__ __forceinline__ void store_row4(float *p, const float (&v)[4])
+{
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store_row4(bf16 *p, const float (&v)[4])
+{
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(__float2bfloat16_rn(v[0]), __float2bfloat16_rn(v[1])),
+                                               pack_bf16x2(__float2bfloat16_rn(v[2]), __float2bfloat16_rn(v[3])));
+}
+__device__ __forceinline__ void acc_row16(float w, const uint4 &q, float (&r)[4], float)
+{
+    r[0] = fmaf(w, __uint_as_float(q.x), r[0]);
+    r[1] = fmaf(w, __uint_as_float(q.y), r[1]);
+    r[2] = fmaf(w, __uint_as_float(q.z), r[2]);
+    r[3] = fmaf(w, __uint_as_float(q.w), r[3]);
+}
+__device__ __forceinline__ void acc_row16(float w, const uint4 &q, float (&r)[8], bf16)
+{
+    const uint32_t a[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        r[2 * j] = fmaf(w, __uint_as_float(a[j] << 16), r[2 * j]);
+        r[2 * j + 1] = fmaf(w, __uint_as_float(a[j] & 0xffff0000u), r[2 * j + 1]);
+    }
+}
+template <typename TY>
+struct EpiRoutedRows {   // routed expert output of grouped row m into its (token, slot) row (FP32 or BF16)
+    TY *YS;
     const int *rows;
     int H;
     int nrows;     // (token, slot) rows of the launch: a row index outside is never written
@@ -470,7 +498,7 @@ struct EpiRoutedRows {   // routed expert output of grouped row m into its (toke
             atomicCAS(status, 0, DS4G_EINVAL);
             return;
         }
-        *reinterpret_cast<float4 *>(YS + (size_t)r * H + n) = make_float4(v[0], v[1], v[2], v[3]);
+        store_row4(YS + (size_t)r * H + n, v);
     }
 };
 
@@ -485,59 +513,67 @@ struct EpiSwiGLU {   // h[m][i0 .. i0+31] = silu(gate) * up as hi/lo BF16 (lo ma
 };
 
 // x[t] += sum over slots s (in order) of w[t][s] * YS[t*K + s]: the selected experts'
-// outputs, after the shared expert's down projection was added by its GEMM.  A
-// thread takes 4 values of each slot's row a step, the slots' loads in flight
-// together.  With gnext: also the next layer's attention RMSNorm of the new row, as
-// BF16 hi/lo into hi, lo (what k_rmsnorm_hilo would write next; lo may be null);
-// each thread reads back the residual values it has just written.
-__global__ void __launch_bounds__(256) k_moe_combine(float *X, const float *YS, const float *wts, int H, int K,
+// outputs (FP32, or BF16 rows widened exactly), after the shared expert's down
+// projection was added by its GEMM.  A thread takes 16 bytes of each slot's row a
+// step (4 FP32 or 8 BF16 values), the slots' loads in flight together.  With gnext:
+// also the next layer's attention RMSNorm of the new row, as BF16 hi/lo into hi, lo
+// (what k_rmsnorm_hilo would write next; lo may be null); each thread reads back the
+// residual values it has just written.
+template <typename TY>
+__global__ void __launch_bounds__(256) k_moe_combine(float *X, const TY *YS, const float *wts, int H, int K,
                                                      const float *gnext, float eps, bf16 *nhi, bf16 *nlo)
 {
     pdl_wait();      // inputs of the previous kernel (programmatic launch)
     pdl_trigger();
-    const int t = blockIdx.x, step = blockDim.x * 4;
+    constexpr int VEC = 16 / (int)sizeof(TY);   // values per thread and step
+    const int t = blockIdx.x, step = blockDim.x * VEC;
     float w[8];
 #pragma unroll
     for (int s = 0; s < 8; ++s) w[s] = s < K ? wts[(size_t)t * K + s] : 0.f;
     float *xrow = X + (size_t)t * H;
-    for (int i = threadIdx.x * 4; i < H; i += step) {
-        float4 y[8];
+    for (int i = threadIdx.x * VEC; i < H; i += step) {
+        uint4 y[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            if (s < K) y[s] = *reinterpret_cast<const float4 *>(YS + ((size_t)t * K + s) * H + i);
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < K) y[s] = *reinterpret_cast<const uint4 *>(YS + ((size_t)t * K + s) * H + i);
+        float r[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) r[k] = 0.f;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            if (s < K) {
-                r.x = fmaf(w[s], y[s].x, r.x);
-                r.y = fmaf(w[s], y[s].y, r.y);
-                r.z = fmaf(w[s], y[s].z, r.z);
-                r.w = fmaf(w[s], y[s].w, r.w);
-            }
+            if (s < K) acc_row16(w[s], y[s], r, TY{});
         float4 *x = reinterpret_cast<float4 *>(xrow + i);
-        const float4 xv = *x;
-        *x = make_float4(xv.x + r.x, xv.y + r.y, xv.z + r.z, xv.w + r.w);
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 xv = x[q];
+            x[q] = make_float4(xv.x + r[4 * q], xv.y + r[4 * q + 1], xv.z + r[4 * q + 2], xv.w + r[4 * q + 3]);
+        }
     }
     if (!gnext) return;
     __shared__ float red[32];
     float ss = 0.f;
-    for (int i = threadIdx.x * 4; i < H; i += step) {
-        const float4 v = *reinterpret_cast<const float4 *>(xrow + i);
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-    }
+    for (int i = threadIdx.x * VEC; i < H; i += step)
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 v = reinterpret_cast<const float4 *>(xrow + i)[q];
+            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        }
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / (float)H + eps);
-    for (int i = threadIdx.x * 4; i < H; i += step) {
-        const float4 v = *reinterpret_cast<const float4 *>(xrow + i);
-        const float4 gv = *reinterpret_cast<const float4 *>(gnext + i);
-        __align__(8) bf16 h[4], l[4];
-        split_hilo(v.x * inv * gv.x, h[0], l[0]);
-        split_hilo(v.y * inv * gv.y, h[1], l[1]);
-        split_hilo(v.z * inv * gv.z, h[2], l[2]);
-        split_hilo(v.w * inv * gv.w, h[3], l[3]);
-        *reinterpret_cast<uint2 *>(nhi + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(h);
-        if (nlo) *reinterpret_cast<uint2 *>(nlo + (size_t)t * H + i) = *reinterpret_cast<const uint2 *>(l);
-    }
+    for (int i = threadIdx.x * VEC; i < H; i += step)
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const int j = i + 4 * q;
+            const float4 v = *reinterpret_cast<const float4 *>(xrow + j);
+            const float4 gv = *reinterpret_cast<const float4 *>(gnext + j);
+            __align__(8) bf16 h[4], l[4];
+            split_hilo(v.x * inv * gv.x, h[0], l[0]);
+            split_hilo(v.y * inv * gv.y, h[1], l[1]);
+            split_hilo(v.z * inv * gv.z, h[2], l[2]);
+            split_hilo(v.w * inv * gv.w, h[3], l[3]);
+            *reinterpret_cast<uint2 *>(nhi + (size_t)t * H + j) = *reinterpret_cast<const uint2 *>(h);
+            if (nlo) *reinterpret_cast<uint2 *>(nlo + (size_t)t * H + j) = *reinterpret_cast<const uint2 *>(l);
+        }
 }
 
 // ------------------------------------------------------------------ maps and eligibility
@@ -760,8 +796,13 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
         }
         // routed down (grouped) into per-(token, slot) rows; the shared expert's down
         // projection into the residual; then the weighted routed rows, slot order
+        // The routed rows are FP32 with hi/lo activations, else BF16: each expert's
+        // output is rounded once before the fixed-order weighted sum, and the down GEMM
+        // writes and the combine reads half the bytes.
+        using TY = std::conditional_t<HL, float, bf16>;
+        TY *ys = reinterpret_cast<TY *>(pb.YS);
         g.n_out = H, g.k = I;
-        if ((e = tc::launch<false, HL>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows{pb.YS, pb.rows, H, nent, pb.status},
+        if ((e = tc::launch<false, HL>(m.wd, m.wd, am.hg_hi, am.hg_lo, g, EpiRoutedRows<TY>{ys, pb.rows, H, nent, pb.status},
                                    max_tiles, nsm, st)))
             return e;
         mark(DS4G_K_P_DOWN);
@@ -772,7 +813,7 @@ static cudaError_t chunk_tc_t(const Dims &d, const LayerPtrs *layers, const TcLa
             return e;
         }
         const float *gn = l + 1 < d.L ? layers[l + 1].attn_norm : nullptr;
-        if ((e = launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, st, pb.X, (const float *)pb.YS,
+        if ((e = launch_pdl(k_moe_combine<TY>, dim3(n), dim3(256), 0, st, pb.X, (const TY *)ys,
                             (const float *)pb.wts, H, K, gn, d.eps, ap.xn_hi, HL ? ap.xn_lo : nullptr)))
             return e;
         mark(DS4G_K_P_COMBINE);
