@@ -4,12 +4,12 @@
 //
 // Same steps, order and fixed reductions as the SIMT form in prefill.cu, with every
 // weight contraction a tcgen05 GEMM (tc_gemm.cuh).  Activations entering a GEMM are
-// stored as BF16 hi/lo pairs; the residual, the queries and the router scores stay
-// FP32.  The buffers are those of the SIMT form: an FP32-sized buffer holds exactly
-// one hi and one lo BF16 array, and the grouped copy of the MoE input (needed only
-// by the routed gate/up GEMM) lives in the routed-output buffer, which is written
-// only afterwards.  Weight tensor maps are built once per model, activation maps
-// once per session.
+// BF16 (the router's input a BF16 hi/lo pair; every activation a pair in the hi/lo
+// mode); the residual and the router scores stay FP32, the routed experts' per-slot
+// rows are BF16 (FP32 in the hi/lo mode).  The buffers are those of the SIMT form:
+// an FP32-sized buffer holds exactly one hi and one lo BF16 array.  The shared
+// expert's GEMMs run on the session's side stream.  Weight tensor maps are built
+// once per model, activation maps once per session.
 #include <type_traits>
 
 #include "kernels.h"
